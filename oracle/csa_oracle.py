@@ -1,0 +1,321 @@
+"""fp64 CPU oracle of the Compressed Sparse Attention (CSA) hot path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product imports this module: only
+the tests, the smoke check of ``__graft_entry__`` and the CPU-baseline leg of
+``bench.py`` may call it.  It shares no code with the CUDA library (no
+helpers, tables or constants); both sides only share the seeded input
+generator, which computes none of the method's arithmetic.
+
+Every function is the plain definition written out in float64 with numpy,
+one query row at a time, in the order the pages describe the step.  Inputs
+are read as stored (bf16 values widen exactly to float64).  Sources, by
+page title and section:
+
+* "Add unfused SBHD compressed sparse attention" (Megatron-LM PR #6400):
+  compressor review (softmax-weighted pooling in fp32, cast once),
+  causal compressed mask (block j visible to token t iff j < (t+1)//ratio),
+  indexer/top-k block (k = min(index_topk, n_compressed), validity + offset,
+  -1 padding), review of the gather backward (compact [b*n_kv, hn] KV buffer,
+  index_add backward, repeated indices), attention-sink parameter (per-head
+  fp32 logit), softmax_scale default v_head_dim**-0.5.
+* "Refactor Deepseek v4 to use Attention Gym's Compressed Sparse Attention"
+  (torchtitan PR #4452): one softmax over window + selected compressed
+  entries + sink, returning the per-head LSE (the sink is in the
+  denominator, contributes no value).
+* "Add the min-memory DSA attention kernels" (Megatron-LM PR #7152): exact
+  ties after ReLU are common and routing must be tie-exact with one full
+  top-k; the selected support is sorted by position; repeated keys
+  accumulate their gradients in fp32.
+
+Readings where the pages are silent (each one is listed with its reason in
+the design notes of the repository):
+  * window of query t = raw rows {t-W+1, ..., t} (its own token included);
+  * KV row order = raw rows 0..sq-1 then compressed rows sq..sq+n_c-1;
+  * tokens past the last complete block are never pooled;
+  * top-k ties go to the lower block index; output ascending, -1 tail;
+  * an index j is padding when j < 0, j >= n_c or j >= vis(t);
+  * a repeated index is two separate softmax terms;
+  * LSE = natural log including the sink; sink absent = -inf.
+
+All functions take and return numpy arrays; floating results are float64.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "round_to_storage", "round_bf16",
+    "visible_blocks", "compress", "compress_bwd",
+    "indexer_scores", "indexer_scores_row", "topk_select", "topk_select_row",
+    "query_slots", "attn_fwd_query", "attn_fwd", "attn_bwd_query", "attn_bwd",
+]
+
+
+# ---------------------------------------------------------------------------
+# Storage rounding (the one cast of the pooled result and of O)
+# ---------------------------------------------------------------------------
+
+def round_bf16(x):
+    """Round float64 values to the nearest bfloat16 value, ties to even.
+
+    bfloat16 keeps 8 significant bits; the value m * 2**e (0.5 <= |m| < 1) is
+    rounded at 2**(e-8).  Values below the smallest normal (2**-126) round on
+    the fixed subnormal grid 2**-133.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    step = np.ldexp(1.0, e - 8)
+    return np.round(x / step) * step
+
+
+def round_to_storage(x, dtype: str):
+    """The single cast to the storage dtype ('fp32' or 'bf16'), as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    if dtype == "fp32":
+        return x.astype(np.float32).astype(np.float64)
+    if dtype == "bf16":
+        return round_bf16(x)
+    if dtype == "fp64":
+        return x
+    raise ValueError(dtype)
+
+
+# ---------------------------------------------------------------------------
+# Step 1: compressor (softmax-weighted pooling of `ratio` consecutive tokens)
+# ---------------------------------------------------------------------------
+
+def visible_blocks(t: int, ratio: int) -> int:
+    """vis(t): compressed blocks visible to token t (0-based) = (t+1)//ratio.
+
+    PR #6400 builds the mask from positions = arange(1, sq+1) and marks block
+    j invalid where j >= positions // ratio.
+    """
+    return (t + 1) // ratio
+
+
+def compress(kv, score, ratio: int, out_dtype: str = "fp64"):
+    """Pool each block of `ratio` consecutive tokens.
+
+    kv    [b, sq, d]   raw KV rows
+    score [b, sq, d_s] pooling scores, d_s in {1, d} (d_s = 1 broadcasts)
+    returns kv_c [b, n_c, d], n_c = sq // ratio, rounded once to out_dtype.
+
+    Per block j and channel c: weights = softmax over the block's tokens of
+    score[., c]; kv_c[j, c] = sum_t weights_t * kv[t, c].  The pages keep the
+    weights, the products and the sum in fp32 and cast once (compressor
+    review of PR #6400); the oracle does the same in fp64.
+    """
+    kv = np.asarray(kv, np.float64)
+    score = np.asarray(score, np.float64)
+    b, sq, d = kv.shape
+    n_c = sq // ratio
+    out = np.zeros((b, n_c, d))
+    for bi in range(b):
+        for j in range(n_c):
+            rows = slice(j * ratio, (j + 1) * ratio)
+            s = score[bi, rows]                     # [ratio, d_s]
+            s = s - s.max(axis=0, keepdims=True)
+            e = np.exp(s)
+            weights = e / e.sum(axis=0, keepdims=True)
+            out[bi, j] = (weights * kv[bi, rows]).sum(axis=0)
+    return round_to_storage(out, out_dtype)
+
+
+def compress_bwd(kv, score, ratio: int, g):
+    """Gradient of the pooling (unrounded) w.r.t. kv and score.
+
+    g [b, n_c, d] = dL/dkv_c.  With weights w_t of a block and channel:
+      dkv_t   = w_t * g
+      dscore_t = w_t * (g*kv_t - sum_t' w_t' * g*kv_t')
+    Tokens past the last complete block get zero gradient.  A d_s = 1 score
+    sums its per-channel gradient over channels.
+    """
+    kv = np.asarray(kv, np.float64)
+    score = np.asarray(score, np.float64)
+    g = np.asarray(g, np.float64)
+    b, sq, d = kv.shape
+    d_s = score.shape[2]
+    n_c = sq // ratio
+    dkv = np.zeros_like(kv)
+    dscore = np.zeros_like(score)
+    for bi in range(b):
+        for j in range(n_c):
+            rows = slice(j * ratio, (j + 1) * ratio)
+            s = score[bi, rows]
+            s = s - s.max(axis=0, keepdims=True)
+            e = np.exp(s)
+            weights = np.broadcast_to(e / e.sum(axis=0, keepdims=True), (ratio, d))
+            dkv[bi, rows] = weights * g[bi, j]
+            gk = g[bi, j] * kv[bi, rows]                      # [ratio, d]
+            ds = weights * (gk - (weights * gk).sum(axis=0, keepdims=True))
+            dscore[bi, rows] = ds if d_s == d else ds.sum(axis=1, keepdims=True)
+    return dkv, dscore
+
+
+# ---------------------------------------------------------------------------
+# Steps 2-3: lightning indexer and causal top-k
+# ---------------------------------------------------------------------------
+
+def indexer_scores_row(q_I_t, k_I_b, w_t, t: int, ratio: int):
+    """I[t, j] = sum_h w[t,h] * max(0, q_I[t,h,:] . k_I[j,:]) for j < vis(t).
+
+    q_I_t [H_I, d_I], k_I_b [n_c, d_I], w_t [H_I]; returns a length-vis
+    float64 vector (the visible prefix of the row).
+    """
+    v = min(visible_blocks(t, ratio), k_I_b.shape[0])
+    if v == 0:
+        return np.zeros(0)
+    dots = np.asarray(q_I_t, np.float64) @ np.asarray(k_I_b[:v], np.float64).T   # [H_I, v]
+    return np.asarray(w_t, np.float64) @ np.maximum(dots, 0.0)
+
+
+def indexer_scores(q_I, k_I, w, ratio: int):
+    """Full score matrix [b, sq, n_c]; entries with j >= vis(t) are -inf."""
+    b, sq = q_I.shape[:2]
+    n_c = k_I.shape[1]
+    out = np.full((b, sq, n_c), -np.inf)
+    for bi in range(b):
+        for t in range(sq):
+            row = indexer_scores_row(q_I[bi, t], k_I[bi], w[bi, t], t, ratio)
+            out[bi, t, :row.shape[0]] = row
+    return out
+
+
+def topk_select_row(scores_vis, K: int):
+    """Top-K of one row's visible scores.
+
+    Sort the (score, j) pairs by score descending, then j ascending (ties go
+    to the lower block index), keep the first min(K, vis), and return them in
+    ascending j (support sorted by position) padded with -1 to length K.
+    """
+    v = scores_vis.shape[0]
+    order = np.lexsort((np.arange(v), -np.asarray(scores_vis, np.float64)))
+    sel = np.sort(order[:min(K, v)])
+    out = np.full(K, -1, np.int32)
+    out[:sel.shape[0]] = sel
+    return out
+
+
+def topk_select(scores, K: int):
+    """Apply topk_select_row to every row of a [b, sq, n_c] matrix whose
+    non-visible entries are -inf."""
+    b, sq, n_c = scores.shape
+    out = np.full((b, sq, K), -1, np.int32)
+    for bi in range(b):
+        for t in range(sq):
+            row = scores[bi, t]
+            v = int(np.isfinite(row).sum())
+            out[bi, t] = topk_select_row(row[:v], K)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Steps 4-5: sparse MQA over window + selected compressed rows + sink
+# ---------------------------------------------------------------------------
+
+def query_slots(t: int, idx_row, sq: int, n_c: int, ratio: int, window: int):
+    """KV rows that query t attends to, in the flat [n_kv] row space.
+
+    Window: raw rows max(0, t-window+1) .. t.  Compressed: row sq + j for every
+    entry j of the index row with 0 <= j < n_c and j < vis(t); other entries
+    are padding.  A repeated entry yields a repeated row (two terms).
+    """
+    raw = list(range(max(0, t - window + 1), t + 1))
+    vis = visible_blocks(t, ratio)
+    comp = [sq + int(j) for j in idx_row if 0 <= int(j) < n_c and int(j) < vis]
+    return np.asarray(raw + comp, dtype=np.int64)
+
+
+def _sink_vec(sink, H):
+    if sink is None:
+        return np.full(H, -np.inf)
+    return np.asarray(sink, np.float64)
+
+
+def attn_fwd_query(q_t, kv_b, slots, sink_h, scale: float):
+    """One query, all heads.
+
+    s_i = scale * q_h . kv_i; LSE_h = log(exp(sink_h) + sum_i exp(s_i));
+    O_h = sum_i exp(s_i - LSE_h) * kv_i.  The sink only enters the
+    denominator.  Returns (O [H,d], LSE [H], P [H,S], gathered rows [S,d]).
+    """
+    kvg = np.asarray(kv_b, np.float64)[slots]
+    s = scale * (np.asarray(q_t, np.float64) @ kvg.T)
+    m = np.maximum(s.max(axis=1), sink_h)
+    e = np.exp(s - m[:, None])
+    z = e.sum(axis=1) + np.exp(sink_h - m)
+    lse = m + np.log(z)
+    p = e / z[:, None]
+    return p @ kvg, lse, p, kvg
+
+
+def attn_fwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int,
+             rows=None, out_dtype: str = "fp64"):
+    """O [b, sq, H, d] (rounded once to out_dtype) and LSE [b, sq, H].
+
+    ``rows``: optional list of (b, t) pairs; only those rows are computed and
+    the results come back as arrays of shape [len(rows), H, d] / [len(rows), H].
+    """
+    b, sq, H, d = q.shape
+    n_c = kv_full.shape[1] - sq
+    sink_h = _sink_vec(sink, H)
+    pairs = rows if rows is not None else [(bi, t) for bi in range(b) for t in range(sq)]
+    O = np.zeros((len(pairs), H, d))
+    L = np.zeros((len(pairs), H))
+    for n, (bi, t) in enumerate(pairs):
+        slots = query_slots(t, idx[bi, t], sq, n_c, ratio, window)
+        o, lse, _, _ = attn_fwd_query(q[bi, t], kv_full[bi], slots, sink_h, scale)
+        O[n], L[n] = o, lse
+    O = round_to_storage(O, out_dtype)
+    if rows is None:
+        return O.reshape(b, sq, H, d), L.reshape(b, sq, H)
+    return O, L
+
+
+def attn_bwd_query(q_t, kv_b, slots, sink_h, scale: float, dO_t):
+    """Exact gradients of L = sum_h dO_h . O_h for one query.
+
+    D_h = dO_h . O_h;  p_i = exp(s_i - LSE);  ds_i = p_i (dO_h . kv_i - D_h);
+    dq_h = scale * sum_i ds_i kv_i;  per slot: dkv_i = sum_h (p_i dO_h + scale ds_i q_h);
+    dsink_h = -exp(sink_h - LSE_h) * D_h.
+    Returns (dq [H,d], per-slot dkv contributions [S,d], dsink [H]).
+    """
+    o, lse, p, kvg = attn_fwd_query(q_t, kv_b, slots, sink_h, scale)
+    dO_t = np.asarray(dO_t, np.float64)
+    q_t = np.asarray(q_t, np.float64)
+    D = (dO_t * o).sum(axis=1)
+    dp = dO_t @ kvg.T
+    ds = p * (dp - D[:, None])
+    dq = scale * (ds @ kvg)
+    dkv_slots = p.T @ dO_t + scale * (ds.T @ q_t)
+    dsink = -np.exp(sink_h - lse) * D
+    return dq, dkv_slots, dsink
+
+
+def attn_bwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int, dO, rows=None):
+    """dq [b, sq, H, d], dkv [b, n_kv, d] and dsink [H].
+
+    The slot contributions scatter-add into the compact [b, n_kv, d] buffer
+    (np.add.at sums repeated rows); dsink sums over b and t.  With ``rows``
+    only those queries are processed: dq comes back as [len(rows), H, d] and
+    dkv / dsink hold the contributions of those queries alone.
+    """
+    b, sq, H, d = q.shape
+    n_kv = kv_full.shape[1]
+    n_c = n_kv - sq
+    sink_h = _sink_vec(sink, H)
+    pairs = rows if rows is not None else [(bi, t) for bi in range(b) for t in range(sq)]
+    dq = np.zeros((len(pairs), H, d))
+    dkv = np.zeros((b, n_kv, d))
+    dsink = np.zeros(H)
+    for n, (bi, t) in enumerate(pairs):
+        slots = query_slots(t, idx[bi, t], sq, n_c, ratio, window)
+        dq_t, dkv_s, ds_t = attn_bwd_query(q[bi, t], kv_full[bi], slots, sink_h, scale, dO[bi, t])
+        dq[n] = dq_t
+        np.add.at(dkv[bi], slots, dkv_s)
+        if sink is not None:
+            dsink += ds_t
+    if rows is None:
+        dq = dq.reshape(b, sq, H, d)
+    return dq, dkv, dsink

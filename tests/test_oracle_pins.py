@@ -1,0 +1,430 @@
+"""Pins of the fp64 oracle to facts that do not come from the oracle itself.
+
+Each test checks one oracle function against something independent of it:
+a hand-derived worked example (tests/golden), a closed form, a special case
+that reduces to a library routine (numpy matmul, torch's scaled-dot-product
+attention and autograd in float64), brute-force enumeration, central finite
+differences, or an invariant.  The cases are chosen so that a dropped term, a
+wrong sign or index, or a transposed operand in the oracle fails one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import csa_oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _ev(x):
+    """Evaluate a closed-form expression string of a golden fixture."""
+    if isinstance(x, list):
+        return [_ev(v) for v in x]
+    if isinstance(x, str):
+        return float(eval(x, {"__builtins__": {}}, {"log": math.log, "exp": math.exp}))
+    return float(x)
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# storage rounding
+# ---------------------------------------------------------------------------
+
+def test_round_bf16_matches_torch_on_fp32_values():
+    rng = np.random.default_rng(0)
+    x32 = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    ours = orc.round_bf16(x32.astype(np.float64))
+    ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_round_bf16_is_nearest_and_ties_even():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to the even mantissa (1.0)
+    assert orc.round_bf16(1.0 + 2.0 ** -8) == 1.0
+    assert orc.round_bf16(1.0 + 3 * 2.0 ** -8) == 1.0 + 2 * 2.0 ** -7
+    assert orc.round_bf16(-(1.0 + 2.0 ** -8 + 2.0 ** -30)) == -(1.0 + 2.0 ** -7)
+
+
+# ---------------------------------------------------------------------------
+# compressor
+# ---------------------------------------------------------------------------
+
+def test_compress_golden():
+    g = _load("compress_tiny.json")
+    kv = np.array(_ev(g["kv"]))
+    score = np.array(_ev(g["score"]))
+    out = orc.compress(kv, score, g["ratio"])
+    assert out.shape == (1, 1, 2)
+    np.testing.assert_allclose(out, np.array(_ev(g["expected_kv_c"])), rtol=0, atol=1e-14)
+
+
+def test_compress_ratio1_is_identity():
+    rng = np.random.default_rng(1)
+    kv = rng.standard_normal((2, 9, 5))
+    score = rng.standard_normal((2, 9, 5)) * 10
+    np.testing.assert_allclose(orc.compress(kv, score, 1), kv, rtol=0, atol=1e-15)
+
+
+def test_compress_constant_score_is_block_mean():
+    rng = np.random.default_rng(2)
+    kv = rng.standard_normal((1, 12, 3))
+    score = np.full((1, 12, 3), 0.7)
+    ref = kv.reshape(1, 3, 4, 3).mean(axis=2)
+    np.testing.assert_allclose(orc.compress(kv, score, 4), ref, rtol=0, atol=1e-14)
+
+
+def test_compress_dominant_score_selects_token():
+    rng = np.random.default_rng(3)
+    kv = rng.standard_normal((1, 8, 4))
+    score = np.zeros((1, 8, 4))
+    score[0, 2, :] = 800.0   # block 0 -> token 2
+    score[0, 4, :] = 800.0   # block 1 -> token 4
+    out = orc.compress(kv, score, 4)
+    np.testing.assert_allclose(out[0, 0], kv[0, 2], atol=1e-12)
+    np.testing.assert_allclose(out[0, 1], kv[0, 4], atol=1e-12)
+
+
+def test_compress_scalar_score_broadcasts():
+    rng = np.random.default_rng(4)
+    kv = rng.standard_normal((2, 8, 6))
+    s1 = rng.standard_normal((2, 8, 1))
+    np.testing.assert_allclose(orc.compress(kv, s1, 4), orc.compress(kv, np.repeat(s1, 6, 2), 4),
+                               atol=1e-15)
+
+
+def test_compress_rounds_once_to_storage():
+    rng = np.random.default_rng(5)
+    kv = orc.round_bf16(rng.standard_normal((1, 16, 8)))
+    score = orc.round_bf16(rng.standard_normal((1, 16, 8)))
+    exact = orc.compress(kv, score, 4)
+    stored = orc.compress(kv, score, 4, out_dtype="bf16")
+    np.testing.assert_array_equal(stored, orc.round_bf16(exact))
+    assert np.abs(stored - exact).max() <= 2.0 ** -8 * np.abs(exact).max()
+
+
+@pytest.mark.parametrize("d_s", [1, 3])
+def test_compress_bwd_finite_differences(d_s):
+    rng = np.random.default_rng(6)
+    b, sq, d, r = 1, 7, 3, 3   # token 6 is past the last block: zero gradient
+    kv = rng.standard_normal((b, sq, d))
+    score = rng.standard_normal((b, sq, d_s))
+    g = rng.standard_normal((b, sq // r, d))
+    dkv, dscore = orc.compress_bwd(kv, score, r, g)
+    h = 1e-6
+
+    def loss(kv_, sc_):
+        return float((orc.compress(kv_, sc_, r) * g).sum())
+    for arr, grad in ((kv, dkv), (score, dscore)):
+        fd = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            a0 = arr[i]
+            arr[i] = a0 + h
+            lp = loss(kv, score)
+            arr[i] = a0 - h
+            lm = loss(kv, score)
+            arr[i] = a0
+            fd[i] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(grad, fd, atol=1e-8)
+    assert np.all(dkv[0, 6] == 0) and np.all(dscore[0, 6] == 0)
+
+
+# ---------------------------------------------------------------------------
+# indexer and top-k
+# ---------------------------------------------------------------------------
+
+def test_visible_blocks_values():
+    # positions 1..8 // 4 -> 0,0,0,1,1,1,1,2
+    assert [orc.visible_blocks(t, 4) for t in range(8)] == [0, 0, 0, 1, 1, 1, 1, 2]
+
+
+def test_indexer_golden():
+    g = _load("indexer_tiny.json")
+    I = orc.indexer_scores(np.array(g["q_I"]), np.array(g["k_I"]), np.array(g["w"]), g["ratio"])
+    exp = g["expected_rows"]
+    for t, row in enumerate(exp):
+        np.testing.assert_allclose(I[0, t, :len(row)], _ev(row), atol=1e-15)
+        assert np.all(np.isneginf(I[0, t, len(row):]))
+
+
+def test_indexer_single_head_unit_weight_is_relu_matmul():
+    rng = np.random.default_rng(7)
+    b, sq, d_I, r = 2, 24, 5, 3
+    q_I = rng.standard_normal((b, sq, 1, d_I))
+    k_I = rng.standard_normal((b, sq // r, d_I))
+    w = np.ones((b, sq, 1))
+    I = orc.indexer_scores(q_I, k_I, w, r)
+    for bi in range(b):
+        full = np.maximum(q_I[bi, :, 0] @ k_I[bi].T, 0)
+        for t in range(sq):
+            v = (t + 1) // r
+            np.testing.assert_allclose(I[bi, t, :v], full[t, :v], atol=1e-13)
+            assert np.all(np.isneginf(I[bi, t, v:]))
+
+
+def test_indexer_linear_in_w_and_homogeneous_in_q():
+    rng = np.random.default_rng(8)
+    b, sq, H, d_I, r = 1, 16, 3, 4, 2
+    q_I = rng.standard_normal((b, sq, H, d_I))
+    k_I = rng.standard_normal((b, sq // r, d_I))
+    w1 = rng.standard_normal((b, sq, H))
+    w2 = rng.standard_normal((b, sq, H))
+    fin = lambda x: np.where(np.isfinite(x), x, 0)
+    I1 = fin(orc.indexer_scores(q_I, k_I, w1, r))
+    I2 = fin(orc.indexer_scores(q_I, k_I, w2, r))
+    I12 = fin(orc.indexer_scores(q_I, k_I, w1 + w2, r))
+    np.testing.assert_allclose(I12, I1 + I2, atol=1e-12)
+    np.testing.assert_allclose(fin(orc.indexer_scores(q_I, k_I, -w1, r)), -I1, atol=1e-12)
+    np.testing.assert_allclose(fin(orc.indexer_scores(2.5 * q_I, k_I, w1, r)), 2.5 * I1, atol=1e-12)
+    # ReLU: flipping q changes the score unless every dot is zero
+    assert not np.allclose(fin(orc.indexer_scores(-q_I, k_I, w1, r)), -I1)
+
+
+def test_topk_golden():
+    g = _load("topk_tiny.json")
+    s = np.array(g["scores"])
+    for c in g["cases"]:
+        assert orc.topk_select_row(s, c["K"]).tolist() == c["expected"]
+
+
+def _brute_topk(scores, K):
+    """Enumerate all subsets of size min(K, v); keep those in which every member
+    beats every non-member under (score desc, index asc)."""
+    v = len(scores)
+    k = min(K, v)
+    better = lambda i, j: scores[i] > scores[j] or (scores[i] == scores[j] and i < j)
+    found = [S for S in itertools.combinations(range(v), k)
+             if all(better(i, j) for i in S for j in range(v) if j not in S)]
+    assert len(found) == 1
+    return list(found[0]) + [-1] * (K - k)
+
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.default_rng(9)
+    for trial in range(300):
+        v = int(rng.integers(0, 9))
+        K = int(rng.integers(1, 7))
+        s = rng.integers(-2, 3, size=v).astype(np.float64)   # many exact ties
+        assert orc.topk_select_row(s, K).tolist() == _brute_topk(list(s), K)
+
+
+def test_topk_ties_from_relu_zeros_and_duplicate_keys():
+    rng = np.random.default_rng(10)
+    b, sq, H, d_I, r, K = 1, 40, 2, 4, 2, 5
+    q_I = np.abs(rng.standard_normal((b, sq, H, d_I)))
+    k_I = rng.standard_normal((b, sq // r, d_I))
+    k_I[0, 3] = k_I[0, 7]                  # duplicate key rows -> exact ties
+    k_I[0, 10] = -np.abs(k_I[0, 10])       # all dots negative -> ReLU zeros
+    k_I[0, 11] = -np.abs(k_I[0, 11])
+    w = np.abs(rng.standard_normal((b, sq, H)))
+    I = orc.indexer_scores(q_I, k_I, w, r)
+    idx = orc.topk_select(I, K)
+    for t in range(sq):
+        v = (t + 1) // r
+        assert idx[0, t].tolist() == _brute_topk(list(I[0, t, :v]), K)
+    assert I[0, sq - 1, 3] == I[0, sq - 1, 7]
+    assert I[0, sq - 1, 10] == 0.0 and I[0, sq - 1, 11] == 0.0
+
+
+# ---------------------------------------------------------------------------
+# attention: dense masked attention through torch's SDPA in float64
+# ---------------------------------------------------------------------------
+
+def _dense_sdpa(q, kv, idx, sink, scale, window, ratio, dO=None):
+    """The same layer as dense attention over all n_kv rows plus one sink key,
+    with an explicit additive mask: log(multiplicity) for allowed rows, -inf
+    elsewhere.  Evaluated by torch.nn.functional.scaled_dot_product_attention
+    in float64; gradients by torch autograd."""
+    b, sq, H, d = q.shape
+    n_kv = kv.shape[1]
+    n_c = n_kv - sq
+    count = np.zeros((b, sq, n_kv))
+    for bi in range(b):
+        for t in range(sq):
+            count[bi, t, max(0, t - window + 1):t + 1] = 1.0
+            for j in idx[bi, t]:
+                if 0 <= j < n_c and j < (t + 1) // ratio:
+                    count[bi, t, sq + j] += 1.0
+    with np.errstate(divide="ignore"):
+        bias = np.log(count)
+    bias = np.concatenate([bias, np.zeros((b, sq, 1))], axis=2)          # sink column
+    qt = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    kvt = torch.tensor(kv, dtype=torch.float64, requires_grad=True)
+    has_sink = sink is not None
+    st = torch.tensor(sink if has_sink else np.zeros(H), dtype=torch.float64, requires_grad=True)
+    qh = qt.permute(0, 2, 1, 3)                                          # [b,H,sq,d]
+    q_ext = torch.cat([qh, torch.ones(b, H, sq, 1, dtype=torch.float64)], dim=3)
+    k_rows = torch.cat([kvt, torch.zeros(b, n_kv, 1, dtype=torch.float64)], dim=2)
+    k_rows = k_rows.unsqueeze(1).expand(b, H, n_kv, d + 1)
+    k_sink = torch.cat([torch.zeros(H, d, dtype=torch.float64), (st / scale).view(H, 1)], dim=1)
+    k_ext = torch.cat([k_rows, k_sink.view(1, H, 1, d + 1).expand(b, H, 1, d + 1)], dim=2)
+    v_ext = torch.cat([kvt.unsqueeze(1).expand(b, H, n_kv, d),
+                       torch.zeros(b, H, 1, d, dtype=torch.float64)], dim=2)
+    mask = torch.tensor(bias).view(b, 1, sq, n_kv + 1)
+    if not has_sink:
+        mask = mask.clone()
+        mask[..., -1] = -math.inf
+    o = torch.nn.functional.scaled_dot_product_attention(q_ext, k_ext, v_ext, attn_mask=mask,
+                                                         scale=scale)
+    logits = scale * (q_ext @ k_ext.transpose(-1, -2)) + mask
+    lse = torch.logsumexp(logits, dim=-1)                                # [b,H,sq]
+    O = o.permute(0, 2, 1, 3)
+    res = {"O": O.detach().numpy(), "LSE": lse.permute(0, 2, 1).detach().numpy()}
+    if dO is not None:
+        (O * torch.tensor(dO)).sum().backward()
+        res["dq"] = qt.grad.numpy()
+        res["dkv"] = kvt.grad.numpy()
+        res["dsink"] = st.grad.numpy() if has_sink else np.zeros(H)
+    return res
+
+
+def _random_case(seed, b=2, sq=24, H=3, d=5, ratio=4, window=5, K=4, sink=True):
+    rng = np.random.default_rng(seed)
+    n_c = sq // ratio
+    q = rng.standard_normal((b, sq, H, d))
+    kv = rng.standard_normal((b, sq + n_c, d))
+    # repeated indices, -1 padding, out-of-range and not-yet-visible entries
+    idx = rng.integers(-1, n_c + 2, size=(b, sq, K)).astype(np.int32)
+    idx[:, :, 1] = idx[:, :, 0]
+    snk = rng.standard_normal(H) if sink else None
+    dO = rng.standard_normal((b, sq, H, d))
+    return q, kv, idx, snk, d ** -0.5, window, ratio, dO
+
+
+@pytest.mark.parametrize("sink", [True, False])
+def test_attn_matches_dense_sdpa(sink):
+    q, kv, idx, snk, scale, W, r, dO = _random_case(11, sink=sink)
+    O, L = orc.attn_fwd(q, kv, idx, snk, scale, W, r)
+    dq, dkv, dsink = orc.attn_bwd(q, kv, idx, snk, scale, W, r, dO)
+    ref = _dense_sdpa(q, kv, idx, snk, scale, W, r, dO)
+    np.testing.assert_allclose(O, ref["O"], atol=1e-12)
+    np.testing.assert_allclose(L, ref["LSE"], atol=1e-12)
+    np.testing.assert_allclose(dq, ref["dq"], atol=1e-12)
+    np.testing.assert_allclose(dkv, ref["dkv"], atol=1e-12)
+    np.testing.assert_allclose(dsink, ref["dsink"], atol=1e-12)
+
+
+def test_attn_reduces_to_causal_dense_attention():
+    """sink = -inf, every visible block selected, window = sq: plain masked
+    attention over kv_full with M[t,i] = (i <= t) for raw rows and
+    (i - sq < vis(t)) for compressed rows."""
+    rng = np.random.default_rng(12)
+    b, sq, H, d, r = 1, 16, 2, 4, 4
+    n_c = sq // r
+    q = rng.standard_normal((b, sq, H, d))
+    kv = rng.standard_normal((b, sq + n_c, d))
+    idx = np.tile(np.arange(n_c, dtype=np.int32), (b, sq, 1))
+    O, L = orc.attn_fwd(q, kv, idx, None, 0.5, sq, r)
+    for t in range(sq):
+        allowed = [i for i in range(sq) if i <= t] + [sq + j for j in range(n_c) if j < (t + 1) // r]
+        s = 0.5 * q[0, t] @ kv[0, allowed].T
+        p = torch.softmax(torch.tensor(s), dim=1).numpy()
+        np.testing.assert_allclose(O[0, t], p @ kv[0, allowed], atol=1e-13)
+        np.testing.assert_allclose(L[0, t], torch.logsumexp(torch.tensor(s), 1).numpy(), atol=1e-13)
+
+
+def test_attn_golden():
+    g = _load("attn_tiny.json")
+    q = np.array(_ev(g["q"]))
+    kv = np.array(_ev(g["kv_full"]))
+    idx = np.array(g["idx"], dtype=np.int32)
+    sink = np.array(g["sink"])
+    dO = np.array(g["dO"])
+    O, L = orc.attn_fwd(q, kv, idx, sink, g["scale"], g["window"], g["ratio"])
+    dq, dkv, dsink = orc.attn_bwd(q, kv, idx, sink, g["scale"], g["window"], g["ratio"], dO)
+    e = g["expected"]
+    np.testing.assert_allclose(O, np.array(_ev(e["O"])), atol=1e-14)
+    np.testing.assert_allclose(L, np.array(_ev(e["LSE"])), atol=1e-14)
+    np.testing.assert_allclose(dq, np.array(_ev(e["dq"])), atol=1e-14)
+    np.testing.assert_allclose(dkv, np.array(_ev(e["dkv"])), atol=1e-14)
+    np.testing.assert_allclose(dsink, np.array(_ev(e["dsink"])), atol=1e-14)
+
+
+def test_attn_probabilities_plus_sink_sum_to_one():
+    q, kv, idx, snk, scale, W, r, _ = _random_case(13)
+    sq, n_c = q.shape[1], kv.shape[1] - q.shape[1]
+    for bi in range(q.shape[0]):
+        for t in range(sq):
+            slots = orc.query_slots(t, idx[bi, t], sq, n_c, r, W)
+            _, lse, p, _ = orc.attn_fwd_query(q[bi, t], kv[bi], slots, snk, scale)
+            np.testing.assert_allclose(p.sum(axis=1) + np.exp(snk - lse), 1.0, atol=1e-14)
+
+
+def test_attn_padding_and_batch_independence():
+    q, kv, idx, snk, scale, W, r, dO = _random_case(14)
+    O, L = orc.attn_fwd(q, kv, idx, snk, scale, W, r)
+    # appending -1 slots changes nothing
+    idx_pad = np.concatenate([idx, -np.ones_like(idx)], axis=2)
+    O2, L2 = orc.attn_fwd(q, kv, idx_pad, snk, scale, W, r)
+    np.testing.assert_array_equal(O, O2)
+    np.testing.assert_array_equal(L, L2)
+    # b=2 equals two b=1 runs
+    for bi in range(2):
+        Ob, Lb = orc.attn_fwd(q[bi:bi + 1], kv[bi:bi + 1], idx[bi:bi + 1], snk, scale, W, r)
+        np.testing.assert_array_equal(Ob[0], O[bi])
+        dqb, dkvb, _ = orc.attn_bwd(q[bi:bi + 1], kv[bi:bi + 1], idx[bi:bi + 1], snk, scale, W, r,
+                                    dO[bi:bi + 1])
+        dq, dkv, _ = orc.attn_bwd(q, kv, idx, snk, scale, W, r, dO)
+        np.testing.assert_allclose(dqb[0], dq[bi], atol=1e-14)
+        np.testing.assert_allclose(dkvb[0], dkv[bi], atol=1e-14)
+
+
+def test_attn_large_logits_stable():
+    """LSE near 1000 (two keys, two heads): finite results that match the
+    dense float64 formulation."""
+    rng = np.random.default_rng(15)
+    b, sq, H, d, r = 1, 4, 2, 3, 2
+    q = rng.standard_normal((b, sq, H, d)) * 300
+    kv = rng.standard_normal((b, sq + sq // r, d)) * 3
+    idx = np.zeros((b, sq, 1), np.int32)
+    snk = np.array([1000.0, -5.0])
+    dO = rng.standard_normal((b, sq, H, d))
+    O, L = orc.attn_fwd(q, kv, idx, snk, 1.0, 2, r)
+    dq, dkv, ds = orc.attn_bwd(q, kv, idx, snk, 1.0, 2, r, dO)
+    ref = _dense_sdpa(q, kv, idx, snk, 1.0, 2, r, dO)
+    assert np.all(np.isfinite(L)) and np.abs(L).max() > 500
+    np.testing.assert_allclose(L, ref["LSE"], rtol=1e-13)
+    np.testing.assert_allclose(O, ref["O"], atol=1e-9)
+    np.testing.assert_allclose(dq, ref["dq"], atol=1e-7)
+    np.testing.assert_allclose(dkv, ref["dkv"], atol=1e-7)
+    np.testing.assert_allclose(ds, ref["dsink"], atol=1e-9)
+
+
+def test_attn_bwd_finite_differences():
+    q, kv, idx, snk, scale, W, r, dO = _random_case(16, b=1, sq=9, H=2, d=3, ratio=3, window=3, K=3)
+    dq, dkv, dsink = orc.attn_bwd(q, kv, idx, snk, scale, W, r, dO)
+    h = 1e-6
+
+    def loss():
+        O, _ = orc.attn_fwd(q, kv, idx, snk, scale, W, r)
+        return float((O * dO).sum())
+    for arr, grad in ((q, dq), (kv, dkv), (snk, dsink)):
+        for i in np.ndindex(arr.shape):
+            a0 = arr[i]
+            arr[i] = a0 + h
+            lp = loss()
+            arr[i] = a0 - h
+            lm = loss()
+            arr[i] = a0
+            assert abs((lp - lm) / (2 * h) - grad[i]) < 1e-7, (i, grad[i])
+
+
+def test_attn_rows_subset_matches_full():
+    q, kv, idx, snk, scale, W, r, dO = _random_case(17)
+    O, L = orc.attn_fwd(q, kv, idx, snk, scale, W, r)
+    dq, _, _ = orc.attn_bwd(q, kv, idx, snk, scale, W, r, dO)
+    rows = [(1, 5), (0, 23), (0, 0)]
+    Or, Lr = orc.attn_fwd(q, kv, idx, snk, scale, W, r, rows=rows)
+    dqr, _, _ = orc.attn_bwd(q, kv, idx, snk, scale, W, r, dO, rows=rows)
+    for n, (bi, t) in enumerate(rows):
+        np.testing.assert_array_equal(Or[n], O[bi, t])
+        np.testing.assert_array_equal(Lr[n], L[bi, t])
+        np.testing.assert_allclose(dqr[n], dq[bi, t], atol=1e-15)
