@@ -1,0 +1,241 @@
+"""Python binding of the CSA C ABI (include/csa.h).
+
+Argument marshalling only: each function checks the tensors it is given,
+allocates missing outputs with PyTorch (device memory is PyTorch's job),
+and calls the entry point of the same name in libcsa.so with raw device
+pointers and the current CUDA stream.  All arithmetic runs in the library's
+kernels; there is no fallback: if libcsa.so is missing or the call fails,
+these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcsa.so")
+
+CSA_FP32, CSA_BF16 = 0, 1
+STATUS = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_CUDA",
+          4: "CSA_ERR_WORKSPACE", 5: "CSA_ERR_TIMEOUT", 6: "CSA_ERR_DEVICE_CHECK"}
+
+_lib = None
+
+_c_int, _c_ll, _c_p, _c_f, _c_sz = ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_float, ctypes.c_size_t
+
+SIGNATURES = {
+    "csa_status_string": (ctypes.c_char_p, [_c_int]),
+    "csa_version": (_c_int, []),
+    "csa_compress": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll, _c_int, _c_int, _c_int, _c_int,
+                              _c_int, _c_p]),
+    "csa_indexer_topk_workspace_size": (_c_sz, [_c_int] * 6 + [_c_int]),
+    "csa_indexer_topk_min_workspace": (_c_sz, [_c_int, _c_int]),
+    "csa_indexer_topk": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7 + [_c_int, _c_p, _c_sz,
+                                                                                   _c_p]),
+    "csa_attn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p] + [_c_int] * 8 + [_c_int,
+                                                                                         _c_p]),
+    "csa_attn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+                     + [_c_int] * 8 + [_c_int, _c_p]),
+    "csa_get_device_status": (_c_int, [_c_p, ctypes.POINTER(_c_int)]),
+}
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libcsa.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CSA CUDA library not found at {path}; build it with "
+                           "compressed_sparse_attention_sum_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+class CSAError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = load_library().csa_status_string(code).decode()
+        super().__init__(f"{fn} failed: {msg}")
+        self.code = code
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise CSAError(fn, code)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return CSA_BF16
+    if t.dtype == torch.float32:
+        return CSA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, contiguous=True):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def csa_compress(kv: torch.Tensor, score: torch.Tensor, ratio: int,
+                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Softmax-weighted pooling of `ratio` consecutive tokens.
+
+    kv [b, sq, d] (rows contiguous; may be the raw-row view kv_full[:, :sq]),
+    score [b, sq, d] or [b, sq, 1] packed, out [b, sq//ratio, d] (rows
+    contiguous; may be the view kv_full[:, sq:]).
+    """
+    lib = load_library()
+    _need(kv, "kv", contiguous=False)
+    _need(score, "score", dtype=kv.dtype)
+    b, sq, d = kv.shape
+    n_c = sq // ratio
+    if kv.stride(2) != 1 or kv.stride(1) != d:
+        raise ValueError("kv rows must be contiguous")
+    if out is None:
+        out = torch.empty(b, n_c, d, dtype=kv.dtype, device=kv.device)
+    _need(out, "out", dtype=kv.dtype, contiguous=False)
+    if out.shape != (b, n_c, d) or out.stride(2) != 1 or out.stride(1) != d:
+        raise ValueError("out must be [b, sq//ratio, d] with contiguous rows")
+    _check("csa_compress", lib.csa_compress(kv.data_ptr(), kv.stride(0), score.data_ptr(),
+                                            score.shape[2], out.data_ptr(), out.stride(0), b, sq,
+                                            d, ratio, _dt(kv), _stream(stream)))
+    return out
+
+
+def csa_indexer_topk_workspace_size(b: int, sq: int, n_c: int, H_I: int, d_I: int, topk: int,
+                                    dtype=torch.bfloat16) -> int:
+    lib = load_library()
+    dt = CSA_BF16 if dtype == torch.bfloat16 else CSA_FP32
+    return int(lib.csa_indexer_topk_workspace_size(b, sq, n_c, H_I, d_I, topk, dt))
+
+
+def csa_indexer_topk(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, topk: int, ratio: int,
+                     workspace: Optional[torch.Tensor] = None,
+                     out_idx: Optional[torch.Tensor] = None,
+                     out_score: Optional[torch.Tensor] = None, return_scores: bool = False,
+                     stream=None):
+    """Lightning-indexer scores + exact causal top-k.
+
+    q_I [b, sq, H_I, d_I], k_I [b, n_c, d_I] (same dtype), w [b, sq, H_I] fp32.
+    Returns idx [b, sq, K] int32 (and the fp32 scores [b, sq, K] when
+    return_scores or out_score is given).
+    """
+    lib = load_library()
+    _need(q_I, "q_I")
+    _need(k_I, "k_I", dtype=q_I.dtype)
+    _need(w, "w", dtype=torch.float32)
+    b, sq, H_I, d_I = q_I.shape
+    n_c = k_I.shape[1]
+    K = min(topk, n_c)
+    dev = q_I.device
+    if workspace is None:
+        nbytes = csa_indexer_topk_workspace_size(b, sq, n_c, H_I, d_I, topk, q_I.dtype)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace")
+    if out_idx is None:
+        out_idx = torch.empty(b, sq, K, dtype=torch.int32, device=dev)
+    _need(out_idx, "out_idx", dtype=torch.int32)
+    if out_score is None and return_scores:
+        out_score = torch.empty(b, sq, K, dtype=torch.float32, device=dev)
+    if out_score is not None:
+        _need(out_score, "out_score", dtype=torch.float32)
+    _check("csa_indexer_topk", lib.csa_indexer_topk(
+        q_I.data_ptr(), k_I.data_ptr(), w.data_ptr(), out_idx.data_ptr(), _ptr(out_score), b, sq,
+        n_c, H_I, d_I, ratio, topk, _dt(q_I), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    if out_score is not None:
+        return out_idx, out_score
+    return out_idx
+
+
+def csa_attn_fwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Tensor],
+                 sink: Optional[torch.Tensor], scale: float, ratio: int, window: int,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse MQA forward; idx None = every visible compressed block."""
+    lib = load_library()
+    _need(q, "q")
+    _need(kv_full, "kv_full", dtype=q.dtype)
+    b, sq, H, d = q.shape
+    n_c = kv_full.shape[1] - sq
+    K = 0
+    if idx is not None:
+        _need(idx, "idx", dtype=torch.int32)
+        K = idx.shape[2]
+    if sink is not None:
+        _need(sink, "sink", dtype=torch.float32)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(b, sq, H, dtype=torch.float32, device=q.device)
+    _need(out, "out", dtype=q.dtype)
+    _need(lse, "lse", dtype=torch.float32)
+    _check("csa_attn_fwd", lib.csa_attn_fwd(
+        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), float(scale), out.data_ptr(),
+        lse.data_ptr(), b, sq, H, d, n_c, ratio, window, K, _dt(q), _stream(stream)))
+    return out, lse
+
+
+def csa_attn_bwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Tensor],
+                 sink: Optional[torch.Tensor], scale: float, ratio: int, window: int,
+                 o: torch.Tensor, lse: torch.Tensor, dO: torch.Tensor,
+                 dq: Optional[torch.Tensor] = None, dkv: Optional[torch.Tensor] = None,
+                 dsink: Optional[torch.Tensor] = None, stream=None):
+    """Sparse MQA backward; returns (dq, dkv, dsink) in fp32."""
+    lib = load_library()
+    _need(q, "q")
+    _need(kv_full, "kv_full", dtype=q.dtype)
+    _need(o, "o", dtype=q.dtype)
+    _need(dO, "dO", dtype=q.dtype)
+    _need(lse, "lse", dtype=torch.float32)
+    b, sq, H, d = q.shape
+    n_kv = kv_full.shape[1]
+    n_c = n_kv - sq
+    K = 0
+    if idx is not None:
+        _need(idx, "idx", dtype=torch.int32)
+        K = idx.shape[2]
+    if sink is not None:
+        _need(sink, "sink", dtype=torch.float32)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq = torch.empty(b, sq, H, d, **f32) if dq is None else dq
+    dkv = torch.empty(b, n_kv, d, **f32) if dkv is None else dkv
+    if dsink is None and sink is not None:
+        dsink = torch.empty(H, **f32)
+    _need(dq, "dq", dtype=torch.float32)
+    _need(dkv, "dkv", dtype=torch.float32)
+    _check("csa_attn_bwd", lib.csa_attn_bwd(
+        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), float(scale), o.data_ptr(),
+        lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dkv.data_ptr(), _ptr(dsink), b, sq, H, d,
+        n_c, ratio, window, K, _dt(q), _stream(stream)))
+    return dq, dkv, dsink
+
+
+def csa_get_device_status(stream=None) -> int:
+    """Synchronize the stream, then read and clear the device status word."""
+    lib = load_library()
+    v = ctypes.c_int(0)
+    _check("csa_get_device_status", lib.csa_get_device_status(_stream(stream), ctypes.byref(v)))
+    return v.value

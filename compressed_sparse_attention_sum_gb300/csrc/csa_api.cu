@@ -1,0 +1,245 @@
+// C ABI entry points of the CSA library: argument validation, dispatch to the
+// kernels, and the chunk loop of the indexer.  Every check runs before the
+// first CUDA call, so a rejected call leaves the device untouched.
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/csa.h"
+#include "csa_common.cuh"
+#include "csa_kernels.h"
+
+namespace csa {
+// kernels defined in the other translation units
+cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, const float* w,
+                                       float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
+                                       int d_I, int ratio, bool bf16, cudaStream_t s);
+bool indexer_tc_supported(int H_I, int d_I);
+cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
+                                     float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
+                                     int d_I, int ratio, int* status, cudaStream_t s);
+bool attn_mma_supported(int H, int d, int window, int K);
+cudaError_t launch_attn_fwd_mma(const void* q, const void* kv, const int32_t* idx,
+                                const float* sink, float scale, void* o, float* lse, int b, int sq,
+                                int H, int d, int n_c, int ratio, int window, int K,
+                                cudaStream_t s);
+cudaError_t launch_attn_bwd_mma(const void* q, const void* kv, const int32_t* idx,
+                                const float* sink, float scale, const void* o, const float* lse,
+                                const void* dO, float* dq, float* dkv, float* dsink, int b, int sq,
+                                int H, int d, int n_c, int ratio, int window, int K,
+                                cudaStream_t s);
+cudaError_t launch_attn_fwd_simt(const void* q, const void* kv, const int32_t* idx,
+                                 const float* sink, float scale, void* o, float* lse, int b,
+                                 int sq, int H, int d, int n_c, int ratio, int window, int K,
+                                 bool bf16, cudaStream_t s);
+cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* idx,
+                                 const float* sink, float scale, const void* o, const float* lse,
+                                 const void* dO, float* dq, float* dkv, float* dsink, int b,
+                                 int sq, int H, int d, int n_c, int ratio, int window, int K,
+                                 bool bf16, cudaStream_t s);
+}  // namespace csa
+
+// Device status word (one per device that loads the library).
+static __device__ int g_csa_device_status = 0;
+
+namespace {
+
+constexpr int kMaxD = 512;
+constexpr int kMaxH = 64;
+constexpr int kMaxNc = 16384;
+constexpr int kMaxDI = 256;
+constexpr size_t kDefaultIndexerWorkspace = 128ull << 20;  // stays resident in L2
+constexpr int kIndexerTileRows = 128;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static int* ptrs[64] = {nullptr};
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_csa_device_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+bool valid_dtype(csa_dtype_t dt) { return dt == CSA_FP32 || dt == CSA_BF16; }
+
+// Shared validation of the attention calls.
+csa_status_t check_attn(const void* q, const void* kv_full, const int32_t* idx, float scale,
+                        int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
+                        csa_dtype_t dt) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (q == nullptr || kv_full == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_full) || !aligned16(idx)) return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || H < 1 || d < 8 || d % 8 != 0 || ratio < 1 || window < 1)
+    return CSA_ERR_INVALID_ARG;
+  if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
+  if (idx != nullptr && K < 1) return CSA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return CSA_ERR_INVALID_ARG;
+  if (d > kMaxD || H > kMaxH || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
+  if ((size_t)(window + (idx ? K : n_c)) > 200000) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* csa_status_string(int status) {
+  switch (status) {
+    case CSA_OK: return "CSA_OK";
+    case CSA_ERR_INVALID_ARG: return "CSA_ERR_INVALID_ARG: invalid pointer, alignment or size";
+    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED: shape or dtype not implemented";
+    case CSA_ERR_CUDA: return "CSA_ERR_CUDA: a CUDA call or launch failed";
+    case CSA_ERR_WORKSPACE: return "CSA_ERR_WORKSPACE: indexer workspace too small";
+    case CSA_ERR_TIMEOUT: return "CSA_ERR_TIMEOUT: a bounded device wait gave up";
+    case CSA_ERR_DEVICE_CHECK: return "CSA_ERR_DEVICE_CHECK: a device bounds check failed";
+    default: return "CSA: unknown status";
+  }
+}
+
+int csa_version(void) { return 100; }
+
+csa_status_t csa_compress(const void* kv, long long kv_batch_stride, const void* score,
+                          int score_width, void* out, long long out_batch_stride, int b, int sq,
+                          int d, int ratio, csa_dtype_t dt, csa_stream_t stream) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (kv == nullptr || score == nullptr || out == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(kv) || !aligned16(score) || !aligned16(out)) return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || d < 8 || d % 8 != 0 || ratio < 1 || sq < ratio)
+    return CSA_ERR_INVALID_ARG;
+  if (score_width != 1 && score_width != d) return CSA_ERR_INVALID_ARG;
+  const int n_c = sq / ratio;
+  if (kv_batch_stride < (long long)sq * d || out_batch_stride < (long long)n_c * d)
+    return CSA_ERR_INVALID_ARG;
+  const int esz = dt == CSA_BF16 ? 2 : 4;
+  if ((kv_batch_stride * esz) % 16 != 0 || (out_batch_stride * esz) % 16 != 0)
+    return CSA_ERR_INVALID_ARG;
+  if (d > kMaxD) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(csa::launch_compress(kv, kv_batch_stride, score, score_width, out,
+                                        out_batch_stride, b, sq, d, ratio, dt == CSA_BF16,
+                                        (cudaStream_t)stream));
+}
+
+size_t csa_indexer_topk_min_workspace(int b, int n_c) {
+  if (b < 1 || n_c < 1) return 0;
+  return (size_t)b * kIndexerTileRows * (size_t)n_c * sizeof(float);
+}
+
+size_t csa_indexer_topk_workspace_size(int b, int sq, int n_c, int H_I, int d_I, int topk,
+                                       csa_dtype_t dt) {
+  (void)H_I; (void)d_I; (void)topk; (void)dt;
+  if (b < 1 || sq < 1 || n_c < 1) return 0;
+  const size_t full = (size_t)b * sq * n_c * sizeof(float);
+  const size_t minimum = csa_indexer_topk_min_workspace(b, n_c);
+  size_t ws = full < kDefaultIndexerWorkspace ? full : kDefaultIndexerWorkspace;
+  if (ws < minimum) ws = minimum;
+  return ws;
+}
+
+csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float* w,
+                              int32_t* topk_idx, float* topk_score, int b, int sq, int n_c,
+                              int H_I, int d_I, int ratio, int topk, csa_dtype_t dt,
+                              void* workspace, size_t workspace_bytes, csa_stream_t stream) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (q_idx == nullptr || k_idx == nullptr || w == nullptr || topk_idx == nullptr ||
+      workspace == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
+      !aligned16(topk_score) || !aligned16(workspace))
+    return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || H_I < 1 || d_I < 8 || d_I % 8 != 0 || ratio < 1 || topk < 1)
+    return CSA_ERR_INVALID_ARG;
+  if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
+  if (d_I > kMaxDI || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
+  const size_t row_bytes = (size_t)b * n_c * sizeof(float);
+  if (workspace_bytes < csa_indexer_topk_min_workspace(b, n_c)) return CSA_ERR_WORKSPACE;
+  const int K = topk < n_c ? topk : n_c;
+  cudaStream_t s = (cudaStream_t)stream;
+  // query rows per chunk (all batch elements at once), a multiple of the tile
+  size_t rows = workspace_bytes / row_bytes;
+  rows = rows / kIndexerTileRows * kIndexerTileRows;
+  if (rows > (size_t)sq) rows = (size_t)sq;
+  const bool use_tc = dt == CSA_BF16 && csa::indexer_tc_supported(H_I, d_I);
+  int* status = device_status_ptr();
+  for (int t0 = 0; t0 < sq; t0 += (int)rows) {
+    const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;
+    cudaError_t e;
+    if (use_tc)
+      e = csa::launch_indexer_scores_tc(q_idx, k_idx, w, (float*)workspace, t0, nt, b, sq, n_c,
+                                        H_I, d_I, ratio, status, s);
+    else
+      e = csa::launch_indexer_scores_simt(q_idx, k_idx, w, (float*)workspace, t0, nt, b, sq, n_c,
+                                          H_I, d_I, ratio, dt == CSA_BF16, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    e = csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq, n_c,
+                                ratio, K, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  return CSA_OK;
+}
+
+csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx,
+                          const float* sink, float scale, void* o, float* lse, int b, int sq,
+                          int H, int d, int n_c, int ratio, int window, int K, csa_dtype_t dt,
+                          csa_stream_t stream) {
+  csa_status_t st = check_attn(q, kv_full, idx, scale, b, sq, H, d, n_c, ratio, window, K, dt);
+  if (st != CSA_OK) return st;
+  if (o == nullptr || lse == nullptr || !aligned16(o) || !aligned16(lse) || !aligned16(sink))
+    return CSA_ERR_INVALID_ARG;
+  const int Kl = idx ? K : n_c;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
+    return from_cuda(csa::launch_attn_fwd_mma(q, kv_full, idx, sink, scale, o, lse, b, sq, H, d,
+                                              n_c, ratio, window, Kl, s));
+  return from_cuda(csa::launch_attn_fwd_simt(q, kv_full, idx, sink, scale, o, lse, b, sq, H, d,
+                                             n_c, ratio, window, Kl, dt == CSA_BF16, s));
+}
+
+csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx,
+                          const float* sink, float scale, const void* o, const float* lse,
+                          const void* dO, float* dq, float* dkv, float* dsink, int b, int sq,
+                          int H, int d, int n_c, int ratio, int window, int K, csa_dtype_t dt,
+                          csa_stream_t stream) {
+  csa_status_t st = check_attn(q, kv_full, idx, scale, b, sq, H, d, n_c, ratio, window, K, dt);
+  if (st != CSA_OK) return st;
+  if (o == nullptr || lse == nullptr || dO == nullptr || dq == nullptr || dkv == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (sink != nullptr && dsink == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(lse) || !aligned16(dO) || !aligned16(dq) || !aligned16(dkv) ||
+      !aligned16(dsink) || !aligned16(sink))
+    return CSA_ERR_INVALID_ARG;
+  const int Kl = idx ? K : n_c;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int n_kv = sq + n_c;
+  cudaError_t e = csa::launch_zero_f32(dkv, (size_t)b * n_kv * d, s);
+  if (e == cudaSuccess && dsink != nullptr) e = csa::launch_zero_f32(dsink, (size_t)H, s);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
+  if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
+    return from_cuda(csa::launch_attn_bwd_mma(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
+                                              dsink, b, sq, H, d, n_c, ratio, window, Kl, s));
+  return from_cuda(csa::launch_attn_bwd_simt(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
+                                             dsink, b, sq, H, d, n_c, ratio, window, Kl,
+                                             dt == CSA_BF16, s));
+}
+
+csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out) {
+  if (status_out == nullptr) return CSA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CSA_ERR_CUDA;
+  int* p = device_status_ptr();
+  if (p == nullptr) return CSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  *status_out = v;
+  return CSA_OK;
+}
+
+}  // extern "C"

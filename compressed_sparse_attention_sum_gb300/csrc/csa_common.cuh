@@ -1,0 +1,110 @@
+// Shared device helpers of the CSA CUDA library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device status codes (same values as csa_status_t).
+constexpr int kDevTimeout = 5;
+constexpr int kDevCheck = 6;
+
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Load 8 consecutive elements (16 B for bf16, 32 B for fp32) as floats.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* f) {
+  uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float* f) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* f) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store8(float* p, const float* f) {
+  *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+// fp32 vector atomic add into global memory (no return value).
+__device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
+  asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b)
+               : "memory");
+}
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Gather the attention slot rows of query t into `rows` (flat kv_full row ids
+// within the batch element): window rows max(0,t-W+1)..t, then sq+j for the
+// valid entries j of the index row (0 <= j < n_c and j < vis(t)), in index
+// order.  idx == nullptr means every visible block.  Executed by one warp;
+// returns the slot count to every lane.
+__device__ __forceinline__ int build_slots_warp(int* rows, const int32_t* idx_row, int K, int t,
+                                                int sq, int n_c, int ratio, int window) {
+  const int lane = threadIdx.x & 31;
+  const int w0 = max(0, t - window + 1);
+  const int nw = t - w0 + 1;
+  for (int i = lane; i < nw; i += 32) rows[i] = w0 + i;
+  const int vis = min((t + 1) / ratio, n_c);
+  int count = nw;
+  if (idx_row == nullptr) {
+    for (int j = lane; j < vis; j += 32) rows[nw + j] = sq + j;
+    return nw + vis;
+  }
+  for (int base = 0; base < K; base += 32) {
+    const int s = base + lane;
+    int j = -1;
+    if (s < K) j = idx_row[s];
+    const bool ok = (j >= 0) && (j < vis);
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    if (ok) rows[count + __popc(m & ((1u << lane) - 1u))] = sq + j;
+    count += __popc(m);
+  }
+  return count;
+}
+
+}  // namespace csa

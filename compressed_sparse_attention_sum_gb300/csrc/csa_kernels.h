@@ -1,0 +1,22 @@
+// Host-side launchers of the CSA kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace csa {
+
+// Compressor: softmax-weighted pooling.
+cudaError_t launch_compress(const void* kv, long long kv_bs, const void* score, int score_width,
+                            void* out, long long out_bs, int b, int sq, int d, int ratio,
+                            bool bf16, cudaStream_t s);
+
+// Exact per-row top-K of the chunk of scores in ws (rows [t0, t0+nt) of every
+// batch element, laid out [b][nt][n_c]).
+cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
+                               int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s);
+
+cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
+
+}  // namespace csa

@@ -1,0 +1,247 @@
+// csa_indexer_topk: lightning-indexer scores and the exact causal top-k.
+//
+// Score: I[b,t,j] = sum_h w[b,t,h] * max(0, q_I[b,t,h,:] . k_I[b,j,:]) for
+// j < vis(t) = (t+1)/ratio ("Add unfused SBHD compressed sparse attention",
+// indexer block and causal compressed mask; "Refactor Deepseek v4 to use
+// Attention Gym's Compressed Sparse Attention", indexer selectability).
+// Selection: the K largest scores of each row, ties to the lower block index,
+// emitted in ascending block order ("Add the min-memory DSA attention
+// kernels": routing must be tie-exact with one full top-k; support sorted by
+// position).
+//
+// This file holds the CUDA-core score kernel (fp32 inputs and any shape) and
+// the per-row radix select that every score kernel feeds.  Scores of one
+// chunk of query rows sit in a caller-provided fp32 workspace laid out
+// [b][chunk rows][n_c]; only the visible prefix of each row is written and
+// read, and a chunk is sized to stay resident in L2 between the two kernels.
+#include "csa_common.cuh"
+#include "csa_kernels.h"
+
+namespace csa {
+
+// ----------------------------------------------------------------------------
+// CUDA-core score kernel: 64 query rows x 64 blocks per CTA, 256 threads,
+// 4x4 outputs per thread; loops over the indexer heads.
+// ----------------------------------------------------------------------------
+constexpr int kSQ = 64;
+constexpr int kSK = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(256) indexer_scores_simt(
+    const T* __restrict__ q_idx, const T* __restrict__ k_idx, const float* __restrict__ w,
+    float* __restrict__ ws, int t0, int nt, int sq, int n_c, int H_I, int d_I, int ratio) {
+  extern __shared__ float sm[];
+  float* q_s = sm;                    // [d_I][kSQ]
+  float* k_s = sm + d_I * kSQ;        // [d_I][kSK]
+  float* w_s = k_s + d_I * kSK;       // [kSQ]
+  const int bi = blockIdx.z;
+  const int tq0 = t0 + blockIdx.y * kSQ;               // first query of the tile
+  const int j0 = blockIdx.x * kSK;                     // first block of the tile
+  const int tq_end = min(t0 + nt, tq0 + kSQ);          // exclusive
+  if (tq0 >= tq_end) return;
+  const int vis_max = min(tq_end / ratio, n_c);        // vis of the last query of the tile
+  if (j0 >= vis_max) return;
+  const int tid = threadIdx.x;
+  const int ty = tid / 16, tx = tid % 16;
+
+  // keys of the tile (transposed)
+  for (int e = tid; e < kSK * d_I; e += 256) {
+    const int jj = e / d_I, c = e % d_I;
+    const int j = j0 + jj;
+    k_s[c * kSK + jj] = (j < n_c) ? to_f(k_idx[((long long)bi * n_c + j) * d_I + c]) : 0.f;
+  }
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+
+  for (int h = 0; h < H_I; ++h) {
+    __syncthreads();
+    for (int e = tid; e < kSQ * d_I; e += 256) {
+      const int rr = e / d_I, c = e % d_I;
+      const int t = tq0 + rr;
+      q_s[c * kSQ + rr] =
+          (t < tq_end) ? to_f(q_idx[(((long long)bi * sq + t) * H_I + h) * d_I + c]) : 0.f;
+    }
+    if (tid < kSQ) {
+      const int t = tq0 + tid;
+      w_s[tid] = (t < tq_end) ? w[((long long)bi * sq + t) * H_I + h] : 0.f;
+    }
+    __syncthreads();
+    float dot[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) dot[a][c] = 0.f;
+    for (int c = 0; c < d_I; ++c) {
+      const float4 qv = *reinterpret_cast<const float4*>(&q_s[c * kSQ + ty * 4]);
+      const float4 kv = *reinterpret_cast<const float4*>(&k_s[c * kSK + tx * 4]);
+      const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+      const float ka[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) dot[a][cc] = fmaf(qa[a], ka[cc], dot[a][cc]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float wv = w_s[ty * 4 + a];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) acc[a][cc] = fmaf(wv, fmaxf(dot[a][cc], 0.f), acc[a][cc]);
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int t = tq0 + ty * 4 + a;
+    if (t >= tq_end) continue;
+    const int vis = min((t + 1) / ratio, n_c);
+    float* dst = ws + ((long long)bi * nt + (t - t0)) * n_c;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int j = j0 + tx * 4 + cc;
+      if (j < vis) dst[j] = acc[a][cc];
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Per-row exact top-K by 4-pass 8-bit radix select on order-preserving keys.
+// One warp per query row.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(256) topk_select_kernel(const float* __restrict__ ws,
+                                                          int32_t* __restrict__ out_idx,
+                                                          float* __restrict__ out_score, int t0,
+                                                          int nt, int b, int sq, int n_c,
+                                                          int ratio, int K) {
+  extern __shared__ uint32_t smk[];
+  const int warps = blockDim.x / 32;
+  const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const unsigned FULL = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  uint32_t* keys = smk + (size_t)wid * (n_c + 256);
+  int* hist = reinterpret_cast<int*>(keys + n_c);
+  const int r = blockIdx.x * warps + wid;
+  if (r >= b * nt) return;
+  const int bi = r / nt, t = t0 + r % nt;
+  const int vis = min((t + 1) / ratio, n_c);
+  const float* row = ws + (size_t)r * n_c;
+  int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
+  float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
+  if (vis <= K) {
+    for (int s = lane; s < K; s += 32) {
+      oi[s] = s < vis ? s : -1;
+      if (os) os[s] = s < vis ? row[s] : 0.f;
+    }
+    return;
+  }
+  for (int j = lane; j < vis; j += 32) keys[j] = order_key(row[j]);
+  __syncwarp();
+  uint32_t prefix = 0, pmask = 0;
+  int need = K;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (int j = lane; j < vis; j += 32) {
+      const uint32_t u = keys[j];
+      if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+    }
+    __syncwarp();
+    // lane l owns bins 8*(31-l) .. 8*(31-l)+7, so lane 0 holds the highest bins
+    int cnt[8];
+    int tot = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cnt[i] = hist[8 * (31 - lane) + 7 - i];
+      tot += cnt[i];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int excl = incl - tot;  // keys in bins above this lane's bins
+    const bool mine = (excl < need) && (need <= incl);
+    const unsigned bal = __ballot_sync(FULL, mine);
+    const int src = __ffs(bal) - 1;
+    int bin = 0, above = 0;
+    if (mine) {
+      int run = excl;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (run + cnt[i] >= need) {
+          bin = 8 * (31 - lane) + 7 - i;
+          above = run;
+          break;
+        }
+        run += cnt[i];
+      }
+    }
+    bin = __shfl_sync(FULL, bin, src);
+    above = __shfl_sync(FULL, above, src);
+    need -= above;
+    prefix |= (uint32_t)bin << shift;
+    pmask |= 255u << shift;
+    __syncwarp();
+  }
+  // threshold key = prefix: keep every key above it and the `need` lowest-index
+  // keys equal to it, in ascending block order.
+  int out_pos = 0, eq_seen = 0;
+  for (int base = 0; base < vis; base += 32) {
+    const int j = base + lane;
+    const uint32_t u = (j < vis) ? keys[j] : 0u;
+    const bool gt = (j < vis) && (u > prefix);
+    const bool eq = (j < vis) && (u == prefix);
+    const unsigned eqm = __ballot_sync(FULL, eq);
+    const bool sel = gt || (eq && (eq_seen + __popc(eqm & lt_mask)) < need);
+    const unsigned selm = __ballot_sync(FULL, sel);
+    if (sel) {
+      const int p = out_pos + __popc(selm & lt_mask);
+      oi[p] = j;
+      if (os) os[p] = row[j];
+    }
+    out_pos += __popc(selm);
+    eq_seen += __popc(eqm);
+  }
+}
+
+cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, const float* w,
+                                       float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
+                                       int d_I, int ratio, bool bf16, cudaStream_t s) {
+  dim3 grid((unsigned)((n_c + kSK - 1) / kSK), (unsigned)((nt + kSQ - 1) / kSQ), (unsigned)b);
+  const size_t smem = (size_t)(d_I * (kSQ + kSK) + kSQ) * sizeof(float);
+  if (bf16) {
+    auto k = indexer_scores_simt<__nv_bfloat16>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k<<<grid, 256, smem, s>>>((const __nv_bfloat16*)q_idx, (const __nv_bfloat16*)k_idx, w, ws, t0,
+                              nt, sq, n_c, H_I, d_I, ratio);
+  } else {
+    auto k = indexer_scores_simt<float>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k<<<grid, 256, smem, s>>>((const float*)q_idx, (const float*)k_idx, w, ws, t0, nt, sq, n_c,
+                              H_I, d_I, ratio);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
+                               int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s) {
+  const size_t per_warp = (size_t)(n_c + 256) * sizeof(uint32_t);
+  int warps = (int)((200 * 1024) / per_warp);
+  warps = warps < 1 ? 1 : (warps > 8 ? 8 : warps);
+  const size_t smem = per_warp * warps;
+  const int rows = b * nt;
+  dim3 grid((unsigned)((rows + warps - 1) / warps));
+  cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  topk_select_kernel<<<grid, warps * 32, smem, s>>>(ws, topk_idx, topk_score, t0, nt, b, sq, n_c,
+                                                    ratio, K);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,211 @@
+/*
+ * csa.h - C ABI of the Compressed Sparse Attention (CSA) hot path.
+ *
+ * One CSA layer on one GPU, as four calls (plus helpers):
+ *
+ *   csa_compress      softmax-weighted pooling of `ratio` consecutive KV tokens
+ *   csa_indexer_topk  lightning-indexer scores fused with an exact causal top-k
+ *   csa_attn_fwd      sparse MQA (shared K=V) over window + top-k compressed
+ *                     rows + per-head sink; returns O and LSE
+ *   csa_attn_bwd      dQ, dKV, dSink, accumulated in fp32
+ *
+ * Sources (page title, section):
+ *   "Add unfused SBHD compressed sparse attention" (Megatron-LM PR #6400):
+ *     compressor review, causal compressed mask, indexer / top-k block,
+ *     review of the gather backward, attention-sink parameter.
+ *   "Refactor Deepseek v4 to use Attention Gym's Compressed Sparse Attention"
+ *     (torchtitan PR #4452): the selected_attention operator (window +
+ *     selected compressed entries + sink in one softmax, per-head LSE).
+ *   "Add the min-memory DSA attention kernels" (Megatron-LM PR #7152):
+ *     streamed score tiles, tie-exact top-k, fp32 scatter of repeated keys.
+ *
+ * Notation: b batch, sq query tokens, H query heads, d shared K=V head dim,
+ * r = ratio, n_c = sq / r (integer division), n_kv = sq + n_c,
+ * vis(t) = (t + 1) / r (integer division), W = window,
+ * K = min(topk, n_c), H_I / d_I = indexer heads / head dim.
+ *
+ * Layouts (all row-major, innermost dimension contiguous, batch-major):
+ *   kv_full  [b, n_kv, d]   raw rows 0..sq-1, then compressed rows sq..n_kv-1
+ *   q, o, dO [b, sq, H, d]
+ *   lse      [b, sq, H]     fp32, natural log, sink included
+ *   idx      [b, sq, K]     int32, compressed-relative block ids, -1 = pad
+ *   sink     [H]            fp32 logits (NULL = no sink = -inf)
+ *   q_idx    [b, sq, H_I, d_I], k_idx [b, n_c, d_I], w [b, sq, H_I] fp32
+ *
+ * Ownership: the caller allocates and owns every buffer (including the
+ * indexer workspace).  The library keeps no per-call state and allocates
+ * no memory.  All pointers except `workspace` sizes are device pointers.
+ *
+ * Execution: every call only validates its arguments on the host and
+ * enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  No call synchronizes.  Argument errors are detected before any
+ * CUDA call, so an invalid call has no effect on the device.
+ *
+ * Errors: the return value covers host-side validation and launch errors.
+ * Conditions found on the device (a bounded wait that gave up, a failed
+ * bounds check in a checking build) are recorded in a per-device status
+ * word, read and cleared by csa_get_device_status().
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or shape */
+  CSA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype, d > 512, ...) */
+  CSA_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed */
+  CSA_ERR_WORKSPACE = 4,    /* indexer workspace too small */
+  CSA_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up */
+  CSA_ERR_DEVICE_CHECK = 6  /* device: an index or offset check failed */
+} csa_status_t;
+
+typedef enum { CSA_FP32 = 0, CSA_BF16 = 1 } csa_dtype_t;
+
+typedef void* csa_stream_t; /* cudaStream_t */
+
+/* Static, never-freed description of a status code. */
+const char* csa_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int csa_version(void);
+
+/*
+ * csa_compress - softmax-weighted pooling of ratio consecutive tokens.
+ *
+ * Defined by the compressor review of "Add unfused SBHD compressed sparse
+ * attention": for block j < n_c and channel c,
+ *   weights_t = softmax over t in [j*r, (j+1)*r) of score[b, t, c'],
+ *   out[b, j, c] = sum_t weights_t * kv[b, t, c],
+ * with c' = c when score_width == d and c' = 0 when score_width == 1.
+ * The softmax, products and sum run in fp32; the result is cast once to dt.
+ * Tokens past the last complete block (sq % r of them) are not pooled.
+ *
+ *   kv      in   [b, sq, d] rows of dt; batch stride kv_batch_stride elements
+ *                (sq*d for a packed tensor, n_kv*d when kv lives in kv_full)
+ *   score   in   [b, sq, score_width] of dt, packed
+ *   out     out  [b, n_c, d] rows of dt; batch stride out_batch_stride
+ *                elements (pass kv_full + sq*d and n_kv*d to write the
+ *                compressed rows of kv_full in place)
+ * Errors: INVALID_ARG for null pointers, pointers not 16-byte aligned,
+ * d % 8 != 0, score_width not in {1, d}, ratio < 1, sq < ratio, strides
+ * smaller than a batch's rows; UNSUPPORTED for d > 512.
+ */
+csa_status_t csa_compress(const void* kv, long long kv_batch_stride,
+                          const void* score, int score_width,
+                          void* out, long long out_batch_stride,
+                          int b, int sq, int d, int ratio,
+                          csa_dtype_t dt, csa_stream_t stream);
+
+/*
+ * Bytes of indexer workspace that csa_indexer_topk uses by default: the
+ * fp32 score rows of one chunk of queries (n_c floats per query row, at
+ * most 128 MiB, at least one 128-row tile).  Any workspace of at least
+ * csa_indexer_topk_min_workspace() bytes works: the call then processes
+ * the b*sq query rows in chunks that fit, so peak memory follows the
+ * workspace, not sq * n_c.  Returns 0 for invalid sizes.
+ */
+size_t csa_indexer_topk_workspace_size(int b, int sq, int n_c, int H_I, int d_I,
+                                       int topk, csa_dtype_t dt);
+size_t csa_indexer_topk_min_workspace(int b, int n_c);
+
+/*
+ * csa_indexer_topk - lightning indexer + causal top-k.
+ *
+ * Scores ("Add unfused SBHD compressed sparse attention", indexer block;
+ * "Refactor Deepseek v4 ...", indexer selectability):
+ *   I[b,t,j] = sum_h w[b,t,h] * max(0, q_idx[b,t,h,:] . k_idx[b,j,:]),
+ *   for the visible blocks j < vis(t).  w is used as given (the caller
+ *   folds any softmax scale into it).
+ * Selection ("Add the min-memory DSA attention kernels": tie-exact routing,
+ * support sorted by position): the K = min(topk, n_c) largest scores of the
+ * row, ties to the lower j, written in ascending j; rows with vis(t) < K
+ * hold all visible blocks followed by -1.
+ * Products are bf16 x bf16 (or fp32 x fp32) with fp32 accumulation; the
+ * selection compares the fp32 scores exactly (-0 equals +0).
+ *
+ *   q_idx       in   [b, sq, H_I, d_I] dt
+ *   k_idx       in   [b, n_c, d_I]     dt
+ *   w           in   [b, sq, H_I]      fp32
+ *   topk_idx    out  [b, sq, K]        int32
+ *   topk_score  out  [b, sq, K]        fp32 scores of the selected blocks
+ *                                      (0 at -1 slots); may be NULL
+ *   workspace   scratch, device, 16-byte aligned, >= min workspace
+ * Errors: INVALID_ARG (null or misaligned pointers, d_I % 8 != 0,
+ * n_c != sq / ratio, topk < 1, H_I < 1); WORKSPACE (too small);
+ * UNSUPPORTED (d_I > 256, n_c > 16384).
+ */
+csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float* w,
+                              int32_t* topk_idx, float* topk_score,
+                              int b, int sq, int n_c, int H_I, int d_I, int ratio, int topk,
+                              csa_dtype_t dt, void* workspace, size_t workspace_bytes,
+                              csa_stream_t stream);
+
+/*
+ * csa_attn_fwd - sparse MQA forward with sink.
+ *
+ * Defined by "Add unfused SBHD compressed sparse attention" (unfused sparse
+ * core: gather of the selected rows of the compact KV buffer, the two
+ * einsums, the invalid mask; sink parameter; softmax_scale) and by the
+ * selected_attention operator of "Refactor Deepseek v4 ..." (window +
+ * selected compressed entries + sink in one softmax, returns LSE).
+ * For query (b,t) and head h, over the slots
+ *   window rows      max(0, t-W+1) .. t
+ *   compressed rows  sq + idx[b,t,s] for every s with 0 <= idx < n_c and
+ *                    idx < vis(t) (other entries are padding; a repeated
+ *                    entry is a repeated term),
+ *   s_i = scale * q[b,t,h,:] . kv_full[b,row_i,:]
+ *   lse[b,t,h] = log(exp(sink[h]) + sum_i exp(s_i))
+ *   o[b,t,h,:] = sum_i exp(s_i - lse) * kv_full[b,row_i,:]
+ * idx == NULL selects every visible block (dense compressed mode); K is then
+ * ignored.  fp32 softmax and accumulation; o is cast once to dt.
+ * Errors: INVALID_ARG (null/misaligned pointers, d % 8, window < 1,
+ * H < 1, K < 0, n_c != sq / ratio); UNSUPPORTED (d > 512, H > 64).
+ */
+csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx,
+                          const float* sink, float scale, void* o, float* lse,
+                          int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
+                          csa_dtype_t dt, csa_stream_t stream);
+
+/*
+ * csa_attn_bwd - gradients of the forward above.
+ *
+ * With D = sum_c dO*o, p_i = exp(s_i - lse), ds_i = p_i (dO . kv_i - D):
+ *   dq[b,t,h,:]   = scale * sum_i ds_i kv_i
+ *   dkv[b,row,:] += sum over (t,h,slot i with row_i == row) of
+ *                   p_i dO[b,t,h,:] + scale ds_i q[b,t,h,:]
+ *   dsink[h]      = - sum_{b,t} exp(sink[h] - lse[b,t,h]) * D[b,t,h]
+ * The scatter into the compact [b, n_kv, d] buffer accumulates in fp32 and
+ * sums repeated indices ("Add unfused SBHD compressed sparse attention",
+ * review of the gather backward; "Add the min-memory DSA attention
+ * kernels", fp32 scatter).  No [b, sq, n_kv, d] buffer exists.
+ * o and lse are the forward's outputs.  dq [b,sq,H,d], dkv [b,n_kv,d] and
+ * dsink [H] are fp32 and fully written (dkv and dsink are zeroed by the
+ * call).  dsink may be NULL when sink is NULL.  The fp32 atomic sums make
+ * dkv and dsink reproducible to rounding only, not bit-for-bit.
+ * Errors: as csa_attn_fwd.
+ */
+csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx,
+                          const float* sink, float scale, const void* o, const float* lse,
+                          const void* dO, float* dq, float* dkv, float* dsink,
+                          int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
+                          csa_dtype_t dt, csa_stream_t stream);
+
+/*
+ * Read and clear the device status word of the current device after the
+ * work on `stream` has finished (this call synchronizes `stream`).
+ * *status_out receives CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_CHECK.
+ */
+csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

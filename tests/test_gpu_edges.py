@@ -1,0 +1,177 @@
+"""GPU edge cases against the fp64 oracle, through the C ABI.
+
+Repeated indices with -1 / out-of-range / not-yet-visible entries at b=2
+(the loop-oracle regression of the gather-backward review), no sink, dense
+compressed mode, ragged tails (sq not a multiple of the ratio or of any
+tile), n_c = 1, window 1 and window > sq, topk >= n_c, exact ties in the
+indexer, chunked indexer workspaces, zeroing of dkv/dsink, odd head counts
+and every supported head dim.
+"""
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_sum_gb300 import csa
+from oracle import csa_oracle as orc
+from paritylib import TOL, compare_topk_row, f64, maxabs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from compressed_sparse_attention_sum_gb300 import build
+    build.build()
+    yield
+    assert csa.csa_get_device_status() == 0
+
+
+def _dt(name):
+    return torch.float32 if name == "fp32" else torch.bfloat16
+
+
+def _rand_attn(seed, b, sq, H, d, ratio, window, K, dtype, sink=True, dup=True):
+    g = torch.Generator().manual_seed(seed)
+    n_c = sq // ratio
+    q = torch.randn(b, sq, H, d, generator=g).to(_dt(dtype))
+    kv = torch.randn(b, sq + n_c, d, generator=g).to(_dt(dtype))
+    idx = torch.randint(-1, n_c + 2, (b, sq, K), generator=g, dtype=torch.int32)
+    if dup and K > 1:
+        idx[:, :, 1] = idx[:, :, 0]
+    snk = torch.randn(H, generator=g) if sink else None
+    dO = torch.randn(b, sq, H, d, generator=g).to(_dt(dtype))
+    return q, kv, idx, snk, dO
+
+
+def _run_both(q, kv, idx, snk, dO, ratio, window, dtype):
+    b, sq, H, d = q.shape
+    scale = d ** -0.5
+    c = lambda t: None if t is None else t.cuda()
+    O, L = csa.csa_attn_fwd(c(q), c(kv), c(idx), c(snk), scale, ratio, window)
+    dq, dkv, dsink = csa.csa_attn_bwd(c(q), c(kv), c(idx), c(snk), scale, ratio, window, O, L, c(dO))
+    idn = idx.numpy() if idx is not None else np.tile(
+        np.arange(sq // ratio, dtype=np.int32), (b, sq, 1))
+    sn = None if snk is None else f64(snk)
+    O_ref, L_ref = orc.attn_fwd(f64(q), f64(kv), idn, sn, scale, window, ratio)
+    dq_ref, dkv_ref, ds_ref = orc.attn_bwd(f64(q), f64(kv), idn, sn, scale, window, ratio, f64(dO))
+    tol = TOL[dtype]
+    errs = {"O": maxabs(f64(O), O_ref), "LSE": maxabs(f64(L), L_ref), "dq": maxabs(f64(dq), dq_ref),
+            "dkv": maxabs(f64(dkv), dkv_ref)}
+    if snk is not None:
+        errs["dsink"] = maxabs(f64(dsink), ds_ref)
+    assert max(errs.values()) <= tol, errs
+    return O, L, dq, dkv, dsink
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("sink", [True, False])
+def test_repeated_indices_padding_b2(dtype, sink):
+    q, kv, idx, snk, dO = _rand_attn(1, b=2, sq=96, H=4, d=64, ratio=4, window=8, K=12,
+                                     dtype=dtype, sink=sink)
+    _run_both(q, kv, idx, snk, dO, 4, 8, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("shape", [
+    dict(b=1, sq=4, H=2, d=64, ratio=4, window=1, K=1),        # n_c = 1, window 1
+    dict(b=2, sq=131, H=20, d=128, ratio=4, window=200, K=40),  # ragged tails, window > sq, odd H
+    dict(b=1, sq=77, H=3, d=256, ratio=3, window=5, K=30),      # topk > n_c, d 256
+    dict(b=1, sq=64, H=16, d=512, ratio=8, window=16, K=4),     # d 512
+    dict(b=1, sq=50, H=5, d=40, ratio=5, window=7, K=6),        # d not a power of two
+])
+def test_ragged_shapes(dtype, shape):
+    q, kv, idx, snk, dO = _rand_attn(2, dtype=dtype, **shape)
+    _run_both(q, kv, idx, snk, dO, shape["ratio"], shape["window"], dtype)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_dense_mode_matches_all_visible_list(dtype):
+    b, sq, H, d, ratio, W = 2, 300, 8, 128, 16, 24
+    q, kv, _, snk, dO = _rand_attn(3, b, sq, H, d, ratio, W, 1, dtype)
+    n_c = sq // ratio
+    vis = (torch.arange(1, sq + 1) // ratio).view(sq, 1)
+    j = torch.arange(n_c).view(1, n_c)
+    full = torch.where(j < vis, j, -1).to(torch.int32).expand(b, sq, n_c).contiguous()
+    r_list = _run_both(q, kv, full, snk, dO, ratio, W, dtype)
+    r_dense = _run_both(q, kv, None, snk, dO, ratio, W, dtype)
+    assert torch.equal(r_list[0], r_dense[0]) and torch.equal(r_list[1], r_dense[1])
+    assert torch.equal(r_list[2], r_dense[2])
+
+
+def test_bwd_zeroes_outputs():
+    q, kv, idx, snk, dO = _rand_attn(4, 1, 64, 4, 64, 4, 8, 8, "bf16")
+    c = lambda t: t.cuda()
+    O, L = csa.csa_attn_fwd(c(q), c(kv), c(idx), c(snk), 0.125, 4, 8)
+    ref = csa.csa_attn_bwd(c(q), c(kv), c(idx), c(snk), 0.125, 4, 8, O, L, c(dO))
+    dkv = torch.full_like(ref[1], 7.0)
+    dsink = torch.full_like(ref[2], -3.0)
+    got = csa.csa_attn_bwd(c(q), c(kv), c(idx), c(snk), 0.125, 4, 8, O, L, c(dO), dkv=dkv,
+                           dsink=dsink)
+    assert torch.allclose(got[1], ref[1], atol=1e-5) and torch.allclose(got[2], ref[2], atol=1e-5)
+
+
+# ---------------------------------------------------------------------------
+# indexer
+# ---------------------------------------------------------------------------
+
+def _indexer_case(seed, b, sq, H_I, d_I, ratio, dtype, ties=False):
+    g = torch.Generator().manual_seed(seed)
+    n_c = sq // ratio
+    q_I = torch.randn(b, sq, H_I, d_I, generator=g)
+    k_I = torch.randn(b, n_c, d_I, generator=g)
+    w = torch.randn(b, sq, H_I, generator=g) * 0.5
+    if ties:
+        q_I = q_I.abs()
+        w = w.abs()
+        k_I[:, 1::5] = k_I[:, 0::5][:, :k_I[:, 1::5].shape[1]]      # duplicate key rows
+        k_I[:, 3::7] = -k_I[:, 3::7].abs()                         # all dots < 0: score 0
+    return q_I.to(_dt(dtype)), k_I.to(_dt(dtype)), w
+
+
+def _check_indexer(q_I, k_I, w, topk, ratio, ws_bytes=None):
+    b, sq, H_I, d_I = q_I.shape
+    n_c = k_I.shape[1]
+    K = min(topk, n_c)
+    wsp = None
+    if ws_bytes is not None:
+        wsp = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    idx, sc = csa.csa_indexer_topk(q_I.cuda(), k_I.cuda(), w.cuda(), topk, ratio, workspace=wsp,
+                                   return_scores=True)
+    I = orc.indexer_scores(f64(q_I), f64(k_I), f64(w), ratio)
+    idx = idx.cpu().numpy()
+    for bi in range(b):
+        for t in range(sq):
+            v = min((t + 1) // ratio, n_c)
+            ok, _ = compare_topk_row(idx[bi, t], I[bi, t, :v], K)
+            assert ok, (bi, t, idx[bi, t][:8])
+    return idx, sc
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+def test_indexer_exact_ties(dtype):
+    q_I, k_I, w = _indexer_case(5, 2, 200, 3, 64, 2, dtype, ties=True)
+    _check_indexer(q_I, k_I, w, 17, 2)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("case", [
+    dict(b=1, sq=4, H_I=1, d_I=32, ratio=4, topk=1),      # n_c = 1
+    dict(b=2, sq=333, H_I=5, d_I=64, ratio=4, topk=500),  # topk > n_c, ragged
+    dict(b=1, sq=515, H_I=8, d_I=128, ratio=4, topk=64),  # ragged tile tail
+    dict(b=1, sq=260, H_I=2, d_I=256, ratio=1, topk=100), # d_I 256, ratio 1
+])
+def test_indexer_shapes(dtype, case):
+    q_I, k_I, w = _indexer_case(6, case["b"], case["sq"], case["H_I"], case["d_I"], case["ratio"],
+                                dtype)
+    _check_indexer(q_I, k_I, w, case["topk"], case["ratio"])
+
+
+def test_indexer_chunked_workspace_identical():
+    q_I, k_I, w = _indexer_case(7, 2, 1000, 4, 128, 4, "bf16")
+    full, sc_full = _check_indexer(q_I, k_I, w, 96, 4)
+    lib = csa.load_library()
+    small = int(lib.csa_indexer_topk_min_workspace(2, 250))
+    chunked, sc_chunk = _check_indexer(q_I, k_I, w, 96, 4, ws_bytes=small + 100)
+    assert np.array_equal(full, chunked)
+    assert torch.equal(sc_full, sc_chunk)
