@@ -1,0 +1,484 @@
+"""Benchmark of the CSA hot path on GB300: one step = one CSA layer,
+forward + backward: csa_compress -> csa_indexer_topk -> csa_attn_fwd ->
+csa_attn_bwd, on the CSA-4 workload (b=1, sq=4096, H=32, d=128, ratio 4,
+n_c=1024, window 128, topk 512, indexer 64 heads x 128).
+
+Prints one JSON line.  `value` is queries/s of the whole job (all ranks),
+device-timed with CUDA events around each step on the launching stream; the
+L2 is flushed (a 256 MiB write) before every timed step.  `e2e` is the same
+metric through the C ABI from pinned host buffers, with every step's
+host->device input copies and device->host result copies inside the timed
+region.  `roofline` describes the kernel with the largest share of the
+step.  `cpu_baseline` is the fp64 oracle on the host cores over a bounded
+sample of query rows of the same workload.
+
+--impl reference times the oracle itself (the reference arm of this build).
+Multi-GPU: one process per GPU (torchrun); each rank runs its own layer
+(independent batch element), so per-rank work is fixed (weak scaling) and no
+data-path collective exists; timing takes the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "csa4_bf16"
+METRIC = "CSA fwd+bwd ms/layer & queries/s at sq=4096; % of HBM / tensor-core roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# oracle CPU baseline (spawned worker processes, one BLAS thread each)
+# ---------------------------------------------------------------------------
+_W = {}
+
+
+def _worker_init(cfg_name):
+    os.environ["OMP_NUM_THREADS"] = "1"
+    import numpy as np
+    from compressed_sparse_attention_sum_gb300.inputs import CONFIGS, make_inputs
+    from oracle import csa_oracle as orc
+    cfg = CONFIGS[cfg_name]
+    inp = make_inputs(cfg)
+    f = lambda t: t.double().numpy()
+    kv_raw = f(inp["kv_raw"])
+    t0 = time.perf_counter()
+    kv_c = orc.compress(kv_raw, f(inp["score"]), cfg.ratio, out_dtype=cfg.dtype)
+    _W.update(cfg=cfg, orc=orc, np=np, kv_full=np.concatenate([kv_raw, kv_c], axis=1),
+              q_I=f(inp["q_I"]), k_I=f(inp["k_I"]), w=f(inp["w"]), q=f(inp["q"]),
+              sink=f(inp["sink"]), dO=f(inp["dO"]), t_compress=time.perf_counter() - t0)
+
+
+def _worker_rows(ts):
+    """The oracle's work for query rows ts of batch element 0: indexer row,
+    top-k, attention forward, attention backward (with its dKV scatter)."""
+    cfg, orc, np = _W["cfg"], _W["orc"], _W["np"]
+    dkv = np.zeros_like(_W["kv_full"][0])
+    t0 = time.perf_counter()
+    for t in ts:
+        scores = orc.indexer_scores_row(_W["q_I"][0, t], _W["k_I"][0], _W["w"][0, t], t, cfg.ratio)
+        idx = orc.topk_select_row(scores, cfg.K)
+        slots = orc.query_slots(t, idx, cfg.sq, cfg.n_c, cfg.ratio, cfg.window)
+        orc.attn_fwd_query(_W["q"][0, t], _W["kv_full"][0], slots, _W["sink"], cfg.scale)
+        _, dkv_s, _ = orc.attn_bwd_query(_W["q"][0, t], _W["kv_full"][0], slots, _W["sink"],
+                                         cfg.scale, _W["dO"][0, t])
+        np.add.at(dkv, slots, dkv_s)
+    return time.perf_counter() - t0, _W["t_compress"]
+
+
+class OraclePool:
+    """Spawned pool: the oracle runs on every host core, one process per core."""
+
+    def __init__(self, cfg_name, procs=None):
+        self.procs = procs or (os.cpu_count() or 1)
+        os.environ.setdefault("OMP_NUM_THREADS", "1")
+        os.environ["OPENBLAS_NUM_THREADS"] = "1"
+        os.environ["MKL_NUM_THREADS"] = "1"
+        ctx = mp.get_context("spawn")
+        self.pool = ctx.Pool(self.procs, initializer=_worker_init, initargs=(cfg_name,))
+        self.pool.map(_worker_rows, [[0]] * self.procs)   # warm every worker
+
+    def run(self, rows_total, sq, seed):
+        """Time `rows_total` query rows spread evenly over the sequence (the
+        causal mix of short and long rows); returns (seconds, rows)."""
+        import numpy as np
+        rng = np.random.default_rng(seed)
+        ts = np.sort(rng.choice(sq, size=rows_total, replace=False))
+        chunks = [ts[i::self.procs].tolist() for i in range(self.procs)]
+        t0 = time.perf_counter()
+        res = self.pool.map(_worker_rows, chunks)
+        wall = time.perf_counter() - t0
+        t_compress = res[0][1]
+        # the pooled rows of the whole sequence are charged pro rata
+        return wall + t_compress * rows_total / sq, rows_total
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS)
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of the kernels from the committed ncu summary,
+    valid only while the kernel source is unchanged."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return {}
+    out = {}
+    for name, rec in d.items():
+        src = os.path.join(ROOT, rec["source"])
+        try:
+            h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        except OSError:
+            continue
+        if h == rec.get("source_sha256_16"):
+            out[name] = rec
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def algorithmic_work(cfg, idx):
+    """Algorithmic units of one step (valid slots only; MQA rows gathered once
+    per query and shared by the heads)."""
+    import torch
+    sq, ratio, W, d, H = cfg.sq, cfg.ratio, cfg.window, cfg.d, cfg.H
+    t = torch.arange(sq, device=idx.device)
+    vis = ((t + 1) // ratio).view(1, sq, 1)
+    valid_c = ((idx >= 0) & (idx < vis)).sum().item()
+    n_win = cfg.b * int(torch.clamp(t + 1, max=W).sum().item())
+    slots = valid_c + n_win
+    e = 2 if cfg.dtype == "bf16" else 4
+    vis_sum = cfg.b * int(((t + 1) // ratio).clamp(max=cfg.n_c).sum().item())
+    return {
+        "slots": slots,
+        "compress_bytes": cfg.b * (2 * cfg.sq * d + cfg.n_c * d) * e,
+        "indexer_flops": 2.0 * cfg.H_I * cfg.d_I * vis_sum,
+        "fwd_gathered_bytes": slots * d * e,
+        "bwd_gathered_bytes": slots * (d * e + 4 * d),
+        "fwd_flops": 4.0 * d * H * slots,
+        "bwd_flops": 10.0 * d * H * slots,
+    }
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    from compressed_sparse_attention_sum_gb300 import build as _build
+    _build.build()
+    from compressed_sparse_attention_sum_gb300 import csa
+    from compressed_sparse_attention_sum_gb300.inputs import CONFIGS, make_inputs
+    lib = csa.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = CONFIGS[args.workload]
+    if world > 1:
+        cfg = cfg.with_(seed=cfg.seed + rank)   # independent layer per rank
+    inp = make_inputs(cfg)
+    host = {k: v.pin_memory() for k, v in inp.items()}
+    d_in = {k: v.to(dev) for k, v in inp.items()}
+    b, sq, d, n_c, H = cfg.b, cfg.sq, cfg.d, cfg.n_c, cfg.H
+    kv_full = torch.empty(b, sq + n_c, d, dtype=cfg.torch_dtype, device=dev)
+    ws = torch.empty(csa.csa_indexer_topk_workspace_size(b, sq, n_c, cfg.H_I, cfg.d_I, cfg.topk,
+                                                          cfg.torch_dtype), dtype=torch.uint8,
+                     device=dev)
+    idx = torch.empty(b, sq, cfg.K, dtype=torch.int32, device=dev)
+    O = torch.empty(b, sq, H, d, dtype=cfg.torch_dtype, device=dev)
+    L = torch.empty(b, sq, H, dtype=torch.float32, device=dev)
+    dq = torch.empty(b, sq, H, d, dtype=torch.float32, device=dev)
+    dkv = torch.empty(b, sq + n_c, d, dtype=torch.float32, device=dev)
+    dsink = torch.empty(H, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x):
+        kv_full[:, :sq].copy_(x["kv_raw"])          # raw rows of the KV buffer (layer input)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record(stream)
+        csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:])
+        ev[1].record(stream)
+        csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio, workspace=ws,
+                             out_idx=idx)
+        ev[2].record(stream)
+        csa.csa_attn_fwd(x["q"], kv_full, idx, x["sink"], cfg.scale, cfg.ratio, cfg.window, out=O,
+                         lse=L)
+        ev[3].record(stream)
+        csa.csa_attn_bwd(x["q"], kv_full, idx, x["sink"], cfg.scale, cfg.ratio, cfg.window, O, L,
+                         x["dO"], dq=dq, dkv=dkv, dsink=dsink)
+        ev[4].record(stream)
+        return ev
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(d_in)
+    torch.cuda.synchronize()
+    work = algorithmic_work(cfg, idx)
+
+    # ---- device-timed region -------------------------------------------------
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = []
+    launches0 = lib.csa_kernel_launches()
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            evs.append(step(d_in))
+        torch.cuda.synchronize()
+    launches = lib.csa_kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(4)]
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    ms = sum(step_ms) / len(step_ms)
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    queries = b * sq
+    value = world * queries / (ms_max / 1e3)
+
+    # ---- end-to-end through host buffers -------------------------------------
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("idx", idx), ("O", O), ("L", L), ("dq", dq), ("dkv", dkv),
+                             ("dsink", dsink))}
+    d_e2e = {k: torch.empty_like(v) for k, v in d_in.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in host:
+            d_e2e[k].copy_(host[k], non_blocking=True)
+        step(d_e2e)
+        for n, t in (("idx", idx), ("O", O), ("L", L), ("dq", dq), ("dkv", dkv), ("dsink", dsink)):
+            out_host[n].copy_(t, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e = sum(e2e_ms) / len(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e = float(t.item())
+
+    # ---- roofline ---------------------------------------------------------------
+    peaks = load_peaks()
+    traffic = load_traffic()
+    k_ms = {n: sum(s) / len(s) for n, s in zip(("compress", "indexer_topk", "attn_fwd",
+                                                  "attn_bwd"), seg)}
+    per = {
+        "compress": ("hbm", work["compress_bytes"] / (k_ms["compress"] / 1e3) / 1e9,
+                     peaks["hbm_gbs"], "GB/s"),
+        "indexer_topk": ("tensor", work["indexer_flops"] / (k_ms["indexer_topk"] / 1e3) / 1e12,
+                         peaks["bf16_tflops"], "TFLOP/s"),
+        "attn_fwd": ("hbm", work["fwd_gathered_bytes"] / (k_ms["attn_fwd"] / 1e3) / 1e9,
+                     peaks["hbm_gbs"], "GB/s"),
+        "attn_bwd": ("hbm", work["bwd_gathered_bytes"] / (k_ms["attn_bwd"] / 1e3) / 1e9,
+                     peaks["hbm_gbs"], "GB/s"),
+    }
+    kernels = {}
+    for n, (bound, ach, peak, unit) in per.items():
+        kernels[n] = {"ms": round(k_ms[n], 4), "share": round(k_ms[n] / ms, 4), "bound": bound,
+                      "achieved": round(ach, 2), "peak": peak, "unit": unit,
+                      "frac": round(ach / peak, 4)}
+    kernels["attn_fwd"]["tflops"] = round(work["fwd_flops"] / (k_ms["attn_fwd"] / 1e3) / 1e12, 2)
+    kernels["attn_bwd"]["tflops"] = round(work["bwd_flops"] / (k_ms["attn_bwd"] / 1e3) / 1e12, 2)
+    dom = max(k_ms, key=k_ms.get)
+    bound, ach, peak, unit = per[dom]
+    tr = traffic.get(dom)
+    roofline = {"kernel": dom, "bound": bound, "achieved": round(ach, 2), "peak": peak,
+                "unit": unit, "frac": round(ach / peak, 4),
+                "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "peak_source": peaks["source"]}
+    attn_ms = k_ms["attn_fwd"] + k_ms["attn_bwd"]
+    attn_gb = (work["fwd_gathered_bytes"] + work["bwd_gathered_bytes"]) / (attn_ms / 1e3) / 1e9
+    targets = {
+        "indexer_tensor_frac": kernels["indexer_topk"]["frac"],
+        "attn_fwd_bwd_hbm_frac": round(attn_gb / peaks["hbm_gbs"], 4),
+    }
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: b={cfg.b} sq={sq} H={H} d={d} ratio={cfg.ratio} "
+                               f"n_c={n_c} window={cfg.window} topk={cfg.topk} H_I={cfg.H_I} "
+                               f"d_I={cfg.d_I}",
+                   "global_batch": world * b, "seq_len": sq,
+                   "parallelism": "replicas" if world == 1 else f"dp{world} (independent layers)",
+                   "l2": "flushed (256 MiB write) before every timed step"},
+        "ms_per_layer": round(ms_max, 4),
+        "e2e": {"value": round(world * queries / (e2e / 1e3), 1), "unit": "queries/s",
+                "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": roofline,
+        "kernels": kernels,
+        "targets": targets,
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+    }
+    return res
+
+
+def run_cpu_baseline(cfg_name, rows, seed=0):
+    from compressed_sparse_attention_sum_gb300.inputs import CONFIGS
+    cfg = CONFIGS[cfg_name]
+    pool = OraclePool(cfg_name)
+    try:
+        sec, n = pool.run(rows, cfg.sq, seed)
+    finally:
+        pool.close()
+    return {"value": round(n / sec, 2), "unit": "queries/s", "cores": pool.procs,
+            "kind": "oracle",
+            "sample": f"{n} of {cfg.b * cfg.sq} query rows of {cfg_name} (uniform over t), each "
+                      "row: indexer scores + top-k + attention fwd + bwd in fp64; pooling of the "
+                      "whole sequence charged pro rata; one process per host core"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on the host cores."""
+    from compressed_sparse_attention_sum_gb300.inputs import CONFIGS
+    cfg = CONFIGS[args.workload]
+    pool = OraclePool(args.workload)
+    try:
+        for i in range(args.warmup):
+            pool.run(args.ref_rows, cfg.sq, seed=100 + i)
+        times = []
+        for i in range(args.steps):
+            sec, n = pool.run(args.ref_rows, cfg.sq, seed=i)
+            times.append(sec * cfg.sq / n)       # seconds per full layer (extrapolated)
+    finally:
+        pool.close()
+    ms = 1e3 * sum(times) / len(times)
+    value = cfg.b * cfg.sq / (ms / 1e3)
+    sample = (f"{args.ref_rows} of {cfg.b * cfg.sq} query rows per step (uniform over t), "
+              "fp64 oracle, one process per host core; ms_per_step extrapolated to the full layer")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: b={cfg.b} sq={cfg.sq} H={cfg.H} d={cfg.d} "
+                               f"ratio={cfg.ratio} n_c={cfg.n_c} window={cfg.window} "
+                               f"topk={cfg.topk} H_I={cfg.H_I} d_I={cfg.d_I}",
+                   "global_batch": cfg.b, "seq_len": cfg.sq, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "queries/s", "cores": pool.procs,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "queries/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-rows", type=int, default=4096,
+                    help="query rows of the oracle CPU baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=1024,
+                    help="query rows per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # the oracle pool is spawned before the first GPU call
+        cpu = run_cpu_baseline(args.workload, args.cpu_rows)
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    res["cpu_baseline"] = cpu
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -29,6 +29,7 @@ _c_int, _c_ll, _c_p, _c_f, _c_sz = ctypes.c_int, ctypes.c_longlong, ctypes.c_voi
 SIGNATURES = {
     "csa_status_string": (ctypes.c_char_p, [_c_int]),
     "csa_version": (_c_int, []),
+    "csa_kernel_launches": (ctypes.c_ulonglong, []),
     "csa_compress": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll, _c_int, _c_int, _c_int, _c_int,
                               _c_int, _c_p]),
     "csa_indexer_topk_workspace_size": (_c_sz, [_c_int] * 6 + [_c_int]),

@@ -11,12 +11,17 @@
 // Forward per tile: S = Q K^T (warps split slots), online softmax with the
 // sink as the initial running state (m = sink, l = 1) so it enters only the
 // denominator, P -> bf16 in shared memory, O += P V (warps split d).
-// Backward per tile: S and dP = dO V^T from one KV fragment, P = exp(S - lse)
-// (the forward LSE includes the sink), dS = P (dP - D), dQ += dS K in
-// registers, and dKV_tile = P^T dO + dS^T Q, which sums over the heads inside
-// the MMA before one fp32 vector atomic per element of the compact
-// [b*n_kv, d] buffer ("Add the min-memory DSA attention kernels": scatter of
-// selected gradients with repeated indices accumulates in fp32).
+// Backward: a first pass over the slot tiles forms D = sum_i p_i dP_i (equal
+// to dO.O, but without the bf16 rounding of the stored O); the second pass
+// recomputes S and dP = dO V^T from one KV fragment, P = exp(S - lse) (the
+// forward LSE includes the sink), dS = P (dP - D), dQ += dS K in registers,
+// and dKV_tile = P^T dO + dS^T Q, which sums over the heads inside the MMA
+// before one fp32 vector atomic per element of the compact [b*n_kv, d]
+// buffer ("Add the min-memory DSA attention kernels": scatter of selected
+// gradients with repeated indices accumulates in fp32).  P and dS enter
+// these products as bf16 hi + lo pairs (x = hi + lo, hi = bf16(x),
+// lo = bf16(x - hi)), about 16 significant bits, so the sums over thousands
+// of queries stay within the fp32-accumulation error of the method.
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 
@@ -296,6 +301,50 @@ __global__ void __launch_bounds__(FwdCfg<D, MT>::NT) attn_fwd_mma(
 // ---------------------------------------------------------------------------
 // backward
 // ---------------------------------------------------------------------------
+
+// S = Q K^T and dP = dO V^T for 16 head rows (m-tile mt) x NQ*8 slots from n0,
+// sharing the KV fragments (K = V).
+template <int D, int NQ, int LDQ>
+__device__ __forceinline__ void score_dp_tile(float (&sacc)[NQ][4], float (&pacc)[NQ][4],
+                                              const __nv_bfloat16* Qs,
+                                              const __nv_bfloat16* dOs,
+                                              const __nv_bfloat16* KT, int mt, int n0, int lane) {
+#pragma unroll
+  for (int n = 0; n < NQ; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sacc[n][e] = pacc[n][e] = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < D / 16; ++k) {
+    uint32_t aq[4], ag[4];
+    const int arow = (mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * LDQ + k * 16 +
+                     8 * (lane >> 4);
+    ldsm_x4(aq, Qs + arow);
+    ldsm_x4(ag, dOs + arow);
+    if constexpr (NQ == 2) {
+      uint32_t bb[4];
+      ldsm_x4(bb, KT + (n0 + (lane & 7) + 8 * (lane >> 4)) * LDQ + k * 16 +
+                      8 * ((lane >> 3) & 1));
+      mma_bf16(sacc[0], aq, bb[0], bb[1]);
+      mma_bf16(sacc[1], aq, bb[2], bb[3]);
+      mma_bf16(pacc[0], ag, bb[0], bb[1]);
+      mma_bf16(pacc[1], ag, bb[2], bb[3]);
+    } else {
+      uint32_t bb[2];
+      ldsm_x2(bb, KT + (n0 + (lane & 7)) * LDQ + k * 16 + 8 * ((lane >> 3) & 1));
+      mma_bf16(sacc[0], aq, bb[0], bb[1]);
+      mma_bf16(pacc[0], ag, bb[0], bb[1]);
+    }
+  }
+}
+
+// Store x0, x1 as bf16 hi parts and bf16 residuals (x - hi).
+__device__ __forceinline__ void store_hi_lo(__nv_bfloat16* hi, __nv_bfloat16* lo, float x0,
+                                            float x1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  *reinterpret_cast<__nv_bfloat162*>(hi) = h;
+  *reinterpret_cast<__nv_bfloat162*>(lo) = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+}
 template <int D, int MT>
 struct BwdCfg {
   static constexpr int NW = 4 * MT;
@@ -307,9 +356,9 @@ struct BwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + ROWS * LDQ * 2;
   static constexpr int OFF_KV = OFF_DO + ROWS * LDQ * 2;
-  static constexpr int OFF_P = OFF_KV + 2 * NS * LDQ * 2;
-  static constexpr int OFF_DS = OFF_P + ROWS * LDP * 2;
-  static constexpr int OFF_STAT = OFF_DS + ROWS * LDP * 2;
+  static constexpr int OFF_P = OFF_KV + 2 * NS * LDQ * 2;     // P hi, P lo
+  static constexpr int OFF_DS = OFF_P + 2 * ROWS * LDP * 2;   // dS hi, dS lo
+  static constexpr int OFF_STAT = OFF_DS + 2 * ROWS * LDP * 2;
   static constexpr int OFF_ROWS = OFF_STAT + 2 * ROWS * 4;
   // dKV phase: warps split (slot m16-tile, column group)
   static constexpr int NST = NS / 16;
@@ -334,8 +383,10 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_Q);
   __nv_bfloat16* dOs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_DO);
   __nv_bfloat16* KVs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_KV);
-  __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_P);
-  __nv_bfloat16* dSs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_DS);
+  __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_P);      // hi
+  __nv_bfloat16* Pl = Ps + C::ROWS * LDP;                                       // lo
+  __nv_bfloat16* dSs = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_DS);    // hi
+  __nv_bfloat16* dSl = dSs + C::ROWS * LDP;                                     // lo
   float* lse2_s = reinterpret_cast<float*>(smem + C::OFF_STAT);
   float* D_s = lse2_s + C::ROWS;
   int* rows = reinterpret_cast<int*>(smem + C::OFF_ROWS);
@@ -356,33 +407,62 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
   }
   load_heads<D, C::ROWS, LDQ, NT>(Qs, q + qrow * D, h0, H);
   load_heads<D, C::ROWS, LDQ, NT>(dOs, dO + qrow * D, h0, H);
-  // D_h = dO_h . o_h and the sink gradient, one warp per head row
-  for (int r = w; r < C::ROWS; r += C::NW) {
+  for (int r = tid; r < C::ROWS; r += NT) {
     const int h = h0 + r;
-    float part = 0.f, L = 0.f;
-    if (h < H) {
-      const __nv_bfloat16* orow = o + (qrow + h) * D;
-      const __nv_bfloat16* grow = dO + (qrow + h) * D;
-      for (int c = lane * 8; c < D; c += 256) {
-        float ov[8], gv[8];
-        load8(orow + c, ov);
-        load8(grow + c, gv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) part = fmaf(ov[i], gv[i], part);
-      }
-      L = lse[qrow + h];
-    }
-    const float Dh = warp_sum(part);
-    if (lane == 0) {
-      D_s[r] = Dh;
-      lse2_s[r] = (h < H) ? L * kLog2e : INFINITY;   // padded rows: p = 0
-      if (h < H && sink != nullptr) atomicAdd(&dsink[h], -exp2f(sink[h] * kLog2e - L * kLog2e) * Dh);
-    }
+    lse2_s[r] = (h < H) ? lse[qrow + h] * kLog2e : INFINITY;   // padded rows: p = 0
+    D_s[r] = 0.f;
   }
   __syncthreads();
   const int count = s_count;
   const int ntiles = (count + NS - 1) / NS;
   const float sc2 = scale * kLog2e;
+  const int mt_s = w % MT, grp = w / MT;
+
+  // ---- pass 1: D_h = sum_i p_i dP_i --------------------------------------------
+  {
+    float dpart[2] = {0.f, 0.f};
+    gather_tile<D, NS, LDQ, NT>(KVs, kv_b, rows, 0, count);
+    cp_async_commit();
+    for (int it = 0; it < ntiles; ++it) {
+      cp_async_wait_all();
+      __syncthreads();
+      if (it + 1 < ntiles) {
+        gather_tile<D, NS, LDQ, NT>(KVs + ((it + 1) & 1) * NS * LDQ, kv_b, rows, (it + 1) * NS,
+                                    count);
+        cp_async_commit();
+      }
+      const __nv_bfloat16* KT = KVs + (it & 1) * NS * LDQ;
+      float sacc[NQ][4], pacc[NQ][4];
+      score_dp_tile<D, NQ, LDQ>(sacc, pacc, Qs, dOs, KT, mt_s, grp * (NS / 4), lane);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const float l2 = lse2_s[mt_s * 16 + g + 8 * half];
+#pragma unroll
+        for (int n = 0; n < NQ; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = grp * (NS / 4) + n * 8 + 2 * cq + e;
+            if (it * NS + col < count)
+              dpart[half] += exp2f(sacc[n][2 * half + e] * sc2 - l2) * pacc[n][2 * half + e];
+          }
+      }
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float v = dpart[half];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (cq == 0) atomicAdd(&D_s[mt_s * 16 + g + 8 * half], v);
+    }
+    __syncthreads();
+    // sink gradient: dsink_h = -exp(sink_h - lse) D_h
+    if (sink != nullptr) {
+      for (int r = tid; r < C::ROWS; r += NT) {
+        const int h = h0 + r;
+        if (h < H) atomicAdd(&dsink[h], -exp2f(sink[h] * kLog2e - lse2_s[r]) * D_s[r]);
+      }
+    }
+  }
 
   gather_tile<D, NS, LDQ, NT>(KVs, kv_b, rows, 0, count);
   cp_async_commit();
@@ -391,7 +471,6 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
 #pragma unroll
   for (int n = 0; n < NO; ++n) dqacc[n][0] = dqacc[n][1] = dqacc[n][2] = dqacc[n][3] = 0.f;
 
-  const int mt_s = w % MT, grp = w / MT;
   for (int it = 0; it < ntiles; ++it) {
     cp_async_wait_all();
     __syncthreads();
@@ -402,36 +481,11 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
     }
     const __nv_bfloat16* KT = KVs + (it & 1) * NS * LDQ;
     const int base = it * NS;
-    // ---- S = Q K^T, dP = dO V^T; P and dS to smem ---------------------------
+    // ---- S = Q K^T, dP = dO V^T; P and dS (hi, lo) to smem ------------------
     {
       float sacc[NQ][4], pacc[NQ][4];
-#pragma unroll
-      for (int n = 0; n < NQ; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[n][e] = pacc[n][e] = 0.f;
       const int n0 = grp * (NS / 4);
-#pragma unroll 4
-      for (int k = 0; k < D / 16; ++k) {
-        uint32_t aq[4], ag[4];
-        const int arow = (mt_s * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * LDQ + k * 16 +
-                         8 * (lane >> 4);
-        ldsm_x4(aq, Qs + arow);
-        ldsm_x4(ag, dOs + arow);
-        if constexpr (NQ == 2) {
-          uint32_t bb[4];
-          ldsm_x4(bb, KT + (n0 + (lane & 7) + 8 * (lane >> 4)) * LDQ + k * 16 +
-                          8 * ((lane >> 3) & 1));
-          mma_bf16(sacc[0], aq, bb[0], bb[1]);
-          mma_bf16(sacc[1], aq, bb[2], bb[3]);
-          mma_bf16(pacc[0], ag, bb[0], bb[1]);
-          mma_bf16(pacc[1], ag, bb[2], bb[3]);
-        } else {
-          uint32_t bb[2];
-          ldsm_x2(bb, KT + (n0 + (lane & 7)) * LDQ + k * 16 + 8 * ((lane >> 3) & 1));
-          mma_bf16(sacc[0], aq, bb[0], bb[1]);
-          mma_bf16(pacc[0], ag, bb[0], bb[1]);
-        }
-      }
+      score_dp_tile<D, NQ, LDQ>(sacc, pacc, Qs, dOs, KT, mt_s, n0, lane);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int r = mt_s * 16 + g + 8 * half;
@@ -447,8 +501,8 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
             pv[e] = p;
             dv[e] = p * (pacc[n][2 * half + e] - Dh) * scale;
           }
-          *reinterpret_cast<uint32_t*>(Ps + r * LDP + col) = pack_bf16(pv[0], pv[1]);
-          *reinterpret_cast<uint32_t*>(dSs + r * LDP + col) = pack_bf16(dv[0], dv[1]);
+          store_hi_lo(Ps + r * LDP + col, Pl + r * LDP + col, pv[0], pv[1]);
+          store_hi_lo(dSs + r * LDP + col, dSl + r * LDP + col, dv[0], dv[1]);
         }
       }
     }
@@ -459,9 +513,11 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
       const int cbase = cg * (D / 4);
 #pragma unroll
       for (int k = 0; k < NS / 16; ++k) {
-        uint32_t a[4];
-        ldsm_x4(a, dSs + (mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * LDP + k * 16 +
-                        8 * (lane >> 4));
+        uint32_t a[4], al[4];
+        const int aoff = (mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * LDP + k * 16 +
+                         8 * (lane >> 4);
+        ldsm_x4(a, dSs + aoff);
+        ldsm_x4(al, dSl + aoff);
 #pragma unroll
         for (int n2 = 0; n2 < NO; n2 += 2) {
           uint32_t bb[4];
@@ -469,6 +525,8 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
                             n2 * 8 + 8 * (lane >> 4));
           mma_bf16(dqacc[n2], a, bb[0], bb[1]);
           mma_bf16(dqacc[n2 + 1], a, bb[2], bb[3]);
+          mma_bf16(dqacc[n2], al, bb[0], bb[1]);
+          mma_bf16(dqacc[n2 + 1], al, bb[2], bb[3]);
         }
       }
     }
@@ -481,11 +539,13 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
       for (int n = 0; n < NK; ++n) kacc[n][0] = kacc[n][1] = kacc[n][2] = kacc[n][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < MT; ++kk) {
-        uint32_t ap[4], ad[4];
+        uint32_t ap[4], ad[4], apl[4], adl[4];
         const int aoff = (kk * 16 + (lane & 7) + 8 * (lane >> 4)) * LDP + st * 16 +
                          8 * ((lane >> 3) & 1);
         ldsm_x4_t(ap, Ps + aoff);
         ldsm_x4_t(ad, dSs + aoff);
+        ldsm_x4_t(apl, Pl + aoff);
+        ldsm_x4_t(adl, dSl + aoff);
 #pragma unroll
         for (int n2 = 0; n2 < NK; n2 += 2) {
           const int boff = (kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1)) * LDQ + cbase +
@@ -495,8 +555,12 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
           ldsm_x4_t(bq, Qs + boff);
           mma_bf16(kacc[n2], ap, bg[0], bg[1]);
           mma_bf16(kacc[n2 + 1], ap, bg[2], bg[3]);
+          mma_bf16(kacc[n2], apl, bg[0], bg[1]);
+          mma_bf16(kacc[n2 + 1], apl, bg[2], bg[3]);
           mma_bf16(kacc[n2], ad, bq[0], bq[1]);
           mma_bf16(kacc[n2 + 1], ad, bq[2], bq[3]);
+          mma_bf16(kacc[n2], adl, bq[0], bq[1]);
+          mma_bf16(kacc[n2 + 1], adl, bq[2], bq[3]);
         }
       }
 #pragma unroll
@@ -543,6 +607,7 @@ static cudaError_t run_fwd(const void* q, const void* kv, const int32_t* idx, co
   dim3 grid((unsigned)sq, (unsigned)b, (unsigned)((H + C::ROWS - 1) / C::ROWS));
   k<<<grid, C::NT, smem, s>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
                               (__nv_bfloat16*)o, lse, sq, H, n_c, ratio, window, K);
+    count_launches(1);
   return cudaGetLastError();
 }
 
@@ -560,6 +625,7 @@ static cudaError_t run_bwd(const void* q, const void* kv, const int32_t* idx, co
   k<<<grid, C::NT, smem, s>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
                               (const __nv_bfloat16*)o, lse, (const __nv_bfloat16*)dO, dq, dkv,
                               dsink, sq, H, n_c, ratio, window, K);
+    count_launches(1);
   return cudaGetLastError();
 }
 

@@ -164,10 +164,12 @@ cudaError_t launch_attn_fwd_simt(const void* q, const void* kv, const int32_t* i
     attn_fwd_simt<__nv_bfloat16><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale, (__nv_bfloat16*)o,
         lse, sq, H, d, n_c, ratio, window, K);
+    count_launches(1);
   } else {
     attn_fwd_simt<float><<<grid, 32 * kSimtWarps, smem, s>>>((const float*)q, (const float*)kv,
                                                              idx, sink, scale, (float*)o, lse, sq,
                                                              H, d, n_c, ratio, window, K);
+    count_launches(1);
   }
   return cudaGetLastError();
 }
@@ -184,10 +186,12 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* i
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
         (const __nv_bfloat16*)o, lse, (const __nv_bfloat16*)dO, dq, dkv, dsink, sq, H, d, n_c,
         ratio, window, K);
+    count_launches(1);
   } else {
     attn_bwd_simt<float><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const float*)q, (const float*)kv, idx, sink, scale, (const float*)o, lse,
         (const float*)dO, dq, dkv, dsink, sq, H, d, n_c, ratio, window, K);
+    count_launches(1);
   }
   return cudaGetLastError();
 }
@@ -209,9 +213,13 @@ cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {
     size_t blocks = (n4 + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
     zero_f32_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<float4*>(p), n4);
+    count_launches(1);
   }
   const size_t rem = n - n4 * 4;
-  if (rem) zero_f32_tail<<<1, 32, 0, s>>>(p + n4 * 4, rem);
+  if (rem) {
+    zero_f32_tail<<<1, 32, 0, s>>>(p + n4 * 4, rem);
+    count_launches(1);
+  }
   return cudaGetLastError();
 }
 

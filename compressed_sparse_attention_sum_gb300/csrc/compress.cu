@@ -67,10 +67,12 @@ cudaError_t launch_compress(const void* kv, long long kv_bs, const void* score, 
     compress_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
         (const __nv_bfloat16*)kv, kv_bs, (const __nv_bfloat16*)score, score_width,
         (__nv_bfloat16*)out, out_bs, sq, d, ratio, n_c);
+    count_launches(1);
   } else {
     compress_kernel<float><<<grid, threads, 0, s>>>((const float*)kv, kv_bs, (const float*)score,
                                                     score_width, (float*)out, out_bs, sq, d,
                                                     ratio, n_c);
+    count_launches(1);
   }
   return cudaGetLastError();
 }

@@ -38,6 +38,13 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* i
                                  bool bf16, cudaStream_t s);
 }  // namespace csa
 
+#include <atomic>
+
+namespace csa {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
+}  // namespace csa
+
 // Device status word (one per device that loads the library).
 static __device__ int g_csa_device_status = 0;
 
@@ -104,6 +111,8 @@ const char* csa_status_string(int status) {
 }
 
 int csa_version(void) { return 100; }
+
+unsigned long long csa_kernel_launches(void) { return csa::g_launches.load(); }
 
 csa_status_t csa_compress(const void* kv, long long kv_batch_stride, const void* score,
                           int score_width, void* out, long long out_batch_stride, int b, int sq,

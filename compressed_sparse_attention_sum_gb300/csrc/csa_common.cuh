@@ -7,6 +7,10 @@
 
 namespace csa {
 
+// Process-wide count of kernels this library has enqueued (every launcher
+// adds its launches); read through csa_kernel_launches().
+void count_launches(int n);
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

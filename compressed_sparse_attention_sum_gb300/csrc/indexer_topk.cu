@@ -221,11 +221,13 @@ cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, con
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, s>>>((const __nv_bfloat16*)q_idx, (const __nv_bfloat16*)k_idx, w, ws, t0,
                               nt, sq, n_c, H_I, d_I, ratio);
+    count_launches(1);
   } else {
     auto k = indexer_scores_simt<float>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, s>>>((const float*)q_idx, (const float*)k_idx, w, ws, t0, nt, sq, n_c,
                               H_I, d_I, ratio);
+    count_launches(1);
   }
   return cudaGetLastError();
 }
@@ -241,6 +243,7 @@ cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_s
   cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   topk_select_kernel<<<grid, warps * 32, smem, s>>>(ws, topk_idx, topk_score, t0, nt, b, sq, n_c,
                                                     ratio, K);
+    count_launches(1);
   return cudaGetLastError();
 }
 

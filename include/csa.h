@@ -76,6 +76,10 @@ const char* csa_status_string(int status);
 /* Library version as 10000*major + 100*minor + patch. */
 int csa_version(void);
 
+/* Number of kernels this library has enqueued in this process (all
+ * devices, all calls): lets a caller count the launches of a timed region. */
+unsigned long long csa_kernel_launches(void);
+
 /*
  * csa_compress - softmax-weighted pooling of ratio consecutive tokens.
  *
