@@ -358,8 +358,8 @@ struct BwdCfg {
   static constexpr int OFF_KV = OFF_DO + ROWS * LDQ * 2;
   static constexpr int OFF_P = OFF_KV + 2 * NS * LDQ * 2;     // P hi, P lo
   static constexpr int OFF_DS = OFF_P + 2 * ROWS * LDP * 2;   // dS hi, dS lo
-  static constexpr int OFF_STAT = OFF_DS + 2 * ROWS * LDP * 2;
-  static constexpr int OFF_ROWS = OFF_STAT + 2 * ROWS * 4;
+  static constexpr int OFF_STAT = OFF_DS + 2 * ROWS * LDP * 2;   // lse2, D, D partials [4]
+  static constexpr int OFF_ROWS = OFF_STAT + 6 * ROWS * 4;
   // dKV phase: warps split (slot m16-tile, column group)
   static constexpr int NST = NS / 16;
   static constexpr int NCG = NW / NST;
@@ -410,7 +410,6 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
   for (int r = tid; r < C::ROWS; r += NT) {
     const int h = h0 + r;
     lse2_s[r] = (h < H) ? lse[qrow + h] * kLog2e : INFINITY;   // padded rows: p = 0
-    D_s[r] = 0.f;
   }
   __syncthreads();
   const int count = s_count;
@@ -447,13 +446,19 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
           }
       }
     }
+    // fixed-order reduction (quad lanes, then the four slot groups), so that
+    // D and everything derived from it are reproducible run to run
+    float* D_part = D_s + C::ROWS;   // [4][ROWS]
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float v = dpart[half];
       v += __shfl_xor_sync(0xffffffffu, v, 1);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
-      if (cq == 0) atomicAdd(&D_s[mt_s * 16 + g + 8 * half], v);
+      if (cq == 0) D_part[grp * C::ROWS + mt_s * 16 + g + 8 * half] = v;
     }
+    __syncthreads();
+    for (int r = tid; r < C::ROWS; r += NT)
+      D_s[r] = (D_part[r] + D_part[C::ROWS + r]) + (D_part[2 * C::ROWS + r] + D_part[3 * C::ROWS + r]);
     __syncthreads();
     // sink gradient: dsink_h = -exp(sink_h - lse) D_h
     if (sink != nullptr) {

@@ -2,6 +2,7 @@
 // kernels, and the chunk loop of the indexer.  Every check runs before the
 // first CUDA call, so a rejected call leaves the device untouched.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/csa.h"
@@ -174,7 +175,11 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
   size_t rows = workspace_bytes / row_bytes;
   rows = rows / kIndexerTileRows * kIndexerTileRows;
   if (rows > (size_t)sq) rows = (size_t)sq;
-  const bool use_tc = dt == CSA_BF16 && csa::indexer_tc_supported(H_I, d_I);
+  // CSA_INDEXER_CUDA_CORES=1 selects the CUDA-core score kernel for bf16 too
+  // (same results up to fp32 summation order; used to compare the two).
+  const char* cc = getenv("CSA_INDEXER_CUDA_CORES");
+  const bool use_tc = dt == CSA_BF16 && !(cc && cc[0] == '1') &&
+                      csa::indexer_tc_supported(H_I, d_I);
   int* status = device_status_ptr();
   for (int t0 = 0; t0 < sq; t0 += (int)rows) {
     const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;

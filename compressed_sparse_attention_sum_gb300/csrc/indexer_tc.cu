@@ -1,10 +1,418 @@
-// Tensor-core (tcgen05) indexer score kernel: placeholder until written.
+// Lightning-indexer scores on the 5th-generation tensor cores (tcgen05 + TMEM,
+// operands staged by TMA), bf16 inputs, fp32 accumulation.
+//
+//   I[b,t,j] = sum_h w[b,t,h] * max(0, q_I[b,t,h,:] . k_I[b,j,:]),  j < vis(t)
+//
+// ("Add unfused SBHD compressed sparse attention", indexer block; "Refactor
+// Deepseek v4 to use Attention Gym's Compressed Sparse Attention", indexer
+// selectability j < (t+1)//ratio.)
+//
+// One CTA computes a tile of 128 queries x 128 compressed blocks of one batch
+// element, for all indexer heads, and writes the fp32 tile to the score
+// workspace that the per-row select kernel reads.  Tiles entirely above the
+// causal boundary are skipped.  Roles (320 threads):
+//   warp 0      TMA producer: the k_I tile once, then one q_I head tile per
+//               stage of a 4-deep ring (3D tensor map over [b*sq, H_I, d_I])
+//   warp 1      TMEM owner + MMA issuer: per head, d_I/16 tcgen05.mma
+//               (M=128 queries, N=128 blocks, K=16) into one of two TMEM
+//               accumulators, committed to the ring's "empty" barrier and to
+//               the accumulator's "full" barrier
+//   warps 2-9   epilogue: tcgen05.ld of the head's accumulator (row = query =
+//               TMEM lane), release of the accumulator, then
+//               I += w[t,h] * max(S, 0) in registers; each warp owns one TMEM
+//               lane quarter and one half of the 128 columns
+// Every mbarrier wait is bounded; a wait that gives up records
+// CSA_ERR_TIMEOUT in the device status word and the CTA skips to teardown.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "csa_common.cuh"
 #include "csa_kernels.h"
+
 namespace csa {
-bool indexer_tc_supported(int, int) { return false; }
-cudaError_t launch_indexer_scores_tc(const void*, const void*, const float*, float*, int, int, int,
-                                     int, int, int, int, int, int*, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+namespace tc {
+
+constexpr int kTileM = 128;     // queries per tile (TMEM lanes)
+constexpr int kTileN = 128;     // compressed blocks per tile (TMEM columns per accumulator)
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kMaxHeads = 64;
+constexpr uint32_t kTmemCols = 256;
+constexpr long long kWaitLimit = 1ll << 22;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Bounded parity wait: true when the phase completed, false after the limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand stored as rows of 128 B
+// (64 bf16 of K) in the 128-byte swizzle pattern, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
+  d |= (uint64_t)1u << 16;                          // leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1u << 46;                          // descriptor version
+  d |= (uint64_t)2u << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B (K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | (1u << 7)                     // A format: bf16
+         | (1u << 10)                    // B format: bf16
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+__device__ __forceinline__ void mma_bf16_ss(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane (no wait).
+#define CSA_TMEM_LD32(taddr, r)                                                                   \
+  asm volatile(                                                                                   \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"     \
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"          \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),      \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),  \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),           \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
+      : "r"(taddr))
+
+// tcgen05.wait::ld with the loaded registers as operands, so that no use of
+// them can be scheduled before the wait.
+#define CSA_TMEM_WAIT32(r)                                                                        \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                                 \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),        \
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),      \
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),  \
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),  \
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),  \
+                 "+r"(r[30]), "+r"(r[31])                                                       \
+               :                                                                                \
+               : "memory")
+
+// 64 consecutive fp32 columns of this thread's lane: two loads, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r0)[32],
+                                          uint32_t (&r1)[32]) {
+  CSA_TMEM_LD32(taddr, r0);
+  CSA_TMEM_LD32(taddr + 32, r1);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  CSA_TMEM_WAIT32(r0);
+  CSA_TMEM_WAIT32(r1);
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+    const float* __restrict__ w, float* __restrict__ ws, int t0, int nt, int sq, int n_c,
+    int H_I, int ratio, int* __restrict__ status) {
+  constexpr int KB = DI / 64;                        // 64-wide K blocks
+  constexpr uint32_t kTileBytes = KB * kTileM * 128;  // one operand tile (128 rows x DI bf16)
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sB = sm;                                     // k_I tile
+  unsigned char* sA = sm + kTileBytes;                        // q_I ring
+  float* w_s = reinterpret_cast<float*>(sA + kStages * kTileBytes);   // [H_I][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + kMaxHeads * kTileM);
+  uint64_t* full = bars;                 // [kStages]
+  uint64_t* empty = bars + kStages;      // [kStages]
+  uint64_t* acc_full = bars + 2 * kStages;      // [2]
+  uint64_t* acc_empty = acc_full + 2;           // [2]
+  uint64_t* b_full = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
+  __shared__ int s_abort;
+
+  const int kt = blockIdx.x, qt = blockIdx.y, bi = blockIdx.z;
+  const int tq0 = t0 + qt * kTileM;
+  const int tq_end = min(t0 + nt, tq0 + kTileM);
+  const int vis_max = min(tq_end / ratio, n_c);
+  const int j0 = kt * kTileN;
+  if (tq0 >= tq_end || j0 >= vis_max) return;   // tile above the causal boundary
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kEpiWarps);
+    }
+    mbar_init(b_full, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // indexer weights of the tile's queries, transposed to [h][row]
+  if (warp >= 2) {
+    for (int e = threadIdx.x - 64; e < kTileM * H_I; e += kEpiWarps * 32) {
+      const int r = e / H_I, h = e % H_I;
+      const int t = tq0 + r;
+      w_s[h * kTileM + r] = (t < tq_end) ? w[((long long)bi * sq + t) * H_I + h] : 0.f;
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      mbar_expect_tx(b_full, kTileBytes);
+      for (int kb = 0; kb < KB; ++kb)
+        tma_load_2d(sB + kb * kTileM * 128, &tmap_k, b_full, kb * 64, bi * n_c + j0);
+      for (int h = 0; h < H_I; ++h) {
+        const int s = h % kStages;
+        const uint32_t par = ((h / kStages) & 1) ^ 1;
+        if (!mbar_wait(&empty[s], par)) {
+          set_status(status, kDevTimeout);
+          s_abort = 1;
+          break;
+        }
+        mbar_expect_tx(&full[s], kTileBytes);
+        unsigned char* dst = sA + s * kTileBytes;
+        for (int kb = 0; kb < KB; ++kb)
+          tma_load_3d(dst + kb * kTileM * 128, &tmap_q, &full[s], kb * 64, h,
+                      bi * sq + tq0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN);
+      bool ok = mbar_wait(b_full, 0);
+      const uint32_t b_base = smem_addr(sB);
+      for (int h = 0; ok && h < H_I; ++h) {
+        const int s = h % kStages;
+        const int a = h & 1;
+        if (!mbar_wait(&full[s], (h / kStages) & 1) ||
+            !mbar_wait(&acc_empty[a], ((h >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t a_base = smem_addr(sA + s * kTileBytes);
+        const uint32_t d_tmem = tmem_base + a * kTileN;
+#pragma unroll
+        for (int k = 0; k < DI / 16; ++k) {
+          const uint32_t off = (k / 4) * kTileM * 128 + (k % 4) * 32;
+          mma_bf16_ss(d_tmem, sw128_desc(a_base + off), sw128_desc(b_base + off), idesc,
+                      k > 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+        mma_commit(&acc_full[a]);
+      }
+      if (!ok) {
+        set_status(status, kDevTimeout);
+        s_abort = 1;
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;                 // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;             // column half of the tile
+    const int row = quarter * 32 + lane;          // query within the tile
+    float acc[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+    bool ok = true;
+    for (int h = 0; h < H_I; ++h) {
+      const int a = h & 1;
+      if (!mbar_wait(&acc_full[a], (h >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      fence_after();
+      uint32_t v0[32], v1[32];
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + a * kTileN + half * 64;
+      tmem_ld64(taddr, v0, v1);
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+      const float wv = w_s[h * kTileM + row];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        acc[c] = fmaf(wv, fmaxf(__uint_as_float(v0[c]), 0.f), acc[c]);
+        acc[32 + c] = fmaf(wv, fmaxf(__uint_as_float(v1[c]), 0.f), acc[32 + c]);
+      }
+    }
+    if (!ok) {
+      set_status(status, kDevTimeout);
+      s_abort = 1;
+    }
+    const int t = tq0 + row;
+    if (ok && t < tq_end) {
+      const int vis = min((t + 1) / ratio, n_c);
+      const int jb = j0 + half * 64;
+      float* dst = ws + ((long long)bi * nt + (t - t0)) * n_c + jb;
+      if (jb + 64 <= vis && (n_c & 3) == 0) {
+#pragma unroll
+        for (int c = 0; c < 64; c += 4)
+          *reinterpret_cast<float4*>(dst + c) =
+              make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (jb + c < vis) dst[c] = acc[c];
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace tc
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+}  // namespace
+
+bool indexer_tc_supported(int H_I, int d_I) {
+  return (d_I == 64 || d_I == 128) && H_I >= 1 && H_I <= tc::kMaxHeads && get_encode() != nullptr;
+}
+
+size_t indexer_tc_smem(int d_I) {
+  const size_t tile = (size_t)(d_I / 64) * tc::kTileM * 128;
+  return 1024 + tile * (1 + tc::kStages) + tc::kMaxHeads * tc::kTileM * 4 + 16 * 8 + 16;
+}
+
+cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
+                                     float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
+                                     int d_I, int ratio, int* status, cudaStream_t s) {
+  auto encode = get_encode();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tq, tk;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)d_I, (cuuint64_t)H_I, (cuuint64_t)b * sq};
+    const cuuint64_t strides[2] = {(cuuint64_t)d_I * 2, (cuuint64_t)H_I * d_I * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)tc::kTileM};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_idx), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)d_I, (cuuint64_t)b * n_c};
+    const cuuint64_t strides[1] = {(cuuint64_t)d_I * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)tc::kTileN};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k_idx), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const size_t smem = indexer_tc_smem(d_I);
+  dim3 grid((unsigned)((n_c + tc::kTileN - 1) / tc::kTileN),
+            (unsigned)((nt + tc::kTileM - 1) / tc::kTileM), (unsigned)b);
+  if (d_I == 128) {
+    auto k = tc::indexer_scores_tc_kernel<128>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k<<<grid, tc::kThreads, smem, s>>>(tq, tk, w, ws, t0, nt, sq, n_c, H_I, ratio, status);
+    count_launches(1);
+  } else {
+    auto k = tc::indexer_scores_tc_kernel<64>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k<<<grid, tc::kThreads, smem, s>>>(tq, tk, w, ws, t0, nt, sq, n_c, H_I, ratio, status);
+    count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace csa
