@@ -36,6 +36,8 @@ SIGNATURES = {
     "csa_indexer_topk_min_workspace": (_c_sz, [_c_int, _c_int]),
     "csa_indexer_topk": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7 + [_c_int, _c_p, _c_sz,
                                                                                    _c_p]),
+    "csa_indexer_topk_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
+                                 + [_c_int, _c_p]),
     "csa_attn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p] + [_c_int] * 8 + [_c_int,
                                                                                          _c_p]),
     "csa_attn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]

@@ -73,6 +73,16 @@ int* device_status_ptr() {
   return ptrs[dev];
 }
 
+}  // namespace
+
+namespace csa {
+// Device address of the status word of the current device (for the other
+// translation units of the library).
+int* device_status_word() { return device_status_ptr(); }
+}  // namespace csa
+
+namespace {
+
 csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
 bool valid_dtype(csa_dtype_t dt) { return dt == CSA_FP32 || dt == CSA_BF16; }

@@ -152,6 +152,44 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
                               csa_stream_t stream);
 
 /*
+ * csa_indexer_topk_noalloc - csa_indexer_topk for callers that cannot
+ * allocate device memory.
+ *
+ * The pages have no counterpart to this call.  csa_indexer_topk needs a
+ * scratch workspace from its caller; some callers cannot provide one: a
+ * plugin or custom operator inside a framework that owns all device memory
+ * and gives it no allocator, a serving loop that must not call cudaMalloc
+ * once it runs (cudaMalloc may synchronize the whole device), a C caller
+ * with no spare buffer.  This call takes the same arguments as
+ * csa_indexer_topk minus the workspace and returns the same results; the
+ * score rows it needs live in a fixed array of CSA_NOALLOC_SCRATCH_BYTES in
+ * the library's own device memory.
+ *
+ *  - Memory: every GPU that loads the library holds the array until the
+ *    process exits.  The call allocates nothing (no cudaMalloc, no cudaFree,
+ *    no allocating library routine).
+ *  - Limit: the query rows are processed in chunks that fit the array; a
+ *    problem whose smallest chunk does not fit (b * 128 * n_c * 4 bytes >
+ *    CSA_NOALLOC_SCRATCH_BYTES) is rejected with CSA_ERR_WORKSPACE before any
+ *    work is enqueued.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress, no allocation) with that device current;
+ *    make that first call before any stream capture.
+ *  - Sharing: all calls on a device use the same array, which keeps the last
+ *    call's scores.  Every value a call reads is written earlier in the same
+ *    call, so nothing needs clearing, but two calls whose work overlaps on the
+ *    GPU (different streams, or different host threads on one device) race
+ *    and corrupt each other's results: order them on one stream or with
+ *    events.
+ * Errors: as csa_indexer_topk, with CSA_ERR_WORKSPACE for the limit above.
+ */
+#define CSA_NOALLOC_SCRATCH_BYTES (16u << 20)
+csa_status_t csa_indexer_topk_noalloc(const void* q_idx, const void* k_idx, const float* w,
+                                      int32_t* topk_idx, float* topk_score,
+                                      int b, int sq, int n_c, int H_I, int d_I, int ratio,
+                                      int topk, csa_dtype_t dt, csa_stream_t stream);
+
+/*
  * csa_attn_fwd - sparse MQA forward with sink.
  *
  * Defined by "Add unfused SBHD compressed sparse attention" (unfused sparse
