@@ -42,7 +42,7 @@ SIGNATURES = {
                                                                                          _c_p]),
     "csa_attn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
                      + [_c_int] * 8 + [_c_int, _c_p]),
-    "csa_get_device_status": (_c_int, [_c_p, ctypes.POINTER(_c_int)]),
+    "csa_get_device_status": (_c_int, [_c_p, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
 }
 
 
@@ -236,9 +236,13 @@ def csa_attn_bwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Ten
     return dq, dkv, dsink
 
 
-def csa_get_device_status(stream=None) -> int:
-    """Synchronize the stream, then read and clear the device status word."""
+def csa_get_device_status(stream=None, with_site: bool = False):
+    """Synchronize the stream, then read and clear the device status word.
+
+    Returns the status code (0 = OK), or (code, site) with `with_site`."""
     lib = load_library()
     v = ctypes.c_int(0)
-    _check("csa_get_device_status", lib.csa_get_device_status(_stream(stream), ctypes.byref(v)))
-    return v.value
+    site = ctypes.c_int(0)
+    _check("csa_get_device_status", lib.csa_get_device_status(_stream(stream), ctypes.byref(v),
+                                                              ctypes.byref(site)))
+    return (v.value, site.value) if with_site else v.value

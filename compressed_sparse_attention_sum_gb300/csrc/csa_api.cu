@@ -19,6 +19,11 @@ cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const
                                      float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
                                      int d_I, int ratio, int* status, cudaStream_t s);
 bool attn_mma_supported(int H, int d, int window, int K);
+bool attn_tc_supported(int H, int d, int n_c, int K);
+cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx,
+                               const float* sink, float scale, void* o, float* lse, int b, int sq,
+                               int H, int n_c, int ratio, int window, int K, int* status,
+                               cudaStream_t s);
 cudaError_t launch_attn_fwd_mma(const void* q, const void* kv, const int32_t* idx,
                                 const float* sink, float scale, void* o, float* lse, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
@@ -47,7 +52,7 @@ void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 }  // namespace csa
 
 // Device status word (one per device that loads the library).
-static __device__ int g_csa_device_status = 0;
+static __device__ int g_csa_device_status[2] = {0, 0};
 
 namespace {
 
@@ -218,6 +223,13 @@ csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx
     return CSA_ERR_INVALID_ARG;
   const int Kl = idx ? K : n_c;
   cudaStream_t s = (cudaStream_t)stream;
+  // CSA_ATTN_WARP_MMA=1 selects the warp-level mma.sync kernels for bf16 even
+  // where the tcgen05 kernels apply (same results up to rounding order).
+  const char* wm = getenv("CSA_ATTN_WARP_MMA");
+  const bool warp_mma = wm && wm[0] == '1';
+  if (dt == CSA_BF16 && !warp_mma && csa::attn_tc_supported(H, d, n_c, Kl))
+    return from_cuda(csa::launch_attn_fwd_tc(q, kv_full, idx, sink, scale, o, lse, b, sq, H, n_c,
+                                             ratio, window, Kl, device_status_ptr(), s));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
     return from_cuda(csa::launch_attn_fwd_mma(q, kv_full, idx, sink, scale, o, lse, b, sq, H, d,
                                               n_c, ratio, window, Kl, s));
@@ -252,17 +264,18 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
                                              dt == CSA_BF16, s));
 }
 
-csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out) {
+csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out, int* site_out) {
   if (status_out == nullptr) return CSA_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CSA_ERR_CUDA;
   int* p = device_status_ptr();
   if (p == nullptr) return CSA_ERR_CUDA;
-  int v = 0;
-  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
-  const int zero = 0;
-  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+  int v[2] = {0, 0};
+  if (cudaMemcpy(v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  const int zero[2] = {0, 0};
+  if (cudaMemcpy(p, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
     return CSA_ERR_CUDA;
-  *status_out = v;
+  *status_out = v[0];
+  if (site_out != nullptr) *site_out = v[1];
   return CSA_OK;
 }
 

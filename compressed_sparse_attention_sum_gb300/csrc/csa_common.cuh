@@ -18,9 +18,15 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kDevTimeout = 5;
 constexpr int kDevCheck = 6;
 
-__device__ __forceinline__ void set_status(int* status, int code) {
-  if (status != nullptr) atomicCAS(status, 0, code);
+// The device status word is two ints: [0] the first error code, [1] the
+// site that recorded it (which kernel and which wait), for diagnosis.
+__device__ __forceinline__ void set_status(int* status, int code, int site = 0) {
+  if (status != nullptr && atomicCAS(status, 0, code) == 0) atomicExch(status + 1, site);
 }
+
+// Sites recorded with CSA_ERR_TIMEOUT.
+constexpr int kSiteIdxProducer = 0x11, kSiteIdxMma = 0x12, kSiteIdxEpilogue = 0x13;
+constexpr int kSiteFwdQ = 0x21, kSiteFwdS = 0x22, kSiteFwdO = 0x23, kSiteFwdLast = 0x24;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -242,9 +242,16 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
 /*
  * Read and clear the device status word of the current device after the
  * work on `stream` has finished (this call synchronizes `stream`).
- * *status_out receives CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_CHECK.
+ * *status_out receives CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_CHECK (the
+ * first error recorded since the last read).  site_out (nullable) receives
+ * where it was recorded: 0x11-0x13 the indexer's TMA producer, MMA issuer or
+ * epilogue waits; 0x21-0x24 the tensor-core attention forward's waits for the
+ * Q tile, the score MMA, the PV MMA inside the loop and the last PV MMA.
+ * Every device wait of the library is bounded (about one second of wall
+ * time); a wait that gives up records CSA_ERR_TIMEOUT here and its CTA skips
+ * the rest of its work, so the results of that call are not valid.
  */
-csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out);
+csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out, int* site_out);
 
 #ifdef __cplusplus
 }

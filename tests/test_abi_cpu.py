@@ -96,7 +96,7 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.csa_indexer_topk(fake, fake, fake, fake, None, 1, 512, 128, 4, 64, 4, 0, 1, fake,
                                 1 << 20, None) == INVALID
     # device status needs an output pointer
-    assert lib.csa_get_device_status(None, None) == INVALID
+    assert lib.csa_get_device_status(None, None, None) == INVALID
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -175,3 +175,29 @@ def test_indexer_chunked_workspace_identical():
     chunked, sc_chunk = _check_indexer(q_I, k_I, w, 96, 4, ws_bytes=small + 100)
     assert np.array_equal(full, chunked)
     assert torch.equal(sc_full, sc_chunk)
+
+
+# ---------------------------------------------------------------------------
+# tensor-core attention forward (d = 128, H in {16, 32, 64}: rows are
+# (query, head) pairs of consecutive queries over the union of their slots)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H", [16, 32, 64])
+@pytest.mark.parametrize("sink", [True, False])
+@pytest.mark.parametrize("case", [
+    dict(b=2, sq=203, ratio=4, window=16, K=24),    # ragged: sq not a multiple of the block
+    dict(b=1, sq=300, ratio=2, window=130, K=64),   # window longer than one slot tile
+])
+def test_tc_forward_repeated_and_padded_indices(H, sink, case):
+    q, kv, idx, snk, dO = _rand_attn(8, H=H, d=128, dtype="bf16", sink=sink, **case)
+    # more repeats: a block listed three times in one row
+    idx[:, :, 2] = idx[:, :, 0]
+    _run_both(q, kv, idx, snk, dO, case["ratio"], case["window"], "bf16")
+
+
+@pytest.mark.parametrize("H", [16, 32])
+def test_tc_forward_dense_mode_and_large_logits(H):
+    b, sq, ratio, W = 1, 260, 8, 40
+    q, kv, _, snk, dO = _rand_attn(9, b, sq, H, 128, ratio, W, 1, "bf16")
+    q = (q.float() * 4).bfloat16()           # logits spread over a wide range
+    _run_both(q, kv, None, snk, dO, ratio, W, "bf16")
