@@ -1,0 +1,528 @@
+// Sparse MQA backward on the 5th-generation tensor cores (tcgen05 + TMEM),
+// bf16, d = 128.
+//
+// Semantics as csa_attn_bwd ("Add unfused SBHD compressed sparse attention",
+// review of the gather backward: compact [b*n_kv, d] dKV with repeated
+// indices summed; "Add the min-memory DSA attention kernels": fp32 scatter):
+//   D = sum_i p_i dP_i,  p_i = exp(s_i - lse),  ds_i = p_i (dP_i - D),
+//   dq = scale sum_i ds_i kv_i,  dkv_i += p_i dO + scale ds_i q,
+//   dsink = -exp(sink - lse) D.
+//
+// The CTA owns the same 128 (query, head) rows and walks the same union of
+// slots as the tensor-core forward.  TMEM holds four 128-column fp32 blocks:
+// S (rows x slots), dP (rows x slots), the tile's dKV (slots x d) and the
+// running dQ (rows x d).  Pass 1 forms D = sum p dP per row (exact, without
+// the bf16 rounding of the stored O).  Pass 2, per tile of 128 slots:
+//   S = Q K^T, dP = dO V^T                       (K-major A and B)
+//   P as bf16 hi + lo -> smem X, Y;  dKV = P^T dO   (A = P^T and B = dO read
+//                                                  MN-major from the same tiles)
+//   dS*scale as bf16 hi + lo -> X, Y; dKV += dS^T Q; dQ += dS K
+//   dKV (summed over the block's heads and queries inside the MMA) is
+//   scattered into the compact buffer with fp32 vector atomics.
+// The hi/lo split carries ~16 significant bits of P and dS into the
+// products, so the fp32 sums over thousands of queries stay accurate.
+// KV tiles are double-buffered: the next tile's gather overlaps this tile.
+#include "csa_common.cuh"
+#include "csa_kernels.h"
+#include "tcgen05.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace csa {
+namespace atb {
+
+using namespace csa::umma;
+
+constexpr int kRows = 128;
+constexpr int kSlots = 128;
+constexpr int kD = 128;
+constexpr int kThreads = 256;                   // 8 warps: TMEM lane quarter x column half
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDKV = 256, kColDQ = 384;
+constexpr uint32_t kBlk = kRows * 128;          // 16 KB: 128 lines of 128 B
+
+struct Layout {
+  static constexpr uint32_t Q = 0;              // [2][128][128 B] K-major
+  static constexpr uint32_t DO = 2 * kBlk;
+  static constexpr uint32_t KV = 4 * kBlk;      // two buffers of 2 blocks
+  static constexpr uint32_t X = 8 * kBlk;       // P / dS hi
+  static constexpr uint32_t Y = 10 * kBlk;      // P / dS lo
+  static constexpr uint32_t BARS = 12 * kBlk;   // q, sp, p, ds
+  static constexpr uint32_t TSLOT = BARS + 4 * 8;
+  static constexpr uint32_t SCAL = TSLOT + 8;
+  static constexpr uint32_t RED = SCAL + 32;    // [2][128] floats
+  static constexpr uint32_t CONTRIB = RED + 1024;   // [128] floats
+  static constexpr uint32_t BIAS = CONTRIB + 512;   // [2][QB][128] floats
+};
+
+__device__ __forceinline__ uint32_t sw_off(int r, int ch) {
+  return (uint32_t)((ch >> 3) * kBlk + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void cp_async_commit_() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group_() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Store two halves of 8 values as bf16 hi (to X) and bf16 residual (to Y).
+__device__ __forceinline__ void store_hi_lo8(unsigned char* X, unsigned char* Y, uint32_t off,
+                                             const float (&v)[8]) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+    hi[e] = *reinterpret_cast<const uint32_t*>(&h);
+    lo[e] = *reinterpret_cast<const uint32_t*>(&l);
+  }
+  *reinterpret_cast<uint4*>(X + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(Y + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+template <int QB>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_do,
+    const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ idx,
+    const float* __restrict__ sink, float scale, const float* __restrict__ lse,
+    float* __restrict__ dq, float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H,
+    int n_c, int ratio, int window, int K, int* __restrict__ status) {
+  constexpr int NW = (QB + 3) / 4;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + Layout::BARS);
+  uint64_t* bar_sp = bar_q + 1;
+  uint64_t* bar_p = bar_q + 2;
+  uint64_t* bar_ds = bar_q + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Layout::TSLOT);
+  int* scal = reinterpret_cast<int*>(sm + Layout::SCAL);
+  float* red = reinterpret_cast<float*>(sm + Layout::RED);
+  float* contrib = reinterpret_cast<float*>(sm + Layout::CONTRIB);
+  float* bias = reinterpret_cast<float*>(sm + Layout::BIAS);                 // [2][QB][128]
+  uint64_t* cnt = reinterpret_cast<uint64_t*>(bias + 2 * QB * kSlots);       // [n_c][NW]
+  int* ulist = reinterpret_cast<int*>(cnt + (size_t)n_c * NW);               // [n_c]
+  int* wsum = ulist + n_c;                                                   // [8]
+  unsigned char* X = sm + Layout::X;
+  unsigned char* Y = sm + Layout::Y;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bi = blockIdx.y;
+  const int t0 = blockIdx.x * QB;
+  const int n_kv = sq + n_c;
+  const __nv_bfloat16* kv_b = kv + (long long)bi * n_kv * kD;
+  float* dkv_b = dkv + (long long)bi * n_kv * kD;
+
+  // ---- set-up: barriers, TMEM, Q and dO tiles --------------------------------
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(bar_q + i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  for (int e = tid; e < n_c * NW; e += kThreads) cnt[e] = 0ull;
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) {
+    mbar_expect_tx(bar_q, 4 * kBlk);
+    const int row0 = (bi * sq + t0) * H;
+    tma_load_2d(sm + Layout::Q, &tmap_q, bar_q, 0, row0);
+    tma_load_2d(sm + Layout::Q + kBlk, &tmap_q, bar_q, 64, row0);
+    tma_load_2d(sm + Layout::DO, &tmap_do, bar_q, 0, row0);
+    tma_load_2d(sm + Layout::DO + kBlk, &tmap_do, bar_q, 64, row0);
+  }
+
+  // ---- union of the block's selected compressed blocks (as the forward) ------
+  const int t_last = min(t0 + QB, sq) - 1;
+  const int vmax = min((t_last + 1) / ratio, n_c);
+  for (int q = 0; q < QB; ++q) {
+    const int t = t0 + q;
+    if (t >= sq) break;
+    const int vis = min((t + 1) / ratio, n_c);
+    const unsigned long long inc = 1ull << (16 * (q & 3));
+    if (idx != nullptr) {
+      const int32_t* row = idx + ((long long)bi * sq + t) * K;
+      for (int s = tid; s < K; s += kThreads) {
+        const int j = row[s];
+        if (j >= 0 && j < vis)
+          atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[j * NW + (q >> 2)]), inc);
+      }
+    } else {
+      for (int j = tid; j < vis; j += kThreads)
+        atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[j * NW + (q >> 2)]), inc);
+    }
+  }
+  __syncthreads();
+  {
+    const int per = (vmax + kThreads - 1) / kThreads;
+    const int j0 = tid * per, j1 = min(vmax, j0 + per);
+    int c = 0;
+    for (int j = j0; j < j1; ++j) {
+      bool any = false;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) any |= cnt[j * NW + w] != 0ull;
+      c += any;
+    }
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+    int pos = base + incl - c;
+    for (int j = j0; j < j1; ++j) {
+      bool any = false;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) any |= cnt[j * NW + w] != 0ull;
+      if (any) ulist[pos++] = j;
+    }
+    if (tid == kThreads - 1) scal[0] = base + incl;
+  }
+  __syncthreads();
+  const int nu = scal[0];
+  const int win0 = max(0, t0 - window + 1);
+  const int nwin = t_last - win0 + 1;
+  const int S_total = nwin + nu;
+  const int ntiles = (S_total + kSlots - 1) / kSlots;
+
+  auto slot_row = [&](int s) -> int {
+    return s < nwin ? win0 + s : (s < S_total ? sq + ulist[s - nwin] : 0);
+  };
+  // gather tile `it` into KV buffer (it & 1) and its bias table
+  auto stage_tile = [&](int it) {
+    const int sbase = it * kSlots;
+    unsigned char* dst = sm + Layout::KV + (it & 1) * 2 * kBlk;
+    for (int c = tid; c < kSlots * 16; c += kThreads) {
+      const int rr = c >> 4, ch = c & 15;
+      cp_async_16(dst + sw_off(rr, ch), kv_b + (long long)slot_row(sbase + rr) * kD + ch * 8);
+    }
+    cp_async_commit_();
+    float* bt = bias + (it & 1) * QB * kSlots;
+    for (int e = tid; e < QB * kSlots; e += kThreads) {
+      const int qq = e / kSlots, c = e % kSlots;
+      const int s = sbase + c;
+      const int tq = t0 + qq;
+      float bv = -INFINITY;
+      if (tq < sq) {
+        if (s < nwin) {
+          const int raw = win0 + s;
+          if (raw <= tq && raw > tq - window) bv = 0.f;
+        } else if (s < S_total) {
+          const int j = ulist[s - nwin];
+          const uint32_t cq = (uint32_t)(cnt[j * NW + (qq >> 2)] >> (16 * (qq & 3))) & 0xFFFFu;
+          if (cq != 0u) bv = cq == 1u ? 0.f : log2f((float)cq);
+        }
+      }
+      bt[e] = bv;
+    }
+  };
+
+  // ---- per-thread state -------------------------------------------------------
+  const int qd = warp & 3, hf = warp >> 2;
+  const int r = qd * 32 + lane;                    // TMEM lane: row (S, dP, dQ) or slot (dKV)
+  const int q = r / H, h = r % H;
+  const int t = t0 + q;
+  const bool row_ok = t < sq;
+  const float sc2 = scale * kLog2e;
+  const float lse2 = row_ok ? lse[(long long)(bi * sq + t0) * H + r] * kLog2e : INFINITY;
+  const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+  const uint32_t tS = tmem + lane_base + kColS + hf * 64;
+  const uint32_t tDP = tmem + lane_base + kColDP + hf * 64;
+  const uint32_t tDKV = tmem + lane_base + kColDKV + hf * 64;
+  const uint32_t tDQ = tmem + lane_base + kColDQ + hf * 64;
+  uint32_t n_sp = 0;          // completed phases of bar_sp
+  bool ok = __syncthreads_and(mbar_wait(bar_q, 0));
+  int site = ok ? 0 : kSiteBwdQ;
+
+  auto issue_s_dp = [&](int it) {
+    constexpr uint32_t idesc = idesc_bf16_f32_major(kRows, kSlots, 0, 0);
+    const uint32_t qa = smem_addr(sm + Layout::Q), ga = smem_addr(sm + Layout::DO);
+    const uint32_t ka = smem_addr(sm + Layout::KV + (it & 1) * 2 * kBlk);
+#pragma unroll
+    for (int k = 0; k < kD / 16; ++k) {
+      const uint32_t off = (k >> 2) * kBlk + (k & 3) * 32;
+      mma_bf16_ss(tmem + kColS, sw128_desc(qa + off), sw128_desc(ka + off), idesc, k > 0);
+      mma_bf16_ss(tmem + kColDP, sw128_desc(ga + off), sw128_desc(ka + off), idesc, k > 0);
+    }
+    mma_commit(bar_sp);
+  };
+
+  // ---- pass 1: D = sum_i p_i dP_i ------------------------------------------------
+  float dpart = 0.f;
+  if (ok && ntiles > 0) stage_tile(0);
+  for (int it = 0; it < ntiles && ok; ++it) {
+    if (it + 1 < ntiles) {
+      stage_tile(it + 1);
+      cp_async_wait_group_<1>();
+    } else {
+      cp_async_wait_group_<0>();
+    }
+    fence_proxy_async_smem();
+    fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      fence_after();
+      issue_s_dp(it);
+    }
+    ok = __syncthreads_and(mbar_wait(bar_sp, n_sp & 1));
+    ++n_sp;
+    if (!ok) { site = kSiteBwdS; break; }
+    fence_after();
+    const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 64;
+#pragma unroll
+    for (int c4 = 0; c4 < 2; ++c4) {
+      uint32_t vs[32], vp[32];
+      tmem_ld32_wait(tS + c4 * 32, vs);
+      tmem_ld32_wait(tDP + c4 * 32, vp);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c4 * 32 + c]);
+        if (x != -INFINITY) dpart = fmaf(exp2f(x - lse2), __uint_as_float(vp[c]), dpart);
+      }
+    }
+    // the next iteration restages the other bias buffer: every thread must be
+    // done reading this one's predecessor first
+    __syncthreads();
+  }
+  red[hf * kRows + r] = dpart;
+  __syncthreads();
+  const float Drow = red[r] + red[kRows + r];          // fixed order: reproducible
+  // sink gradient: -exp(sink - lse) D, summed over the block's queries per head
+  if (hf == 0)
+    contrib[r] = (row_ok && sink != nullptr) ? -exp2f(sink[h] * kLog2e - lse2) * Drow : 0.f;
+  __syncthreads();
+  if (ok && sink != nullptr && tid < H) {
+    float sacc = 0.f;
+    for (int qq = 0; qq < QB; ++qq) sacc += contrib[qq * H + tid];
+    atomicAdd(&dsink[tid], sacc);
+  }
+
+  // ---- pass 2 -------------------------------------------------------------------------
+  uint32_t n_p = 0, n_ds = 0;
+  if (ok && ntiles > 0) stage_tile(0);
+  for (int it = 0; it < ntiles && ok; ++it) {
+    if (it + 1 < ntiles) {
+      stage_tile(it + 1);
+      cp_async_wait_group_<1>();
+    } else {
+      cp_async_wait_group_<0>();
+    }
+    fence_proxy_async_smem();
+    fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      fence_after();
+      issue_s_dp(it);
+    }
+    ok = __syncthreads_and(mbar_wait(bar_sp, n_sp & 1));
+    ++n_sp;
+    if (!ok) { site = kSiteBwdS; break; }
+    fence_after();
+    const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 64;
+    // P (hi, lo) -> X, Y
+#pragma unroll
+    for (int c4 = 0; c4 < 2; ++c4) {
+      uint32_t vs[32];
+      tmem_ld32_wait(tS + c4 * 32, vs);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float x = fmaf(__uint_as_float(vs[c8 * 8 + e]), sc2, bq[c4 * 32 + c8 * 8 + e]);
+          p[e] = (x == -INFINITY) ? 0.f : exp2f(x - lse2);
+        }
+        store_hi_lo8(X, Y, sw_off(r, hf * 8 + c4 * 4 + c8), p);
+      }
+    }
+    fence_proxy_async_smem();
+    fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      fence_after();
+      // dKV = P^T dO: M = slots, N = d, K = rows; A = P^T (MN-major view of X/Y),
+      // B = dO (MN-major view of its K-major tile)
+      constexpr uint32_t idesc = idesc_bf16_f32_major(kSlots, kD, 1, 1);
+      const uint32_t xa = smem_addr(X), ya = smem_addr(Y), ga = smem_addr(sm + Layout::DO);
+#pragma unroll
+      for (int k = 0; k < kRows / 16; ++k) {
+        const uint64_t b = sw128_desc_mn(ga + k * 2048, kBlk);
+        mma_bf16_ss(tmem + kColDKV, sw128_desc_mn(xa + k * 2048, kBlk), b, idesc, k > 0);
+        mma_bf16_ss(tmem + kColDKV, sw128_desc_mn(ya + k * 2048, kBlk), b, idesc, 1u);
+      }
+      mma_commit(bar_p);
+    }
+    ok = __syncthreads_and(mbar_wait(bar_p, n_p & 1));
+    ++n_p;
+    if (!ok) { site = kSiteBwdP; break; }
+    fence_after();
+    // dS * scale (hi, lo) -> X, Y
+#pragma unroll
+    for (int c4 = 0; c4 < 2; ++c4) {
+      uint32_t vs[32], vp[32];
+      tmem_ld32_wait(tS + c4 * 32, vs);
+      tmem_ld32_wait(tDP + c4 * 32, vp);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        float ds[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = c8 * 8 + e;
+          const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c4 * 32 + c]);
+          const float p = (x == -INFINITY) ? 0.f : exp2f(x - lse2);
+          ds[e] = p * (__uint_as_float(vp[c]) - Drow) * scale;
+        }
+        store_hi_lo8(X, Y, sw_off(r, hf * 8 + c4 * 4 + c8), ds);
+      }
+    }
+    fence_proxy_async_smem();
+    fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      fence_after();
+      const uint32_t xa = smem_addr(X), ya = smem_addr(Y);
+      const uint32_t qa = smem_addr(sm + Layout::Q);
+      const uint32_t ka = smem_addr(sm + Layout::KV + (it & 1) * 2 * kBlk);
+      // dKV += dS^T Q
+      constexpr uint32_t idesc_kv = idesc_bf16_f32_major(kSlots, kD, 1, 1);
+#pragma unroll
+      for (int k = 0; k < kRows / 16; ++k) {
+        const uint64_t b = sw128_desc_mn(qa + k * 2048, kBlk);
+        mma_bf16_ss(tmem + kColDKV, sw128_desc_mn(xa + k * 2048, kBlk), b, idesc_kv, 1u);
+        mma_bf16_ss(tmem + kColDKV, sw128_desc_mn(ya + k * 2048, kBlk), b, idesc_kv, 1u);
+      }
+      // dQ += dS K: M = rows, N = d, K = slots; A = dS (K-major X/Y), B = KV (MN-major)
+      constexpr uint32_t idesc_q = idesc_bf16_f32_major(kRows, kD, 0, 1);
+#pragma unroll
+      for (int k = 0; k < kSlots / 16; ++k) {
+        const uint32_t aoff = (k >> 2) * kBlk + (k & 3) * 32;
+        const uint64_t b = sw128_desc_mn(ka + k * 2048, kBlk);
+        mma_bf16_ss(tmem + kColDQ, sw128_desc(xa + aoff), b, idesc_q, (it > 0 || k > 0) ? 1u : 0u);
+        mma_bf16_ss(tmem + kColDQ, sw128_desc(ya + aoff), b, idesc_q, 1u);
+      }
+      mma_commit(bar_ds);
+    }
+    ok = __syncthreads_and(mbar_wait(bar_ds, n_ds & 1));
+    ++n_ds;
+    if (!ok) { site = kSiteBwdDS; break; }
+    fence_after();
+    // scatter this tile's dKV rows (TMEM lane = slot) into the compact buffer
+    {
+      const int s = it * kSlots + r;
+      const bool valid = s < S_total;
+      float* drow = dkv_b + (long long)slot_row(s) * kD + hf * 64;
+#pragma unroll
+      for (int c4 = 0; c4 < 2; ++c4) {
+        uint32_t v[32];
+        tmem_ld32_wait(tDKV + c4 * 32, v);
+        if (valid) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            red_add_v4(drow + c4 * 32 + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                       __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+        }
+      }
+    }
+  }
+  if (!ok && tid == 0) set_status(status, kDevTimeout, site);
+  // ---- dq rows -----------------------------------------------------------------
+  if (ok && ntiles > 0) {
+    float* dqrow = dq + ((long long)(bi * sq + t0) * H + r) * kD + hf * 64;
+#pragma unroll
+    for (int c4 = 0; c4 < 2; ++c4) {
+      uint32_t v[32];
+      tmem_ld32_wait(tDQ + c4 * 32, v);
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4*>(dqrow + c4 * 32 + c) =
+              make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                          __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace atb
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn_bwd() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+size_t attn_tc_bwd_smem(int QB, int n_c) {
+  const int NW = (QB + 3) / 4;
+  return 1024 + atb::Layout::BIAS + (size_t)2 * QB * atb::kSlots * 4 + (size_t)n_c * NW * 8 +
+         (size_t)n_c * 4 + 64;
+}
+
+bool make_rows_map(CUtensorMap* m, const void* base, long long rows) {
+  auto encode = encode_fn_bwd();
+  if (encode == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)atb::kD, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)atb::kD * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)atb::kRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+}  // namespace
+
+bool attn_tc_bwd_supported(int H, int d, int n_c, int K) {
+  if (d != 128 || !(H == 16 || H == 32 || H == 64) || K > 65535) return false;
+  if (encode_fn_bwd() == nullptr) return false;
+  return attn_tc_bwd_smem(128 / H, n_c) <= 227 * 1024;
+}
+
+cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx,
+                               const float* sink, float scale, const float* lse, const void* dO,
+                               float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
+                               int ratio, int window, int K, int* status, cudaStream_t s) {
+  CUtensorMap tq, tg;
+  const long long rows = (long long)b * sq * H;
+  if (!make_rows_map(&tq, q, rows) || !make_rows_map(&tg, dO, rows)) return cudaErrorInvalidValue;
+  const int QB = 128 / H;
+  const size_t smem = attn_tc_bwd_smem(QB, n_c);
+  dim3 grid((unsigned)((sq + QB - 1) / QB), (unsigned)b);
+#define CSA_TC_BWD(QQ)                                                                        \
+  {                                                                                           \
+    auto k = atb::attn_bwd_tc_kernel<QQ>;                                                     \
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);         \
+    k<<<grid, atb::kThreads, smem, s>>>(tq, tg, (const __nv_bfloat16*)kv, idx, sink, scale, \
+                                        lse, dq, dkv, dsink, sq, H, n_c, ratio, window, K,  \
+                                        status);                                              \
+    count_launches(1);                                                                        \
+  }
+  if (QB == 8) CSA_TC_BWD(8)
+  else if (QB == 4) CSA_TC_BWD(4)
+  else CSA_TC_BWD(2)
+#undef CSA_TC_BWD
+  return cudaGetLastError();
+}
+
+}  // namespace csa

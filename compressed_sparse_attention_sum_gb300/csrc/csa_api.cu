@@ -20,6 +20,11 @@ cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const
                                      int d_I, int ratio, int* status, cudaStream_t s);
 bool attn_mma_supported(int H, int d, int window, int K);
 bool attn_tc_supported(int H, int d, int n_c, int K);
+bool attn_tc_bwd_supported(int H, int d, int n_c, int K);
+cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx,
+                               const float* sink, float scale, const float* lse, const void* dO,
+                               float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
+                               int ratio, int window, int K, int* status, cudaStream_t s);
 cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx,
                                const float* sink, float scale, void* o, float* lse, int b, int sq,
                                int H, int n_c, int ratio, int window, int K, int* status,
@@ -256,6 +261,12 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
   cudaError_t e = csa::launch_zero_f32(dkv, (size_t)b * n_kv * d, s);
   if (e == cudaSuccess && dsink != nullptr) e = csa::launch_zero_f32(dsink, (size_t)H, s);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
+  const char* wm = getenv("CSA_ATTN_WARP_MMA");
+  const bool warp_mma = wm && wm[0] == '1';
+  if (dt == CSA_BF16 && !warp_mma && csa::attn_tc_bwd_supported(H, d, n_c, Kl))
+    return from_cuda(csa::launch_attn_bwd_tc(q, kv_full, idx, sink, scale, lse, dO, dq, dkv,
+                                             dsink, b, sq, H, n_c, ratio, window, Kl,
+                                             device_status_ptr(), s));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
     return from_cuda(csa::launch_attn_bwd_mma(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                               dsink, b, sq, H, d, n_c, ratio, window, Kl, s));

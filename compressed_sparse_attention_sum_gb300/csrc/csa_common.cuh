@@ -27,6 +27,7 @@ __device__ __forceinline__ void set_status(int* status, int code, int site = 0) 
 // Sites recorded with CSA_ERR_TIMEOUT.
 constexpr int kSiteIdxProducer = 0x11, kSiteIdxMma = 0x12, kSiteIdxEpilogue = 0x13;
 constexpr int kSiteFwdQ = 0x21, kSiteFwdS = 0x22, kSiteFwdO = 0x23, kSiteFwdLast = 0x24;
+constexpr int kSiteBwdQ = 0x31, kSiteBwdS = 0x32, kSiteBwdP = 0x33, kSiteBwdDS = 0x34;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }

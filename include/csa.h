@@ -246,7 +246,9 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
  * first error recorded since the last read).  site_out (nullable) receives
  * where it was recorded: 0x11-0x13 the indexer's TMA producer, MMA issuer or
  * epilogue waits; 0x21-0x24 the tensor-core attention forward's waits for the
- * Q tile, the score MMA, the PV MMA inside the loop and the last PV MMA.
+ * Q tile, the score MMA, the PV MMA inside the loop and the last PV MMA;
+ * 0x31-0x34 the tensor-core backward's waits for the Q/dO tiles, the S/dP
+ * MMAs, the P^T dO MMAs and the dS MMAs.
  * Every device wait of the library is bounded (about one second of wall
  * time); a wait that gives up records CSA_ERR_TIMEOUT here and its CTA skips
  * the rest of its work, so the results of that call are not valid.
