@@ -11,8 +11,11 @@
 // The CTA owns the same 128 (query, head) rows and walks the same union of
 // slots as the tensor-core forward.  TMEM holds four 128-column fp32 blocks:
 // S (rows x slots), dP (rows x slots), the tile's dKV (slots x d) and the
-// running dQ (rows x d).  Pass 1 forms D = sum p dP per row (exact, without
-// the bf16 rounding of the stored O).  Pass 2, per tile of 128 slots:
+// running dQ (rows x d).  Pass 1 forms D = sum p dP per row exactly (the
+// bf16 rounding of the stored O would move dq and dkv by up to 1e-2 when a
+// query has few slots); during pass 1 the dKV/dQ columns are free, so S and dP
+// alternate between two TMEM buffers and the next tile's MMAs overlap this
+// tile's sum.  Pass 2, per tile of 128 slots:
 //   S = Q K^T, dP = dO V^T                       (K-major A and B)
 //   P as bf16 hi + lo -> smem X, Y;  dKV = P^T dO   (A = P^T and B = dO read
 //                                                  MN-major from the same tiles)
@@ -36,7 +39,8 @@ using namespace csa::umma;
 constexpr int kRows = 128;
 constexpr int kSlots = 128;
 constexpr int kD = 128;
-constexpr int kThreads = 256;                   // 8 warps: TMEM lane quarter x column half
+constexpr int kThreads = 512;                   // 16 warps: TMEM lane quarter x column quarter
+constexpr int kCG = 4;                          // column groups of 32
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDKV = 256, kColDQ = 384;
 constexpr uint32_t kBlk = kRows * 128;          // 16 KB: 128 lines of 128 B
@@ -47,11 +51,11 @@ struct Layout {
   static constexpr uint32_t KV = 4 * kBlk;      // two buffers of 2 blocks
   static constexpr uint32_t X = 8 * kBlk;       // P / dS hi
   static constexpr uint32_t Y = 10 * kBlk;      // P / dS lo
-  static constexpr uint32_t BARS = 12 * kBlk;   // q, sp, p, ds
-  static constexpr uint32_t TSLOT = BARS + 4 * 8;
+  static constexpr uint32_t BARS = 12 * kBlk;   // q, sp, p, ds, pass-1 buffers 0/1
+  static constexpr uint32_t TSLOT = BARS + 6 * 8;
   static constexpr uint32_t SCAL = TSLOT + 8;
-  static constexpr uint32_t RED = SCAL + 32;    // [2][128] floats
-  static constexpr uint32_t CONTRIB = RED + 1024;   // [128] floats
+  static constexpr uint32_t RED = SCAL + 64;    // [4][128] floats
+  static constexpr uint32_t CONTRIB = RED + 2048;   // [128] floats
   static constexpr uint32_t BIAS = CONTRIB + 512;   // [2][QB][128] floats
 };
 
@@ -86,9 +90,10 @@ __device__ __forceinline__ void store_hi_lo8(unsigned char* X, unsigned char* Y,
 template <int QB>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_do,
-    const __nv_bfloat16* __restrict__ kv, const int32_t* __restrict__ idx,
-    const float* __restrict__ sink, float scale, const float* __restrict__ lse,
-    float* __restrict__ dq, float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H,
+    const __nv_bfloat16* __restrict__ kv, const __nv_bfloat16* __restrict__ dO_g,
+    const int32_t* __restrict__ idx,
+    const float* __restrict__ sink, float scale, const __nv_bfloat16* __restrict__ o,
+    const float* __restrict__ lse, float* __restrict__ dq, float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H,
     int n_c, int ratio, int window, int K, int* __restrict__ status) {
   constexpr int NW = (QB + 3) / 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -98,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   uint64_t* bar_sp = bar_q + 1;
   uint64_t* bar_p = bar_q + 2;
   uint64_t* bar_ds = bar_q + 3;
+  uint64_t* bar_d1 = bar_q + 4;          // [2] pass-1 S/dP buffers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Layout::TSLOT);
   int* scal = reinterpret_cast<int*>(sm + Layout::SCAL);
   float* red = reinterpret_cast<float*>(sm + Layout::RED);
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   float* bias = reinterpret_cast<float*>(sm + Layout::BIAS);                 // [2][QB][128]
   uint64_t* cnt = reinterpret_cast<uint64_t*>(bias + 2 * QB * kSlots);       // [n_c][NW]
   int* ulist = reinterpret_cast<int*>(cnt + (size_t)n_c * NW);               // [n_c]
-  int* wsum = ulist + n_c;                                                   // [8]
+  int* wsum = ulist + n_c;                                                   // [16]
   unsigned char* X = sm + Layout::X;
   unsigned char* Y = sm + Layout::Y;
 
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
 
   // ---- set-up: barriers, TMEM, Q and dO tiles --------------------------------
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(bar_q + i, 1);
+    for (int i = 0; i < 6; ++i) mbar_init(bar_q + i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   };
 
   // ---- per-thread state -------------------------------------------------------
-  const int qd = warp & 3, hf = warp >> 2;
+  const int qd = warp & 3, hf = warp >> 2;         // hf: column group (32 columns)
   const int r = qd * 32 + lane;                    // TMEM lane: row (S, dP, dQ) or slot (dKV)
   const int q = r / H, h = r % H;
   const int t = t0 + q;
@@ -234,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   const float sc2 = scale * kLog2e;
   const float lse2 = row_ok ? lse[(long long)(bi * sq + t0) * H + r] * kLog2e : INFINITY;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-  const uint32_t tS = tmem + lane_base + kColS + hf * 64;
-  const uint32_t tDP = tmem + lane_base + kColDP + hf * 64;
-  const uint32_t tDKV = tmem + lane_base + kColDKV + hf * 64;
-  const uint32_t tDQ = tmem + lane_base + kColDQ + hf * 64;
+  const uint32_t tS = tmem + lane_base + kColS + hf * 32;
+  const uint32_t tDP = tmem + lane_base + kColDP + hf * 32;
+  const uint32_t tDKV = tmem + lane_base + kColDKV + hf * 32;
+  const uint32_t tDQ = tmem + lane_base + kColDQ + hf * 32;
   uint32_t n_sp = 0;          // completed phases of bar_sp
   bool ok = __syncthreads_and(mbar_wait(bar_q, 0));
   int site = ok ? 0 : kSiteBwdQ;
@@ -255,92 +261,114 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     mma_commit(bar_sp);
   };
 
-  // ---- pass 1: D = sum_i p_i dP_i ------------------------------------------------
-  float dpart = 0.f;
-  if (ok && ntiles > 0) stage_tile(0);
-  for (int it = 0; it < ntiles && ok; ++it) {
-    if (it + 1 < ntiles) {
-      stage_tile(it + 1);
-      cp_async_wait_group_<1>();
-    } else {
-      cp_async_wait_group_<0>();
-    }
-    fence_proxy_async_smem();
-    fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      fence_after();
-      issue_s_dp(it);
-    }
-    ok = __syncthreads_and(mbar_wait(bar_sp, n_sp & 1));
-    ++n_sp;
-    if (!ok) { site = kSiteBwdS; break; }
-    fence_after();
-    const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 64;
+  // ---- pass 1: D = sum_i p_i dP_i (S/dP double-buffered in TMEM) --------------------
+  {
+    auto issue_pass1 = [&](int it) {
+      constexpr uint32_t idesc = idesc_bf16_f32_major(kRows, kSlots, 0, 0);
+      const uint32_t qa = smem_addr(sm + Layout::Q), ga = smem_addr(sm + Layout::DO);
+      const uint32_t ka = smem_addr(sm + Layout::KV + (it & 1) * 2 * kBlk);
+      const uint32_t cs = (it & 1) * 256;
 #pragma unroll
-    for (int c4 = 0; c4 < 2; ++c4) {
-      uint32_t vs[32], vp[32];
-      tmem_ld32_wait(tS + c4 * 32, vs);
-      tmem_ld32_wait(tDP + c4 * 32, vp);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c4 * 32 + c]);
-        if (x != -INFINITY) dpart = fmaf(exp2f(x - lse2), __uint_as_float(vp[c]), dpart);
+      for (int k = 0; k < kD / 16; ++k) {
+        const uint32_t off = (k >> 2) * kBlk + (k & 3) * 32;
+        mma_bf16_ss(tmem + cs, sw128_desc(qa + off), sw128_desc(ka + off), idesc, k > 0);
+        mma_bf16_ss(tmem + cs + 128, sw128_desc(ga + off), sw128_desc(ka + off), idesc, k > 0);
+      }
+      mma_commit(&bar_d1[it & 1]);
+    };
+    float dpart = 0.f;
+    if (ok && ntiles > 0) {
+      stage_tile(0);
+      if (ntiles > 1) {
+        stage_tile(1);
+        cp_async_wait_group_<1>();
+      } else {
+        cp_async_wait_group_<0>();
+      }
+      fence_proxy_async_smem();
+      fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        fence_after();
+        issue_pass1(0);
       }
     }
-    // the next iteration restages the other bias buffer: every thread must be
-    // done reading this one's predecessor first
-    __syncthreads();
-  }
-  red[hf * kRows + r] = dpart;
-  __syncthreads();
-  const float Drow = red[r] + red[kRows + r];          // fixed order: reproducible
-  // sink gradient: -exp(sink - lse) D, summed over the block's queries per head
-  if (hf == 0)
-    contrib[r] = (row_ok && sink != nullptr) ? -exp2f(sink[h] * kLog2e - lse2) * Drow : 0.f;
-  __syncthreads();
-  if (ok && sink != nullptr && tid < H) {
-    float sacc = 0.f;
-    for (int qq = 0; qq < QB; ++qq) sacc += contrib[qq * H + tid];
-    atomicAdd(&dsink[tid], sacc);
-  }
-
-  // ---- pass 2 -------------------------------------------------------------------------
-  uint32_t n_p = 0, n_ds = 0;
-  if (ok && ntiles > 0) stage_tile(0);
-  for (int it = 0; it < ntiles && ok; ++it) {
-    if (it + 1 < ntiles) {
-      stage_tile(it + 1);
-      cp_async_wait_group_<1>();
-    } else {
-      cp_async_wait_group_<0>();
+    for (int it = 0; it < ntiles && ok; ++it) {
+      if (it + 1 < ntiles) {
+        // tile it+1 is staged: start its MMAs into the other TMEM buffer
+        cp_async_wait_group_<0>();
+        fence_proxy_async_smem();
+        fence_before();
+        __syncthreads();
+        if (tid == 0) {
+          fence_after();
+          issue_pass1(it + 1);
+        }
+      }
+      ok = __syncthreads_and(mbar_wait(&bar_d1[it & 1], (it >> 1) & 1));
+      if (!ok) { site = kSiteBwdS; break; }
+      fence_after();
+      const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 32;
+      const uint32_t cs = lane_base + (it & 1) * 256 + hf * 32;
+      {
+        uint32_t vs[32], vp[32];
+        CSA_TMEM_LD32(tmem + cs, vs);
+        CSA_TMEM_LD32(tmem + cs + 128, vp);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        CSA_TMEM_WAIT32(vs);
+        CSA_TMEM_WAIT32(vp);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c]);
+          if (x != -INFINITY) dpart = fmaf(exp2f(x - lse2), __uint_as_float(vp[c]), dpart);
+        }
+      }
+      fence_before();
+      // everyone is done with this tile's bias table and TMEM buffer; its KV
+      // buffer was released when its MMAs completed: stage tile it+2 there
+      __syncthreads();
+      if (it + 2 < ntiles) stage_tile(it + 2);
     }
+    red[hf * kRows + r] = dpart;
+  }
+  __syncthreads();
+  const float Drow = (red[r] + red[kRows + r]) + (red[2 * kRows + r] + red[3 * kRows + r]);
+
+  // ---- pass 2 ---------------------------------------------------------------------
+  uint32_t n_p = 0, n_ds = 0;
+  if (ok && ntiles > 0) {
+    stage_tile(0);
+    cp_async_wait_group_<0>();
     fence_proxy_async_smem();
     fence_before();
     __syncthreads();
     if (tid == 0) {
       fence_after();
-      issue_s_dp(it);
+      issue_s_dp(0);
     }
+  }
+  for (int it = 0; it < ntiles && ok; ++it) {
+    // the next tile's gather overlaps this tile (its buffers were released
+    // when the previous tile's MMAs completed)
+    if (it + 1 < ntiles) stage_tile(it + 1);
     ok = __syncthreads_and(mbar_wait(bar_sp, n_sp & 1));
     ++n_sp;
     if (!ok) { site = kSiteBwdS; break; }
     fence_after();
-    const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 64;
+    const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 32;
     // P (hi, lo) -> X, Y
-#pragma unroll
-    for (int c4 = 0; c4 < 2; ++c4) {
+    {
       uint32_t vs[32];
-      tmem_ld32_wait(tS + c4 * 32, vs);
+      tmem_ld32_wait(tS, vs);
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float x = fmaf(__uint_as_float(vs[c8 * 8 + e]), sc2, bq[c4 * 32 + c8 * 8 + e]);
+          const float x = fmaf(__uint_as_float(vs[c8 * 8 + e]), sc2, bq[c8 * 8 + e]);
           p[e] = (x == -INFINITY) ? 0.f : exp2f(x - lse2);
         }
-        store_hi_lo8(X, Y, sw_off(r, hf * 8 + c4 * 4 + c8), p);
+        store_hi_lo8(X, Y, sw_off(r, hf * 4 + c8), p);
       }
     }
     fence_proxy_async_smem();
@@ -365,24 +393,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     if (!ok) { site = kSiteBwdP; break; }
     fence_after();
     // dS * scale (hi, lo) -> X, Y
-#pragma unroll
-    for (int c4 = 0; c4 < 2; ++c4) {
+    {
       uint32_t vs[32], vp[32];
-      tmem_ld32_wait(tS + c4 * 32, vs);
-      tmem_ld32_wait(tDP + c4 * 32, vp);
+      CSA_TMEM_LD32(tS, vs);
+      CSA_TMEM_LD32(tDP, vp);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      CSA_TMEM_WAIT32(vs);
+      CSA_TMEM_WAIT32(vp);
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         float ds[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int c = c8 * 8 + e;
-          const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c4 * 32 + c]);
+          const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c]);
           const float p = (x == -INFINITY) ? 0.f : exp2f(x - lse2);
           ds[e] = p * (__uint_as_float(vp[c]) - Drow) * scale;
         }
-        store_hi_lo8(X, Y, sw_off(r, hf * 8 + c4 * 4 + c8), ds);
+        store_hi_lo8(X, Y, sw_off(r, hf * 4 + c8), ds);
       }
     }
+    if (it + 1 < ntiles) cp_async_wait_group_<0>();
     fence_proxy_async_smem();
     fence_before();
     __syncthreads();
@@ -409,44 +440,51 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
         mma_bf16_ss(tmem + kColDQ, sw128_desc(ya + aoff), b, idesc_q, 1u);
       }
       mma_commit(bar_ds);
+      // S and dP of the next tile (S/dP were fully read above)
+      if (it + 1 < ntiles) issue_s_dp(it + 1);
     }
     ok = __syncthreads_and(mbar_wait(bar_ds, n_ds & 1));
     ++n_ds;
     if (!ok) { site = kSiteBwdDS; break; }
     fence_after();
-    // scatter this tile's dKV rows (TMEM lane = slot) into the compact buffer
+    // scatter this tile's dKV rows (TMEM lane = slot) into the compact buffer,
+    // while the tensor core computes the next tile's S and dP
     {
       const int s = it * kSlots + r;
       const bool valid = s < S_total;
-      float* drow = dkv_b + (long long)slot_row(s) * kD + hf * 64;
+      float* drow = dkv_b + (long long)slot_row(s) * kD + hf * 32;
+      uint32_t v[32];
+      tmem_ld32_wait(tDKV, v);
+      if (valid) {
 #pragma unroll
-      for (int c4 = 0; c4 < 2; ++c4) {
-        uint32_t v[32];
-        tmem_ld32_wait(tDKV + c4 * 32, v);
-        if (valid) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            red_add_v4(drow + c4 * 32 + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                       __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-        }
+        for (int c = 0; c < 32; c += 4)
+          red_add_v4(drow + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                     __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
       }
     }
+    fence_before();
+  }
+  // ---- sink gradient: -exp(sink - lse) D, summed over the block's queries per head --
+  if (hf == 0)
+    contrib[r] = (row_ok && sink != nullptr) ? -exp2f(sink[h] * kLog2e - lse2) * Drow : 0.f;
+  __syncthreads();
+  if (ok && sink != nullptr && tid < H) {
+    float sacc = 0.f;
+    for (int qq = 0; qq < QB; ++qq) sacc += contrib[qq * H + tid];
+    atomicAdd(&dsink[tid], sacc);
   }
   if (!ok && tid == 0) set_status(status, kDevTimeout, site);
   // ---- dq rows -----------------------------------------------------------------
   if (ok && ntiles > 0) {
-    float* dqrow = dq + ((long long)(bi * sq + t0) * H + r) * kD + hf * 64;
+    float* dqrow = dq + ((long long)(bi * sq + t0) * H + r) * kD + hf * 32;
+    uint32_t v[32];
+    tmem_ld32_wait(tDQ, v);
+    if (row_ok) {
 #pragma unroll
-    for (int c4 = 0; c4 < 2; ++c4) {
-      uint32_t v[32];
-      tmem_ld32_wait(tDQ + c4 * 32, v);
-      if (row_ok) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          *reinterpret_cast<float4*>(dqrow + c4 * 32 + c) =
-              make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                          __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-      }
+      for (int c = 0; c < 32; c += 4)
+        *reinterpret_cast<float4*>(dqrow + c) =
+            make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                        __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
     }
   }
   fence_before();
@@ -500,7 +538,8 @@ bool attn_tc_bwd_supported(int H, int d, int n_c, int K) {
 }
 
 cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx,
-                               const float* sink, float scale, const float* lse, const void* dO,
+                               const float* sink, float scale, const void* o, const float* lse,
+                               const void* dO,
                                float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
                                int ratio, int window, int K, int* status, cudaStream_t s) {
   CUtensorMap tq, tg;
@@ -513,9 +552,10 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
   {                                                                                           \
     auto k = atb::attn_bwd_tc_kernel<QQ>;                                                     \
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);         \
-    k<<<grid, atb::kThreads, smem, s>>>(tq, tg, (const __nv_bfloat16*)kv, idx, sink, scale, \
-                                        lse, dq, dkv, dsink, sq, H, n_c, ratio, window, K,  \
-                                        status);                                              \
+    k<<<grid, atb::kThreads, smem, s>>>(tq, tg, (const __nv_bfloat16*)kv,                   \
+                                        (const __nv_bfloat16*)dO, idx, sink, scale,           \
+                                        (const __nv_bfloat16*)o, lse, dq, dkv, dsink, sq, H,  \
+                                        n_c, ratio, window, K, status);                       \
     count_launches(1);                                                                        \
   }
   if (QB == 8) CSA_TC_BWD(8)

@@ -22,7 +22,8 @@ bool attn_mma_supported(int H, int d, int window, int K);
 bool attn_tc_supported(int H, int d, int n_c, int K);
 bool attn_tc_bwd_supported(int H, int d, int n_c, int K);
 cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx,
-                               const float* sink, float scale, const float* lse, const void* dO,
+                               const float* sink, float scale, const void* o, const float* lse,
+                               const void* dO,
                                float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
                                int ratio, int window, int K, int* status, cudaStream_t s);
 cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx,
@@ -264,7 +265,7 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
   const char* wm = getenv("CSA_ATTN_WARP_MMA");
   const bool warp_mma = wm && wm[0] == '1';
   if (dt == CSA_BF16 && !warp_mma && csa::attn_tc_bwd_supported(H, d, n_c, Kl))
-    return from_cuda(csa::launch_attn_bwd_tc(q, kv_full, idx, sink, scale, lse, dO, dq, dkv,
+    return from_cuda(csa::launch_attn_bwd_tc(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                              dsink, b, sq, H, n_c, ratio, window, Kl,
                                              device_status_ptr(), s));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
