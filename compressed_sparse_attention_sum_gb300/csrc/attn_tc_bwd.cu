@@ -448,19 +448,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     if (!ok) { site = kSiteBwdDS; break; }
     fence_after();
     // scatter this tile's dKV rows (TMEM lane = slot) into the compact buffer,
-    // while the tensor core computes the next tile's S and dP
+    // while the tensor core computes the next tile's S and dP: stage the fp32
+    // rows contiguously in X|Y (free until the next tile's P), then one bulk
+    // asynchronous add of 512 B per valid slot row
     {
-      const int s = it * kSlots + r;
-      const bool valid = s < S_total;
-      float* drow = dkv_b + (long long)slot_row(s) * kD + hf * 32;
+      float* stg = reinterpret_cast<float*>(X);          // [128 slots][128] fp32 = 64 KB
       uint32_t v[32];
       tmem_ld32_wait(tDKV, v);
-      if (valid) {
+      float* srow = stg + r * kD + hf * 32;
+      // Store chunk (c + lane) % 8 at step c so that the 32 lanes (32 rows,
+      // 512 B apart) hit different banks: rotate the eight 4-float chunks by
+      // lane % 8 with a 3-stage barrel shift (static register indices only).
+      float4 ch[8];
 #pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          red_add_v4(drow + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                     __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+      for (int c = 0; c < 8; ++c)
+        ch[c] = make_float4(__uint_as_float(v[c * 4]), __uint_as_float(v[c * 4 + 1]),
+                            __uint_as_float(v[c * 4 + 2]), __uint_as_float(v[c * 4 + 3]));
+#pragma unroll
+      for (int k = 1; k < 8; k <<= 1) {
+        const bool rot = (lane & k) != 0;
+        float4 tmp[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) tmp[c] = rot ? ch[(c + k) & 7] : ch[c];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) ch[c] = tmp[c];
       }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4*>(srow + ((c + lane) & 7) * 4) = ch[c];
+      fence_proxy_async_smem();
+      __syncthreads();
+      const int s = it * kSlots + tid;
+      if (tid < kSlots && s < S_total) {
+        bulk_reduce_add_f32(dkv_b + (long long)slot_row(s) * kD, stg + tid * kD, kD * 4);
+        bulk_commit();
+      }
+      // X|Y are rewritten by the next tile: its readers wait for the bulk reads
+      if (tid < kSlots) bulk_wait_read_all();
     }
     fence_before();
   }
