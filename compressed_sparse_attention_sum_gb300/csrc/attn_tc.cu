@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
     }
     // ---- pass 2: P = exp2(x - m) to shared memory (bf16), partial row sum ---------
     float psum = 0.f;
+    const float mref = m_run == -INFINITY ? 0.f : m_run;
     unsigned char* pbuf = sm + Layout::P;
 #pragma unroll
     for (int c4 = 0; c4 < 2; ++c4) {
@@ -282,8 +283,10 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
+          // masked slots: x = -inf and 2^-inf = 0; rows with m_run = -inf have
+          // every x = -inf as well, guarded so that -inf - -inf never occurs
           const float x = fmaf(__uint_as_float(v[c8 * 8 + e]), sc2, biasq[c4 * 32 + c8 * 8 + e]);
-          p[e] = (x == -INFINITY) ? 0.f : exp2f(x - m_run);
+          p[e] = ex2(x - mref);
           psum += p[e];
         }
         uint4 u;

@@ -318,10 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
         CSA_TMEM_WAIT32(vs);
         CSA_TMEM_WAIT32(vp);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c]);
-          if (x != -INFINITY) dpart = fmaf(exp2f(x - lse2), __uint_as_float(vp[c]), dpart);
-        }
+        for (int c = 0; c < 32; ++c)
+          dpart = fmaf(ex2(fmaf(__uint_as_float(vs[c]), sc2, bq[c] - lse2)),
+                       __uint_as_float(vp[c]), dpart);
       }
       fence_before();
       // everyone is done with this tile's bias table and TMEM buffer; its KV
@@ -365,11 +364,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float x = fmaf(__uint_as_float(vs[c8 * 8 + e]), sc2, bq[c8 * 8 + e]);
-          p[e] = (x == -INFINITY) ? 0.f : exp2f(x - lse2);
+          p[e] = ex2(fmaf(__uint_as_float(vs[c8 * 8 + e]), sc2, bq[c8 * 8 + e] - lse2));
+          vs[c8 * 8 + e] = __float_as_uint(p[e]);
         }
         store_hi_lo8(X, Y, sw_off(r, hf * 4 + c8), p);
       }
+      // keep P (fp32) in the S columns for the dS step
+      CSA_TMEM_ST32(tS, vs);
+      tmem_wait_st();
     }
     fence_proxy_async_smem();
     fence_before();
@@ -405,10 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
         float ds[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;
-          const float x = fmaf(__uint_as_float(vs[c]), sc2, bq[c]);
-          const float p = (x == -INFINITY) ? 0.f : exp2f(x - lse2);
-          ds[e] = p * (__uint_as_float(vp[c]) - Drow) * scale;
+          const int c = c8 * 8 + e;         // vs now holds P
+          ds[e] = __uint_as_float(vs[c]) * (__uint_as_float(vp[c]) - Drow) * scale;
         }
         store_hi_lo8(X, Y, sw_off(r, hf * 4 + c8), ds);
       }

@@ -240,5 +240,13 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22; 2^-inf = +0, which the softmax code relies on for masked slots).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace umma
 }  // namespace csa
