@@ -162,7 +162,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
@@ -276,6 +276,8 @@ def run_gpu(args, rank, world, local_rank):
         ev[4].record(stream)
         return ev
 
+    clk = ClockSampler(local_rank)
+    clk.__enter__()          # samples from the warm-up through the end-to-end loop
     for _ in range(args.warmup):
         flush.zero_()
         step(d_in)
@@ -288,11 +290,10 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     evs = []
     launches0 = lib.csa_kernel_launches()
-    with ClockSampler(local_rank) as clk:
-        for _ in range(args.steps):
-            flush.zero_()
-            evs.append(step(d_in))
-        torch.cuda.synchronize()
+    for _ in range(args.steps):
+        flush.zero_()
+        evs.append(step(d_in))
+    torch.cuda.synchronize()
     launches = lib.csa_kernel_launches() - launches0
     if world > 1:
         torch.distributed.barrier()
@@ -328,6 +329,7 @@ def run_gpu(args, rank, world, local_rank):
         e1.synchronize()
         if it >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
+    clk.__exit__(None, None, None)
     e2e = sum(e2e_ms) / len(e2e_ms)
     if world > 1:
         t = torch.tensor([e2e], device=dev)
@@ -445,7 +447,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)

@@ -211,6 +211,123 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
   }
 }
 
+// Register-resident variant for rows of at most 32*PER candidates: lane l
+// holds the keys of blocks l, l+32, ...  A pass whose chosen bin holds exactly
+// the remaining count ends the search early: every key with the selected
+// prefix is taken and no tie needs breaking.
+template <int PER>
+__global__ void __launch_bounds__(256) topk_select_reg_kernel(const float* __restrict__ ws,
+                                                              int32_t* __restrict__ out_idx,
+                                                              float* __restrict__ out_score,
+                                                              int t0, int nt, int b, int sq,
+                                                              int n_c, int ratio, int K) {
+  __shared__ int hist_all[8][256];
+  const int warps = blockDim.x / 32;
+  const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const unsigned FULL = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int* hist = hist_all[wid];
+  const int r = blockIdx.x * warps + wid;
+  if (r >= b * nt) return;
+  const int bi = r / nt, t = t0 + r % nt;
+  const int vis = min((t + 1) / ratio, n_c);
+  const float* row = ws + (size_t)r * n_c;
+  int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
+  float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
+  if (vis <= K) {
+    for (int s = lane; s < K; s += 32) {
+      oi[s] = s < vis ? s : -1;
+      if (os) os[s] = s < vis ? row[s] : 0.f;
+    }
+    return;
+  }
+  uint32_t key[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int j = lane + 32 * i;
+    key[i] = j < vis ? order_key(row[j]) : 0u;      // 0: below every valid key
+  }
+  uint32_t prefix = 0, pmask = 0;
+  int need = K;
+  bool exact = false;                                  // true: a bin matched `need` exactly
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int j = lane + 32 * i;
+      if (j < vis && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+    }
+    __syncwarp();
+    int cnt[8];
+    int tot = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cnt[i] = hist[8 * (31 - lane) + 7 - i];
+      tot += cnt[i];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int excl = incl - tot;
+    const bool mine = (excl < need) && (need <= incl);
+    const int src = __ffs(__ballot_sync(FULL, mine)) - 1;
+    int bin = 0, above = 0, inbin = 0;
+    if (mine) {
+      int run = excl;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (run + cnt[i] >= need) {
+          bin = 8 * (31 - lane) + 7 - i;
+          above = run;
+          inbin = cnt[i];
+          break;
+        }
+        run += cnt[i];
+      }
+    }
+    bin = __shfl_sync(FULL, bin, src);
+    above = __shfl_sync(FULL, above, src);
+    inbin = __shfl_sync(FULL, inbin, src);
+    need -= above;
+    prefix |= (uint32_t)bin << shift;
+    pmask |= 255u << shift;
+    __syncwarp();
+    if (inbin == need) {
+      exact = true;
+      break;
+    }
+  }
+  int out_pos = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int j = lane + 32 * i;
+    if (32 * i >= vis) break;
+    const uint32_t u = key[i];
+    const bool valid = j < vis;
+    bool sel;
+    unsigned eqm = 0u;
+    if (exact) {
+      sel = valid && (u & pmask) >= prefix;
+    } else {
+      const bool eq = valid && u == prefix;
+      eqm = __ballot_sync(FULL, eq);
+      sel = (valid && u > prefix) || (eq && (eq_seen + __popc(eqm & lt_mask)) < need);
+    }
+    const unsigned selm = __ballot_sync(FULL, sel);
+    if (sel) {
+      const int p = out_pos + __popc(selm & lt_mask);
+      oi[p] = j;
+      if (os) os[p] = row[j];
+    }
+    out_pos += __popc(selm);
+    eq_seen += __popc(eqm);
+  }
+}
+
 cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, const float* w,
                                        float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
                                        int d_I, int ratio, bool bf16, cudaStream_t s) {
@@ -234,16 +351,29 @@ cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, con
 
 cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
                                int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s) {
+  const int rows = b * nt;
+  if (n_c <= 2048) {
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+#define CSA_SEL(P)                                                                            \
+  topk_select_reg_kernel<P><<<grid, 256, 0, s>>>(ws, topk_idx, topk_score, t0, nt, b, sq, n_c, \
+                                                 ratio, K);                                   \
+  count_launches(1);
+    if (n_c <= 256) { CSA_SEL(8) }
+    else if (n_c <= 512) { CSA_SEL(16) }
+    else if (n_c <= 1024) { CSA_SEL(32) }
+    else { CSA_SEL(64) }
+#undef CSA_SEL
+    return cudaGetLastError();
+  }
   const size_t per_warp = (size_t)(n_c + 256) * sizeof(uint32_t);
   int warps = (int)((200 * 1024) / per_warp);
   warps = warps < 1 ? 1 : (warps > 8 ? 8 : warps);
   const size_t smem = per_warp * warps;
-  const int rows = b * nt;
   dim3 grid((unsigned)((rows + warps - 1) / warps));
   cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   topk_select_kernel<<<grid, warps * 32, smem, s>>>(ws, topk_idx, topk_score, t0, nt, b, sq, n_c,
                                                     ratio, K);
-    count_launches(1);
+  count_launches(1);
   return cudaGetLastError();
 }
 
