@@ -12,7 +12,7 @@
 // workspace that the per-row select kernel reads.  Tiles entirely above the
 // causal boundary are skipped.  Roles (320 threads):
 //   warp 0      TMA producer: the k_I tile once, then one q_I head tile per
-//               stage of a 4-deep ring (3D tensor map over [b*sq, H_I, d_I])
+//               stage of a 6-deep ring (3D tensor map over [b*sq, H_I, d_I])
 //   warp 1      TMEM owner + MMA issuer: per head, d_I/16 tcgen05.mma
 //               (M=128 queries, N=128 blocks, K=16) into one of two TMEM
 //               accumulators, committed to the ring's "empty" barrier and to
@@ -38,7 +38,7 @@ using namespace csa::umma;
 
 constexpr int kTileM = 128;     // queries per tile (TMEM lanes)
 constexpr int kTileN = 128;     // compressed blocks per tile (TMEM columns per accumulator)
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kMaxHeads = 64;
@@ -55,8 +55,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sB = sm;                                     // k_I tile
   unsigned char* sA = sm + kTileBytes;                        // q_I ring
-  float* w_s = reinterpret_cast<float*>(sA + kStages * kTileBytes);   // [H_I][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + kMaxHeads * kTileM);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + kStages * kTileBytes);
   uint64_t* full = bars;                 // [kStages]
   uint64_t* empty = bars + kStages;      // [kStages]
   uint64_t* acc_full = bars + 2 * kStages;      // [2]
@@ -92,14 +91,6 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  // indexer weights of the tile's queries, transposed to [h][row]
-  if (warp >= 2) {
-    for (int e = threadIdx.x - 64; e < kTileM * H_I; e += kEpiWarps * 32) {
-      const int r = e / H_I, h = e % H_I;
-      const int t = tq0 + r;
-      w_s[h * kTileM + r] = (t < tq_end) ? w[((long long)bi * sq + t) * H_I + h] : 0.f;
-    }
   }
   fence_before();
   __syncthreads();
@@ -163,6 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int half = (warp - 2) >> 2;             // column half of the tile
     const int row = quarter * 32 + lane;          // query within the tile
+    // this query's head weights: one 4-byte read per head from its own
+    // H_I-float row (L1-resident after the first touch)
+    const int tw = min(tq0 + row, tq_end - 1);
+    const float* wrow = w + ((long long)bi * sq + tw) * H_I;
     float acc[64];
 #pragma unroll
     for (int c = 0; c < 64; ++c) acc[c] = 0.f;
@@ -181,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[a]);
-      const float wv = w_s[h * kTileM + row];
+      const float wv = __ldg(wrow + h);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         acc[c] = fmaf(wv, fmaxf(__uint_as_float(v0[c]), 0.f), acc[c]);
@@ -242,7 +237,7 @@ bool indexer_tc_supported(int H_I, int d_I) {
 
 size_t indexer_tc_smem(int d_I) {
   const size_t tile = (size_t)(d_I / 64) * tc::kTileM * 128;
-  return 1024 + tile * (1 + tc::kStages) + tc::kMaxHeads * tc::kTileM * 4 + 16 * 8 + 16;
+  return 1024 + tile * (1 + tc::kStages) + 16 * 8 + 16;
 }
 
 cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
