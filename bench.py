@@ -230,6 +230,21 @@ def algorithmic_work(cfg, idx):
     }
 
 
+def rank_config(cfg, rank, world):
+    """The layer a rank runs: every rank gets its own seeded batch element."""
+    return cfg.with_(seed=cfg.seed + rank) if world > 1 else cfg
+
+
+def max_over_ranks(value_ms, world, device=None):
+    """Max of a per-rank time over all ranks (the job finishes with the slowest)."""
+    if world <= 1:
+        return value_ms
+    import torch
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     from compressed_sparse_attention_sum_gb300 import build as _build
@@ -239,9 +254,7 @@ def run_gpu(args, rank, world, local_rank):
     lib = csa.load_library()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    cfg = CONFIGS[args.workload]
-    if world > 1:
-        cfg = cfg.with_(seed=cfg.seed + rank)   # independent layer per rank
+    cfg = rank_config(CONFIGS[args.workload], rank, world)
     inp = make_inputs(cfg)
     host = {k: v.pin_memory() for k, v in inp.items()}
     d_in = {k: v.to(dev) for k, v in inp.items()}
@@ -300,11 +313,7 @@ def run_gpu(args, rank, world, local_rank):
     seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(4)]
     step_ms = [e[0].elapsed_time(e[4]) for e in evs]
     ms = sum(step_ms) / len(step_ms)
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
     queries = b * sq
     value = world * queries / (ms_max / 1e3)
 
@@ -368,11 +377,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = [t_start.elapsed_time(t_end) / args.steps]
     clk.__exit__(None, None, None)
-    e2e = sum(e2e_ms) / len(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world, dev)
 
     # ---- roofline ---------------------------------------------------------------
     peaks = load_peaks()
