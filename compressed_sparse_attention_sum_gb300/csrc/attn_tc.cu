@@ -236,44 +236,12 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
     ok = __syncthreads_and(mbar_wait(bar_s, it & 1));
     if (!ok) { site = kSiteFwdS; break; }
     fence_after();
-    // ---- softmax: pass 1, row max over both column halves ----------------------
-    float mt = -INFINITY;
-#pragma unroll
-    for (int c4 = 0; c4 < 2; ++c4) {
-      uint32_t v[32];
-      tmem_ld32_wait(tS + c4 * 32, v);
-#pragma unroll
-      for (int c = 0; c < 32; ++c)
-        mt = fmaxf(mt, fmaf(__uint_as_float(v[c]), sc2, biasq[c4 * 32 + c]));
-    }
-    rmax[hf * kRows + r] = mt;
-    __syncthreads();
-    mt = fmaxf(mt, rmax[(hf ^ 1) * kRows + r]);
-    const bool upd = mt > m_run + kRescale || (m_run == -INFINITY && mt != -INFINITY);
-    const float alpha = upd ? exp2f(m_run - mt) : 1.f;   // 0 when m_run = -inf
-    // rescale this thread's half of the O row in TMEM (no MMA is in flight on
-    // O here); the TMEM accesses are .sync.aligned, so the whole warp takes
-    // part whenever one of its rows needs it (the others scale by 1)
-    if (it > 0 && __any_sync(0xffffffffu, upd && m_run != -INFINITY)) {
-      const float f = (upd && m_run != -INFINITY) ? alpha : 1.f;
-#pragma unroll
-      for (int c4 = 0; c4 < 2; ++c4) {
-        uint32_t v[32];
-        tmem_ld32_wait(tO + c4 * 32, v);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
-        CSA_TMEM_ST32(tO + c4 * 32, v);
-      }
-      tmem_wait_st();
-    }
-    if (upd) {
-      l_run *= alpha;
-      m_run = mt;
-    }
-    // ---- pass 2: P = exp2(x - m) to shared memory (bf16), partial row sum ---------
-    float psum = 0.f;
-    const float mref = m_run == -INFINITY ? 0.f : m_run;
+    // ---- softmax: one optimistic pass against the running max -----------------
+    // P = exp2(x - m_run) is written while the tile max is tracked; only rows
+    // whose max grew by more than 2^8 (or had no reference yet) redo their P.
     unsigned char* pbuf = sm + Layout::P;
+    const float mref = m_run == -INFINITY ? 0.f : m_run;
+    float mt = -INFINITY, psum = 0.f;
 #pragma unroll
     for (int c4 = 0; c4 < 2; ++c4) {
       uint32_t v[32];
@@ -283,9 +251,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          // masked slots: x = -inf and 2^-inf = 0; rows with m_run = -inf have
-          // every x = -inf as well, guarded so that -inf - -inf never occurs
+          // masked slots: x = -inf and 2^-inf = 0
           const float x = fmaf(__uint_as_float(v[c8 * 8 + e]), sc2, biasq[c4 * 32 + c8 * 8 + e]);
+          mt = fmaxf(mt, x);
           p[e] = ex2(x - mref);
           psum += p[e];
         }
@@ -296,6 +264,58 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
         u.w = pack_bf16x2(p[6], p[7]);
         *reinterpret_cast<uint4*>(pbuf + sw_off(r, hf * 8 + c4 * 4 + c8)) = u;
       }
+    }
+    rmax[hf * kRows + r] = mt;
+    __syncthreads();
+    mt = fmaxf(mt, rmax[(hf ^ 1) * kRows + r]);
+    const bool upd = mt > m_run + kRescale || (m_run == -INFINITY && mt != -INFINITY);
+    // TMEM accesses are .sync.aligned: the whole warp takes part whenever one
+    // of its rows needs them
+    if (__any_sync(0xffffffffu, upd)) {
+      const float alpha = upd ? ex2(m_run - mt) : 1.f;     // 0 when m_run = -inf
+      // rescale this thread's half of the O row (no MMA is in flight on O here)
+      if (it > 0 && __any_sync(0xffffffffu, upd && m_run != -INFINITY)) {
+        const float f = (upd && m_run != -INFINITY) ? alpha : 1.f;
+#pragma unroll
+        for (int c4 = 0; c4 < 2; ++c4) {
+          uint32_t v[32];
+          tmem_ld32_wait(tO + c4 * 32, v);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * f);
+          CSA_TMEM_ST32(tO + c4 * 32, v);
+        }
+        tmem_wait_st();
+      }
+      if (upd) {
+        l_run *= alpha;
+        m_run = mt;
+      }
+      // redo P against the new max for the rows that moved it
+      float psum2 = 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < 2; ++c4) {
+        uint32_t v[32];
+        tmem_ld32_wait(tS + c4 * 32, v);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float x = fmaf(__uint_as_float(v[c8 * 8 + e]), sc2, biasq[c4 * 32 + c8 * 8 + e]);
+            p[e] = ex2(x - m_run);
+            psum2 += p[e];
+          }
+          if (upd) {
+            uint4 u;
+            u.x = pack_bf16x2(p[0], p[1]);
+            u.y = pack_bf16x2(p[2], p[3]);
+            u.z = pack_bf16x2(p[4], p[5]);
+            u.w = pack_bf16x2(p[6], p[7]);
+            *reinterpret_cast<uint4*>(pbuf + sw_off(r, hf * 8 + c4 * 4 + c8)) = u;
+          }
+        }
+      }
+      if (upd) psum = psum2;
     }
     l_run += psum;
     fence_proxy_async_smem();
