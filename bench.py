@@ -1,6 +1,7 @@
 """Benchmark of the CSA hot path on GB300: one step = one CSA layer,
 forward + backward: csa_compress -> csa_indexer_topk -> csa_attn_fwd ->
-csa_attn_bwd, on the CSA-4 workload (b=1, sq=4096, H=32, d=128, ratio 4,
+csa_attn_bwd -> csa_compress_bwd (the compressed rows' gradient flowing back
+through the pooling), on the CSA-4 workload (b=1, sq=4096, H=32, d=128, ratio 4,
 n_c=1024, window 128, topk 512, indexer 64 heads x 128).
 
 Prints one JSON line.  `value` is queries/s of the whole job (all ranks),
@@ -222,6 +223,9 @@ def algorithmic_work(cfg, idx):
     return {
         "slots": slots,
         "compress_bytes": cfg.b * (2 * cfg.sq * d + cfg.n_c * d) * e,
+        # kv + score read, pooled-row gradient read, raw-row gradient read and
+        # written, score gradient written
+        "compress_bwd_bytes": cfg.b * (2 * cfg.sq * d * e + cfg.n_c * d * 4 + 3 * cfg.sq * d * 4),
         "indexer_flops": 2.0 * cfg.H_I * cfg.d_I * vis_sum,
         "fwd_gathered_bytes": slots * d * e,
         "bwd_gathered_bytes": slots * (d * e + 4 * d),
@@ -269,12 +273,13 @@ def run_gpu(args, rank, world, local_rank):
     dq = torch.empty(b, sq, H, d, dtype=torch.float32, device=dev)
     dkv = torch.empty(b, sq + n_c, d, dtype=torch.float32, device=dev)
     dsink = torch.empty(H, dtype=torch.float32, device=dev)
+    dscore = torch.empty(b, sq, d, dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(x):
         kv_full[:, :sq].copy_(x["kv_raw"])          # raw rows of the KV buffer (layer input)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         ev[0].record(stream)
         csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:])
         ev[1].record(stream)
@@ -287,6 +292,11 @@ def run_gpu(args, rank, world, local_rank):
         csa.csa_attn_bwd(x["q"], kv_full, idx, x["sink"], cfg.scale, cfg.ratio, cfg.window, O, L,
                          x["dO"], dq=dq, dkv=dkv, dsink=dsink)
         ev[4].record(stream)
+        # the compressed rows' gradient flows back through the pooling into the
+        # raw rows (accumulated in place) and the pooling scores
+        csa.csa_compress_bwd(kv_full[:, :sq], x["score"], cfg.ratio, dkv[:, sq:], dkv[:, :sq],
+                             dscore=dscore)
+        ev[5].record(stream)
         return ev
 
     clk = ClockSampler(local_rank)
@@ -310,8 +320,8 @@ def run_gpu(args, rank, world, local_rank):
     launches = lib.csa_kernel_launches() - launches0
     if world > 1:
         torch.distributed.barrier()
-    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(4)]
-    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    seg = [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(5)]
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
     ms = sum(step_ms) / len(step_ms)
     ms_max = max_over_ranks(ms, world, dev)
     queries = b * sq
@@ -326,7 +336,7 @@ def run_gpu(args, rank, world, local_rank):
     def make_out():
         return {"idx": torch.empty_like(idx), "O": torch.empty_like(O), "L": torch.empty_like(L),
                 "dq": torch.empty_like(dq), "dkv": torch.empty_like(dkv),
-                "dsink": torch.empty_like(dsink)}
+                "dsink": torch.empty_like(dsink), "dscore": torch.empty_like(dscore)}
     d_out = [make_out(), make_out()]
     d_e2e = [{k: torch.empty_like(v) for k, v in d_in.items()} for _ in range(2)]
     out_host = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in o.items()}
@@ -359,6 +369,8 @@ def run_gpu(args, rank, world, local_rank):
                          out=y["O"], lse=y["L"])
         csa.csa_attn_bwd(x["q"], kv_full, y["idx"], x["sink"], cfg.scale, cfg.ratio, cfg.window,
                          y["O"], y["L"], x["dO"], dq=y["dq"], dkv=y["dkv"], dsink=y["dsink"])
+        csa.csa_compress_bwd(kv_full[:, :sq], x["score"], cfg.ratio, y["dkv"][:, sq:],
+                             y["dkv"][:, :sq], dscore=y["dscore"])
         ev_comp[sl].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[sl])
@@ -383,7 +395,7 @@ def run_gpu(args, rank, world, local_rank):
     peaks = load_peaks()
     traffic = load_traffic()
     k_ms = {n: sum(s) / len(s) for n, s in zip(("compress", "indexer_topk", "attn_fwd",
-                                                  "attn_bwd"), seg)}
+                                                  "attn_bwd", "compress_bwd"), seg)}
     per = {
         "compress": ("hbm", work["compress_bytes"] / (k_ms["compress"] / 1e3) / 1e9,
                      peaks["hbm_gbs"], "GB/s"),
@@ -393,6 +405,8 @@ def run_gpu(args, rank, world, local_rank):
                      peaks["hbm_gbs"], "GB/s"),
         "attn_bwd": ("hbm", work["bwd_gathered_bytes"] / (k_ms["attn_bwd"] / 1e3) / 1e9,
                      peaks["hbm_gbs"], "GB/s"),
+        "compress_bwd": ("hbm", work["compress_bwd_bytes"] / (k_ms["compress_bwd"] / 1e3) / 1e9,
+                         peaks["hbm_gbs"], "GB/s"),
     }
     kernels = {}
     for n, (bound, ach, peak, unit) in per.items():

@@ -32,6 +32,8 @@ SIGNATURES = {
     "csa_kernel_launches": (ctypes.c_ulonglong, []),
     "csa_compress": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll, _c_int, _c_int, _c_int, _c_int,
                               _c_int, _c_p]),
+    "csa_compress_bwd": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll, _c_p, _c_ll, _c_p]
+                         + [_c_int] * 5 + [_c_p]),
     "csa_indexer_topk_workspace_size": (_c_sz, [_c_int] * 6 + [_c_int]),
     "csa_indexer_topk_min_workspace": (_c_sz, [_c_int, _c_int]),
     "csa_indexer_topk": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7 + [_c_int, _c_p, _c_sz,
@@ -125,6 +127,32 @@ def csa_compress(kv: torch.Tensor, score: torch.Tensor, ratio: int,
                                             score.shape[2], out.data_ptr(), out.stride(0), b, sq,
                                             d, ratio, _dt(kv), _stream(stream)))
     return out
+
+
+def csa_compress_bwd(kv: torch.Tensor, score: torch.Tensor, ratio: int, dout: torch.Tensor,
+                     dkv: torch.Tensor, dscore: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """Gradient of the pooling: adds w*dout into dkv (in place) and returns
+    dscore.  kv [b, sq, d] and dkv [b, sq, d] (fp32) may be row-contiguous
+    views (kv_full[:, :sq], dkv_full[:, :sq]); dout [b, sq//ratio, d] fp32 may
+    be dkv_full[:, sq:]."""
+    lib = load_library()
+    _need(kv, "kv", contiguous=False)
+    _need(score, "score", dtype=kv.dtype)
+    _need(dout, "dout", dtype=torch.float32, contiguous=False)
+    _need(dkv, "dkv", dtype=torch.float32, contiguous=False)
+    b, sq, d = kv.shape
+    for t, n in ((kv, "kv"), (dout, "dout"), (dkv, "dkv")):
+        if t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{n} rows must be contiguous")
+    if dscore is None:
+        dscore = torch.empty(b, sq, score.shape[2], dtype=torch.float32, device=kv.device)
+    _need(dscore, "dscore", dtype=torch.float32)
+    _check("csa_compress_bwd", lib.csa_compress_bwd(
+        kv.data_ptr(), kv.stride(0), score.data_ptr(), score.shape[2], dout.data_ptr(),
+        dout.stride(0), dkv.data_ptr(), dkv.stride(0), dscore.data_ptr(), b, sq, d, ratio,
+        _dt(kv), _stream(stream)))
+    return dscore
 
 
 def csa_indexer_topk_workspace_size(b: int, sq: int, n_c: int, H_I: int, d_I: int, topk: int,

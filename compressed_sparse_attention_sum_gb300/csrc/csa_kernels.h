@@ -17,6 +17,11 @@ cudaError_t launch_compress(const void* kv, long long kv_bs, const void* score, 
 cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
                                int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s);
 
+cudaError_t launch_compress_bwd(const void* kv, long long kv_bs, const void* score,
+                                int score_width, const float* g, long long g_bs, float* dkv,
+                                long long dkv_bs, float* dscore, int b, int sq, int d, int ratio,
+                                bool bf16, cudaStream_t s);
+
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
 
 }  // namespace csa

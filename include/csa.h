@@ -4,6 +4,7 @@
  * One CSA layer on one GPU, as four calls (plus helpers):
  *
  *   csa_compress      softmax-weighted pooling of `ratio` consecutive KV tokens
+ *                     (csa_compress_bwd: its gradient)
  *   csa_indexer_topk  lightning-indexer scores fused with an exact causal top-k
  *   csa_attn_fwd      sparse MQA (shared K=V) over window + top-k compressed
  *                     rows + per-head sink; returns O and LSE
@@ -106,6 +107,35 @@ csa_status_t csa_compress(const void* kv, long long kv_batch_stride,
                           void* out, long long out_batch_stride,
                           int b, int sq, int d, int ratio,
                           csa_dtype_t dt, csa_stream_t stream);
+
+/*
+ * csa_compress_bwd - gradient of csa_compress.
+ *
+ * With w_t the softmax weights of block j and channel c (as in csa_compress)
+ * and g = dout[b, j, c] the gradient of the pooled row:
+ *   dkv[b, t, c]    += w_t * g                         (accumulated)
+ *   dscore[b, t, c'] = w_t * g * (kv[b, t, c] - out[b, j, c])
+ * summed over c for score_width == 1 (c' = 0).  The pooled row is recomputed
+ * in fp32.  Tokens past the last complete block: dkv unchanged, dscore 0.
+ * dkv accumulates so that the raw rows of the attention's dkv
+ * (dkv_full[:, :sq]) receive the compressor's share in place.
+ *
+ *   kv, score  in   as csa_compress
+ *   dout       in   [b, n_c, d] fp32, batch stride dout_batch_stride (pass
+ *                   dkv_full + sq*d and n_kv*d for the compressed rows)
+ *   dkv        in/out [b, sq, d] fp32, batch stride dkv_batch_stride
+ *   dscore     out  [b, sq, score_width] fp32, packed, fully written
+ * Errors: as csa_compress (all pointers 16-byte aligned, strides in elements).
+ * The pages keep this pooling in fp32 and cast once ("Add unfused SBHD
+ * compressed sparse attention", compressor review, which also describes the
+ * test of the KV and score gradients against an fp32 pooling oracle).
+ */
+csa_status_t csa_compress_bwd(const void* kv, long long kv_batch_stride,
+                              const void* score, int score_width,
+                              const float* dout, long long dout_batch_stride,
+                              float* dkv, long long dkv_batch_stride, float* dscore,
+                              int b, int sq, int d, int ratio,
+                              csa_dtype_t dt, csa_stream_t stream);
 
 /*
  * Bytes of indexer workspace that csa_indexer_topk uses by default: the

@@ -201,3 +201,28 @@ def test_tc_forward_dense_mode_and_large_logits(H):
     q, kv, _, snk, dO = _rand_attn(9, b, sq, H, 128, ratio, W, 1, "bf16")
     q = (q.float() * 4).bfloat16()           # logits spread over a wide range
     _run_both(q, kv, None, snk, dO, ratio, W, "bf16")
+
+
+# ---------------------------------------------------------------------------
+# compressor forward/backward: per-token score, ragged tail, fp32 and bf16
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("score_width", [1, "d"])
+def test_compress_fwd_bwd_ragged_and_scalar_score(dtype, score_width):
+    b, sq, d, ratio = 2, 43, 24, 5          # 3 tokens past the last block
+    g = torch.Generator().manual_seed(11)
+    sw = d if score_width == "d" else 1
+    kv = torch.randn(b, sq, d, generator=g).to(_dt(dtype))
+    score = (torch.randn(b, sq, sw, generator=g) * 3).to(_dt(dtype))
+    dout = torch.randn(b, sq // ratio, d, generator=g)
+    out = csa.csa_compress(kv.cuda(), score.cuda(), ratio)
+    dkv = torch.zeros(b, sq, d, device="cuda")
+    dscore = csa.csa_compress_bwd(kv.cuda(), score.cuda(), ratio, dout.cuda(), dkv)
+    torch.cuda.synchronize()
+    tol = TOL[dtype]
+    assert maxabs(f64(out), orc.compress(f64(kv), f64(score), ratio)) <= tol
+    ref_dkv, ref_ds = orc.compress_bwd(f64(kv), f64(score), ratio, f64(dout))
+    assert maxabs(f64(dkv), ref_dkv) <= tol
+    assert maxabs(f64(dscore), ref_ds) <= tol
+    assert torch.all(dkv[:, 40:] == 0) and torch.all(dscore[:, 40:] == 0)

@@ -57,6 +57,30 @@ def test_compress_parity(name):
     assert torch.equal(kv_full[:, :sq], kv_raw)
 
 
+@pytest.mark.parametrize("name", CONFIG_ORDER)
+def test_compress_bwd_parity(name):
+    """Gradient of the pooling in the layer layout: the compressed rows of
+    dkv_full are the incoming gradient, the raw rows accumulate w*g."""
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg, parts=("compress",))
+    b, sq, d, n_c = cfg.b, cfg.sq, cfg.d, cfg.n_c
+    g = torch.Generator().manual_seed(7)
+    dout = torch.randn(b, n_c, d, generator=g)
+    pre = torch.randn(b, sq, d, generator=g)
+    kv_full = torch.zeros(b, sq + n_c, d, dtype=cfg.torch_dtype, device="cuda")
+    kv_full[:, :sq] = inp["kv_raw"].cuda()
+    dkv_full = torch.cat([pre, dout], dim=1).cuda()
+    dscore = csa.csa_compress_bwd(kv_full[:, :sq], inp["score"].cuda(), cfg.ratio,
+                                  dkv_full[:, sq:], dkv_full[:, :sq])
+    torch.cuda.synchronize()
+    ref_dkv, ref_ds = orc.compress_bwd(f64(inp["kv_raw"]), f64(inp["score"]), cfg.ratio, f64(dout))
+    tol = TOL[cfg.dtype]
+    e_kv = maxabs(f64(dkv_full[:, :sq]) - f64(pre), ref_dkv)
+    e_s = maxabs(f64(dscore), ref_ds)
+    assert e_kv <= tol and e_s <= tol, (e_kv, e_s)
+    assert torch.equal(dkv_full[:, sq:].cpu(), dout)
+
+
 # ---------------------------------------------------------------------------
 # indexer + top-k
 # ---------------------------------------------------------------------------
