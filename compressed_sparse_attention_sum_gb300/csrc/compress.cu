@@ -6,20 +6,82 @@
 // the sum stay in fp32 and the pooled row is cast once to the storage dtype.
 //
 // HBM-bound: each kv and score element is read once and each pooled element
-// written once.  One thread owns 8 consecutive channels of one block and
-// walks the block's tokens with an online (running max) softmax, so the
-// scores are read in a single pass.
+// written once.  One thread owns 8 consecutive channels of one block.  For
+// ratio 4 (the CSA ratio) the thread loads the whole block before any
+// arithmetic, so one memory latency covers it; other ratios walk the tokens
+// with an online (running max) softmax, reading the scores in one pass.
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 
 namespace csa {
 
+// 8 channels of token t of a block: kv row and the pooling score (the score is
+// broadcast over the channels when one score drives the whole row)
 template <typename T>
-__global__ void __launch_bounds__(128) compress_kernel(const T* __restrict__ kv, long long kv_bs,
-                                                       const T* __restrict__ score,
-                                                       int score_width, T* __restrict__ out,
-                                                       long long out_bs, int sq, int d,
-                                                       int ratio, int n_c) {
+__device__ __forceinline__ void load_token(const T* kvp, const T* scp, int t, int d,
+                                           int score_width, int c0, float* v, float* s) {
+  load8(kvp + (long long)t * d, v);
+  if (score_width == 1) {
+    const float s1 = to_f(scp[t]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = s1;
+  } else {
+    load8(scp + (long long)t * score_width + c0, s);
+  }
+}
+
+// Per-channel softmax statistics of a block (running max m, sum l) and the
+// pooled value sum_t w_t kv_t.  R > 0: compile-time ratio, the block is held
+// in registers (v, s filled by the caller); R == 0: runtime ratio, online.
+template <typename T, int R>
+__device__ __forceinline__ void pool_block(const T* kvp, const T* scp, int ratio, int d,
+                                           int score_width, int c0, float (*v)[8],
+                                           float (*s)[8], float* m, float* l, float* pooled) {
+  if constexpr (R > 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float mx = s[0][i];
+#pragma unroll
+      for (int t = 1; t < R; ++t) mx = fmaxf(mx, s[t][i]);
+      float sum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int t = 0; t < R; ++t) {
+        const float e = expf(s[t][i] - mx);
+        sum += e;
+        acc = fmaf(e, v[t][i], acc);
+      }
+      m[i] = mx;
+      l[i] = sum;
+      pooled[i] = acc / sum;
+    }
+  } else {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; l[i] = 0.f; acc[i] = 0.f; }
+    for (int t = 0; t < ratio; ++t) {
+      float vt[8], st[8];
+      load_token(kvp, scp, t, d, score_width, c0, vt, st);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float mn = fmaxf(m[i], st[i]);
+        const float alpha = expf(m[i] - mn);  // 0 on the first token (m = -inf)
+        const float e = expf(st[i] - mn);
+        l[i] = l[i] * alpha + e;
+        acc[i] = acc[i] * alpha + e * vt[i];
+        m[i] = mn;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pooled[i] = acc[i] / l[i];
+  }
+}
+
+template <typename T, int R>
+__global__ void __launch_bounds__(64) compress_kernel(const T* __restrict__ kv, long long kv_bs,
+                                                      const T* __restrict__ score,
+                                                      int score_width, T* __restrict__ out,
+                                                      long long out_bs, int sq, int d, int ratio,
+                                                      int n_c) {
   const int groups = d / 8;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int bi = blockIdx.y;
@@ -28,32 +90,14 @@ __global__ void __launch_bounds__(128) compress_kernel(const T* __restrict__ kv,
   const int c0 = (int)(gid % groups) * 8;
   const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d + c0;
   const T* scp = score + ((long long)bi * sq + (long long)j * ratio) * score_width;
-  float m[8], l[8], acc[8];
+  constexpr int RR = R > 0 ? R : 1;
+  float v[RR][8], s[RR][8];
+  if constexpr (R > 0) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; l[i] = 0.f; acc[i] = 0.f; }
-  for (int t = 0; t < ratio; ++t) {
-    float v[8], s[8];
-    load8(kvp + (long long)t * d, v);
-    if (score_width == 1) {
-      const float s1 = to_f(scp[(long long)t]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s[i] = s1;
-    } else {
-      load8(scp + (long long)t * score_width + c0, s);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float mn = fmaxf(m[i], s[i]);
-      const float alpha = expf(m[i] - mn);  // 0 on the first token (m = -inf)
-      const float e = expf(s[i] - mn);
-      l[i] = l[i] * alpha + e;
-      acc[i] = acc[i] * alpha + e * v[i];
-      m[i] = mn;
-    }
+    for (int t = 0; t < R; ++t) load_token(kvp, scp, t, d, score_width, c0, v[t], s[t]);
   }
-  float r[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) r[i] = acc[i] / l[i];
+  float m[8], l[8], r[8];
+  pool_block<T, R>(kvp, scp, ratio, d, score_width, c0, v, s, m, l, r);
   store8(out + bi * out_bs + (long long)j * d + c0, r);
 }
 
@@ -63,70 +107,64 @@ __global__ void __launch_bounds__(128) compress_kernel(const T* __restrict__ kv,
 //                                           the attention's gradient)
 //   dscore_t  = w_t g (kv_t - pooled)      (per channel; summed over channels
 //                                           when one score drives all channels)
-// Tokens past the last complete block get no kv gradient and zero dscore.
-template <typename T>
-__global__ void __launch_bounds__(128) compress_bwd_kernel(
+// Tokens past the last complete block get no kv gradient and zero dscore; with
+// a per-channel score the threads past the last block write those zeros.
+template <typename T, int R>
+__global__ void __launch_bounds__(64) compress_bwd_kernel(
     const T* __restrict__ kv, long long kv_bs, const T* __restrict__ score, int score_width,
     const float* __restrict__ g, long long g_bs, float* __restrict__ dkv, long long dkv_bs,
     float* __restrict__ dscore, int sq, int d, int ratio, int n_c) {
   const int groups = d / 8;
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int bi = blockIdx.y;
-  if (gid >= (long long)n_c * groups) return;
+  if (gid >= (long long)n_c * groups) {
+    if (score_width == 1) return;  // zeroed before the launch
+    const long long tok = (long long)n_c * ratio + (gid - (long long)n_c * groups) / groups;
+    if (tok >= sq) return;
+    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    store8(dscore + ((long long)bi * sq + tok) * score_width + (gid % groups) * 8, z);
+    return;
+  }
   const int j = (int)(gid / groups);
   const int c0 = (int)(gid % groups) * 8;
   const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d + c0;
   const T* scp = score + ((long long)bi * sq + (long long)j * ratio) * score_width;
+  float* dkp = dkv + bi * dkv_bs + (long long)j * ratio * d + c0;
   float gv[8];
   load8(g + bi * g_bs + (long long)j * d + c0, gv);
-  // softmax statistics of the block (per channel)
-  float m[8], l[8], pooled[8];
+  constexpr int RR = R > 0 ? R : 1;
+  float v[RR][8], s[RR][8], dk[RR][8];
+  if constexpr (R > 0) {
+    // everything the block needs, before any arithmetic
 #pragma unroll
-  for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; l[i] = 0.f; pooled[i] = 0.f; }
-  for (int t = 0; t < ratio; ++t) {
-    float v[8], sc[8];
-    load8(kvp + (long long)t * d, v);
-    if (score_width == 1) {
-      const float s1 = to_f(scp[(long long)t]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sc[i] = s1;
-    } else {
-      load8(scp + (long long)t * score_width + c0, sc);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float mn = fmaxf(m[i], sc[i]);
-      const float alpha = expf(m[i] - mn);
-      const float e = expf(sc[i] - mn);
-      l[i] = l[i] * alpha + e;
-      pooled[i] = pooled[i] * alpha + e * v[i];
-      m[i] = mn;
+    for (int t = 0; t < R; ++t) {
+      load_token(kvp, scp, t, d, score_width, c0, v[t], s[t]);
+      load8(dkp + (long long)t * d, dk[t]);
     }
   }
+  float m[8], l[8], pooled[8];
+  pool_block<T, R>(kvp, scp, ratio, d, score_width, c0, v, s, m, l, pooled);
+  const int nt = R > 0 ? R : ratio;
+#pragma unroll(R > 0 ? R : 1)
+  for (int t = 0; t < nt; ++t) {
+    float vt[8], st[8], dt[8];
+    if constexpr (R > 0) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) pooled[i] /= l[i];
-  for (int t = 0; t < ratio; ++t) {
-    float v[8], sc[8], dk[8];
-    const long long tok = (long long)j * ratio + t;
-    load8(kvp + (long long)t * d, v);
-    if (score_width == 1) {
-      const float s1 = to_f(scp[(long long)t]);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sc[i] = s1;
+      for (int i = 0; i < 8; ++i) { vt[i] = v[t][i]; st[i] = s[t][i]; dt[i] = dk[t][i]; }
     } else {
-      load8(scp + (long long)t * score_width + c0, sc);
+      load_token(kvp, scp, t, d, score_width, c0, vt, st);
+      load8(dkp + (long long)t * d, dt);
     }
-    float* dkp = dkv + bi * dkv_bs + tok * d + c0;
-    load8(dkp, dk);
+    const long long tok = (long long)j * ratio + t;
     float ds[8], dsum = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float w = expf(sc[i] - m[i]) / l[i];
-      dk[i] = fmaf(w, gv[i], dk[i]);
-      ds[i] = w * gv[i] * (v[i] - pooled[i]);
+      const float w = expf(st[i] - m[i]) / l[i];
+      dt[i] = fmaf(w, gv[i], dt[i]);
+      ds[i] = w * gv[i] * (vt[i] - pooled[i]);
       dsum += ds[i];
     }
-    store8(dkp, dk);
+    store8(dkp + (long long)t * d, dt);
     if (score_width == 1) {
       atomicAdd(dscore + (long long)bi * sq + tok, dsum);
     } else {
@@ -135,28 +173,60 @@ __global__ void __launch_bounds__(128) compress_bwd_kernel(
   }
 }
 
+namespace {
+constexpr int kCompressThreads = 64;
+
+template <typename T, int R>
+void compress_fwd_t(const void* kv, long long kv_bs, const void* score, int score_width,
+                    void* out, long long out_bs, int b, int sq, int d, int ratio, cudaStream_t s) {
+  const int n_c = sq / ratio;
+  const long long work = (long long)n_c * (d / 8);
+  dim3 grid((unsigned)((work + kCompressThreads - 1) / kCompressThreads), (unsigned)b);
+  compress_kernel<T, R><<<grid, kCompressThreads, 0, s>>>((const T*)kv, kv_bs, (const T*)score,
+                                                          score_width, (T*)out, out_bs, sq, d,
+                                                          ratio, n_c);
+  count_launches(1);
+}
+
+template <typename T, int R>
+void compress_bwd_t(const void* kv, long long kv_bs, const void* score, int score_width,
+                    const float* g, long long g_bs, float* dkv, long long dkv_bs, float* dscore,
+                    int b, int sq, int d, int ratio, cudaStream_t s) {
+  const int n_c = sq / ratio;
+  const int tail = score_width == 1 ? 0 : sq - n_c * ratio;
+  const long long work = (long long)(n_c + tail) * (d / 8);
+  if (work == 0) return;
+  dim3 grid((unsigned)((work + kCompressThreads - 1) / kCompressThreads), (unsigned)b);
+  compress_bwd_kernel<T, R><<<grid, kCompressThreads, 0, s>>>(
+      (const T*)kv, kv_bs, (const T*)score, score_width, g, g_bs, dkv, dkv_bs, dscore, sq, d,
+      ratio, n_c);
+  count_launches(1);
+}
+}  // namespace
+
 cudaError_t launch_compress_bwd(const void* kv, long long kv_bs, const void* score,
                                 int score_width, const float* g, long long g_bs, float* dkv,
                                 long long dkv_bs, float* dscore, int b, int sq, int d, int ratio,
                                 bool bf16, cudaStream_t s) {
-  const int n_c = sq / ratio;
-  // dscore is written for every token; tokens past the last block and the
-  // per-token sums of a shared score start from zero
-  cudaError_t e = launch_zero_f32(dscore, (size_t)b * sq * score_width, s);
-  if (e != cudaSuccess) return e;
-  const long long work = (long long)n_c * (d / 8);
-  const int threads = 128;
-  dim3 grid((unsigned)((work + threads - 1) / threads), (unsigned)b);
+  if (score_width == 1) {
+    // the per-token sums of a shared score (and the tail) start from zero
+    cudaError_t e = launch_zero_f32(dscore, (size_t)b * sq, s);
+    if (e != cudaSuccess) return e;
+  }
   if (bf16) {
-    compress_bwd_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
-        (const __nv_bfloat16*)kv, kv_bs, (const __nv_bfloat16*)score, score_width, g, g_bs, dkv,
-        dkv_bs, dscore, sq, d, ratio, n_c);
-    count_launches(1);
+    if (ratio == 4)
+      compress_bwd_t<__nv_bfloat16, 4>(kv, kv_bs, score, score_width, g, g_bs, dkv, dkv_bs,
+                                       dscore, b, sq, d, ratio, s);
+    else
+      compress_bwd_t<__nv_bfloat16, 0>(kv, kv_bs, score, score_width, g, g_bs, dkv, dkv_bs,
+                                       dscore, b, sq, d, ratio, s);
   } else {
-    compress_bwd_kernel<float><<<grid, threads, 0, s>>>((const float*)kv, kv_bs,
-                                                        (const float*)score, score_width, g, g_bs,
-                                                        dkv, dkv_bs, dscore, sq, d, ratio, n_c);
-    count_launches(1);
+    if (ratio == 4)
+      compress_bwd_t<float, 4>(kv, kv_bs, score, score_width, g, g_bs, dkv, dkv_bs, dscore, b,
+                               sq, d, ratio, s);
+    else
+      compress_bwd_t<float, 0>(kv, kv_bs, score, score_width, g, g_bs, dkv, dkv_bs, dscore, b,
+                               sq, d, ratio, s);
   }
   return cudaGetLastError();
 }
@@ -164,20 +234,18 @@ cudaError_t launch_compress_bwd(const void* kv, long long kv_bs, const void* sco
 cudaError_t launch_compress(const void* kv, long long kv_bs, const void* score, int score_width,
                             void* out, long long out_bs, int b, int sq, int d, int ratio,
                             bool bf16, cudaStream_t s) {
-  const int n_c = sq / ratio;
-  const long long work = (long long)n_c * (d / 8);
-  const int threads = 128;
-  dim3 grid((unsigned)((work + threads - 1) / threads), (unsigned)b);
   if (bf16) {
-    compress_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
-        (const __nv_bfloat16*)kv, kv_bs, (const __nv_bfloat16*)score, score_width,
-        (__nv_bfloat16*)out, out_bs, sq, d, ratio, n_c);
-    count_launches(1);
+    if (ratio == 4)
+      compress_fwd_t<__nv_bfloat16, 4>(kv, kv_bs, score, score_width, out, out_bs, b, sq, d,
+                                       ratio, s);
+    else
+      compress_fwd_t<__nv_bfloat16, 0>(kv, kv_bs, score, score_width, out, out_bs, b, sq, d,
+                                       ratio, s);
   } else {
-    compress_kernel<float><<<grid, threads, 0, s>>>((const float*)kv, kv_bs, (const float*)score,
-                                                    score_width, (float*)out, out_bs, sq, d,
-                                                    ratio, n_c);
-    count_launches(1);
+    if (ratio == 4)
+      compress_fwd_t<float, 4>(kv, kv_bs, score, score_width, out, out_bs, b, sq, d, ratio, s);
+    else
+      compress_fwd_t<float, 0>(kv, kv_bs, score, score_width, out, out_bs, b, sq, d, ratio, s);
   }
   return cudaGetLastError();
 }
