@@ -27,6 +27,7 @@
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 #include "tcgen05.cuh"
+#include "attn_union.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -85,8 +86,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
   int* wsum = ulist + n_c;                                                    // [8] scan scratch
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bi = blockIdx.y;
-  const int t0 = blockIdx.x * QB;
+  int bi, xb;
+  heavy_first_block((sq + QB - 1) / QB, &bi, &xb);
+  const int t0 = xb * QB;
   const int n_kv = sq + n_c;
   const __nv_bfloat16* kv_b = kv + (long long)bi * n_kv * kD;
 
@@ -112,55 +114,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
 
   // ---- union of the block's selected compressed blocks ----------------------
   const int t_last = min(t0 + QB, sq) - 1;
-  const int vmax = min((t_last + 1) / ratio, n_c);
-  for (int q = 0; q < QB; ++q) {
-    const int t = t0 + q;
-    if (t >= sq) break;
-    const int vis = min((t + 1) / ratio, n_c);
-    const unsigned long long inc = 1ull << (16 * (q & 3));
-    if (idx != nullptr) {
-      const int32_t* row = idx + ((long long)bi * sq + t) * K;
-      for (int s = tid; s < K; s += kThreads) {
-        const int j = row[s];
-        if (j >= 0 && j < vis) atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[j * NW + (q >> 2)]), inc);
-      }
-    } else {
-      for (int j = tid; j < vis; j += kThreads) atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[j * NW + (q >> 2)]), inc);
-    }
-  }
-  __syncthreads();
-  {
-    // ascending compaction of the blocks any query selected
-    const int per = (vmax + kThreads - 1) / kThreads;
-    const int j0 = tid * per, j1 = min(vmax, j0 + per);
-    int c = 0;
-    for (int j = j0; j < j1; ++j) {
-      bool any = false;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) any |= cnt[j * NW + w] != 0ull;
-      c += any;
-    }
-    int incl = c;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += wsum[w];
-    int pos = base + incl - c;
-    for (int j = j0; j < j1; ++j) {
-      bool any = false;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) any |= cnt[j * NW + w] != 0ull;
-      if (any) ulist[pos++] = j;
-    }
-    if (tid == kThreads - 1) scal[0] = base + incl;
-  }
-  __syncthreads();
-  const int nu = scal[0];
+  const int nu = build_union<QB, kThreads>(idx, bi, sq, K, t0, ratio, n_c, cnt, ulist, wsum, scal);
   const int win0 = max(0, t0 - window + 1);
   const int nwin = t_last - win0 + 1;
   const int S_total = nwin + nu;
@@ -422,7 +376,7 @@ cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx
     return cudaErrorInvalidValue;
   const int QB = 128 / H;
   const size_t smem = attn_tc_smem(QB, n_c);
-  dim3 grid((unsigned)((sq + QB - 1) / QB), (unsigned)b);
+  dim3 grid((unsigned)(((sq + QB - 1) / QB) * b));   // heaviest blocks first
 #define CSA_TC_FWD(QQ)                                                                          \
   {                                                                                             \
     auto k = atc::attn_fwd_tc_kernel<QQ>;                                                       \
