@@ -401,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     fence_after();
     // scatter this tile's dKV rows (TMEM lane = slot) into the compact buffer,
     // while the tensor core computes the next tile's S and dP: stage the fp32
-    // rows contiguously in X|Y (free until the next tile's P), then one bulk
-    // asynchronous add of 512 B per valid slot row
+    // rows contiguously in X|Y (free until the next tile's P), then one
+    // coalesced fp32 vector reduction of 512 B per valid slot row
     {
       float* stg = reinterpret_cast<float*>(X);          // [128 slots][128] fp32 = 64 KB
       uint32_t v[32];
@@ -428,15 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<float4*>(srow + ((c + lane) & 7) * 4) = ch[c];
-      fence_proxy_async_smem();
       __syncthreads();
-      const int s = it * kSlots + tid;
-      if (tid < kSlots && s < S_total) {
-        bulk_reduce_add_f32(dkv_b + (long long)slot_row(s) * kD, stg + tid * kD, kD * 4);
-        bulk_commit();
+      // one warp per staged row: its 32 lanes add the row's 512 B with one
+      // coalesced vector reduction (X|Y is free again once every thread has
+      // passed the next barrier)
+      const int nrow = min(kSlots, S_total - it * kSlots);
+#pragma unroll 4
+      for (int rr = warp; rr < nrow; rr += kThreads / 32) {
+        const float4 v4 = *reinterpret_cast<const float4*>(stg + rr * kD + lane * 4);
+        red_add_v4(dkv_b + (long long)slot_row(it * kSlots + rr) * kD + lane * 4, v4.x, v4.y,
+                   v4.z, v4.w);
       }
-      // X|Y are rewritten by the next tile: its readers wait for the bulk reads
-      if (tid < kSlots) bulk_wait_read_all();
     }
     fence_before();
   }
