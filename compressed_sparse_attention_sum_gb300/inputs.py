@@ -201,6 +201,26 @@ def zipf_indices(cfg: CSAConfig, g: torch.Generator) -> torch.Tensor:
     return out.contiguous()
 
 
+def packed_doc_ids(b: int, sq: int, ratio: int, n_docs: int, seed: int = 0) -> torch.Tensor:
+    """Per-token document ids [b, sq] int32 of n_docs packed documents per
+    batch element.  Documents are consecutive runs whose boundaries fall on
+    multiples of `ratio` (packing pads every document to a multiple of the
+    compress ratio, torchtitan PR #4452), at seeded random positions; the
+    ids are 0..n_docs-1 in order."""
+    g = torch.Generator().manual_seed(1000 + seed)
+    slots = sq // ratio
+    assert 1 <= n_docs <= slots
+    out = torch.empty(b, sq, dtype=torch.int32)
+    for bi in range(b):
+        cuts = torch.randperm(slots - 1, generator=g)[:n_docs - 1] + 1
+        cuts, _ = torch.sort(cuts * ratio)
+        ids = torch.zeros(sq, dtype=torch.int32)
+        for c in cuts.tolist():
+            ids[c:] += 1
+        out[bi] = ids
+    return out
+
+
 def to_f64(t: torch.Tensor):
     """Exact widening of a stored tensor to a float64 numpy array."""
     return t.to(torch.float64).numpy()

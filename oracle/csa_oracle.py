@@ -22,6 +22,13 @@ page title and section:
   (torchtitan PR #4452): one softmax over window + selected compressed
   entries + sink, returning the per-head LSE (the sink is in the
   denominator, contributes no value).
+  Packed documents (same page, the selected_attention commit message): with
+  per-token doc_ids, the window branch keeps key k for query t only when
+  doc_ids[k] == doc_ids[t]; compressed block j covers tokens
+  [j*ratio, (j+1)*ratio), belongs to doc_ids[j*ratio], and the indexer may
+  select it for t only when doc_ids[t] == doc_ids[j*ratio] (and j < vis(t)).
+  The attention takes the selected entries as given (the caller's indexer
+  already filtered them).
 * "Add the min-memory DSA attention kernels" (Megatron-LM PR #7152): exact
   ties after ReLU are common and routing must be tie-exact with one full
   top-k; the selected support is sorted by position; repeated keys
@@ -46,7 +53,7 @@ import numpy as np
 __all__ = [
     "round_to_storage", "round_bf16",
     "visible_blocks", "compress", "compress_bwd",
-    "indexer_scores", "indexer_scores_row", "topk_select", "topk_select_row",
+    "indexer_selectable", "indexer_scores", "indexer_scores_row", "topk_select", "topk_select_row",
     "query_slots", "attn_fwd_query", "attn_fwd", "attn_bwd_query", "attn_bwd",
 ]
 
@@ -170,8 +177,20 @@ def indexer_scores_row(q_I_t, k_I_b, w_t, t: int, ratio: int):
     return np.asarray(w_t, np.float64) @ np.maximum(dots, 0.0)
 
 
-def indexer_scores(q_I, k_I, w, ratio: int):
-    """Full score matrix [b, sq, n_c]; entries with j >= vis(t) are -inf."""
+def indexer_selectable(t: int, n_c: int, ratio: int, doc_b=None):
+    """Boolean mask [n_c] of the blocks query t may select: j < vis(t) and,
+    with per-token document ids doc_b [sq], doc_b[j*ratio] == doc_b[t]."""
+    j = np.arange(n_c)
+    ok = j < visible_blocks(t, ratio)
+    if doc_b is not None:
+        doc_b = np.asarray(doc_b)
+        ok &= doc_b[np.minimum(j * ratio, doc_b.shape[0] - 1)] == doc_b[t]
+    return ok
+
+
+def indexer_scores(q_I, k_I, w, ratio: int, doc_ids=None):
+    """Full score matrix [b, sq, n_c]; entries query t may not select
+    (j >= vis(t), or another document's block) are -inf."""
     b, sq = q_I.shape[:2]
     n_c = k_I.shape[1]
     out = np.full((b, sq, n_c), -np.inf)
@@ -179,6 +198,8 @@ def indexer_scores(q_I, k_I, w, ratio: int):
         for t in range(sq):
             row = indexer_scores_row(q_I[bi, t], k_I[bi], w[bi, t], t, ratio)
             out[bi, t, :row.shape[0]] = row
+            if doc_ids is not None:
+                out[bi, t, ~indexer_selectable(t, n_c, ratio, doc_ids[bi])] = -np.inf
     return out
 
 
@@ -198,15 +219,18 @@ def topk_select_row(scores_vis, K: int):
 
 
 def topk_select(scores, K: int):
-    """Apply topk_select_row to every row of a [b, sq, n_c] matrix whose
-    non-visible entries are -inf."""
+    """Top-K of every row of a [b, sq, n_c] matrix whose non-selectable
+    entries are -inf: the same rule as topk_select_row over the selectable
+    entries (any subset of the row), ascending block ids, -1 tail."""
     b, sq, n_c = scores.shape
     out = np.full((b, sq, K), -1, np.int32)
     for bi in range(b):
         for t in range(sq):
             row = scores[bi, t]
-            v = int(np.isfinite(row).sum())
-            out[bi, t] = topk_select_row(row[:v], K)
+            cand = np.flatnonzero(np.isfinite(row))
+            sel = topk_select_row(row[cand], K)
+            n = int((sel >= 0).sum())
+            out[bi, t, :n] = cand[sel[:n]]
     return out
 
 
@@ -214,14 +238,16 @@ def topk_select(scores, K: int):
 # Steps 4-5: sparse MQA over window + selected compressed rows + sink
 # ---------------------------------------------------------------------------
 
-def query_slots(t: int, idx_row, sq: int, n_c: int, ratio: int, window: int):
+def query_slots(t: int, idx_row, sq: int, n_c: int, ratio: int, window: int, doc_b=None):
     """KV rows that query t attends to, in the flat [n_kv] row space.
 
-    Window: raw rows max(0, t-window+1) .. t.  Compressed: row sq + j for every
-    entry j of the index row with 0 <= j < n_c and j < vis(t); other entries
-    are padding.  A repeated entry yields a repeated row (two terms).
+    Window: raw rows max(0, t-window+1) .. t (with document ids doc_b [sq],
+    only those of t's document).  Compressed: row sq + j for every entry j of
+    the index row with 0 <= j < n_c and j < vis(t); other entries are
+    padding.  A repeated entry yields a repeated row (two terms).
     """
-    raw = list(range(max(0, t - window + 1), t + 1))
+    raw = [k for k in range(max(0, t - window + 1), t + 1)
+           if doc_b is None or doc_b[k] == doc_b[t]]
     vis = visible_blocks(t, ratio)
     comp = [sq + int(j) for j in idx_row if 0 <= int(j) < n_c and int(j) < vis]
     return np.asarray(raw + comp, dtype=np.int64)
@@ -251,11 +277,12 @@ def attn_fwd_query(q_t, kv_b, slots, sink_h, scale: float):
 
 
 def attn_fwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int,
-             rows=None, out_dtype: str = "fp64"):
+             rows=None, out_dtype: str = "fp64", doc_ids=None):
     """O [b, sq, H, d] (rounded once to out_dtype) and LSE [b, sq, H].
 
     ``rows``: optional list of (b, t) pairs; only those rows are computed and
     the results come back as arrays of shape [len(rows), H, d] / [len(rows), H].
+    ``doc_ids`` [b, sq]: optional document ids restricting the window.
     """
     b, sq, H, d = q.shape
     n_c = kv_full.shape[1] - sq
@@ -264,7 +291,8 @@ def attn_fwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int,
     O = np.zeros((len(pairs), H, d))
     L = np.zeros((len(pairs), H))
     for n, (bi, t) in enumerate(pairs):
-        slots = query_slots(t, idx[bi, t], sq, n_c, ratio, window)
+        slots = query_slots(t, idx[bi, t], sq, n_c, ratio, window,
+                            None if doc_ids is None else doc_ids[bi])
         o, lse, _, _ = attn_fwd_query(q[bi, t], kv_full[bi], slots, sink_h, scale)
         O[n], L[n] = o, lse
     O = round_to_storage(O, out_dtype)
@@ -293,7 +321,8 @@ def attn_bwd_query(q_t, kv_b, slots, sink_h, scale: float, dO_t):
     return dq, dkv_slots, dsink
 
 
-def attn_bwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int, dO, rows=None):
+def attn_bwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int, dO, rows=None,
+             doc_ids=None):
     """dq [b, sq, H, d], dkv [b, n_kv, d] and dsink [H].
 
     The slot contributions scatter-add into the compact [b, n_kv, d] buffer
@@ -310,7 +339,8 @@ def attn_bwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int, dO, r
     dkv = np.zeros((b, n_kv, d))
     dsink = np.zeros(H)
     for n, (bi, t) in enumerate(pairs):
-        slots = query_slots(t, idx[bi, t], sq, n_c, ratio, window)
+        slots = query_slots(t, idx[bi, t], sq, n_c, ratio, window,
+                            None if doc_ids is None else doc_ids[bi])
         dq_t, dkv_s, ds_t = attn_bwd_query(q[bi, t], kv_full[bi], slots, sink_h, scale, dO[bi, t])
         dq[n] = dq_t
         np.add.at(dkv[bi], slots, dkv_s)

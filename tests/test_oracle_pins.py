@@ -238,11 +238,12 @@ def test_topk_ties_from_relu_zeros_and_duplicate_keys():
 # attention: dense masked attention through torch's SDPA in float64
 # ---------------------------------------------------------------------------
 
-def _dense_sdpa(q, kv, idx, sink, scale, window, ratio, dO=None):
+def _dense_sdpa(q, kv, idx, sink, scale, window, ratio, dO=None, doc_ids=None):
     """The same layer as dense attention over all n_kv rows plus one sink key,
     with an explicit additive mask: log(multiplicity) for allowed rows, -inf
-    elsewhere.  Evaluated by torch.nn.functional.scaled_dot_product_attention
-    in float64; gradients by torch autograd."""
+    elsewhere (window rows of another document are not allowed).  Evaluated by
+    torch.nn.functional.scaled_dot_product_attention in float64; gradients by
+    torch autograd."""
     b, sq, H, d = q.shape
     n_kv = kv.shape[1]
     n_c = n_kv - sq
@@ -250,6 +251,8 @@ def _dense_sdpa(q, kv, idx, sink, scale, window, ratio, dO=None):
     for bi in range(b):
         for t in range(sq):
             count[bi, t, max(0, t - window + 1):t + 1] = 1.0
+            if doc_ids is not None:
+                count[bi, t, :sq] *= doc_ids[bi] == doc_ids[bi, t]
             for j in idx[bi, t]:
                 if 0 <= j < n_c and j < (t + 1) // ratio:
                     count[bi, t, sq + j] += 1.0
@@ -428,3 +431,87 @@ def test_attn_rows_subset_matches_full():
         np.testing.assert_array_equal(Or[n], O[bi, t])
         np.testing.assert_array_equal(Lr[n], L[bi, t])
         np.testing.assert_allclose(dqr[n], dq[bi, t], atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# packed documents (doc_ids)
+# ---------------------------------------------------------------------------
+
+def test_attn_doc_window_matches_dense_sdpa():
+    """Arbitrary (not contiguous) document ids: the window keeps only rows of
+    the query's own document; selected compressed entries are taken as given."""
+    q, kv, idx, snk, scale, W, r, dO = _random_case(21, window=7)
+    rng = np.random.default_rng(22)
+    doc = rng.integers(0, 3, size=q.shape[:2]).astype(np.int32)
+    O, L = orc.attn_fwd(q, kv, idx, snk, scale, W, r, doc_ids=doc)
+    dq, dkv, dsink = orc.attn_bwd(q, kv, idx, snk, scale, W, r, dO, doc_ids=doc)
+    ref = _dense_sdpa(q, kv, idx, snk, scale, W, r, dO, doc_ids=doc)
+    for name, got in [("O", O), ("LSE", L), ("dq", dq), ("dkv", dkv), ("dsink", dsink)]:
+        np.testing.assert_allclose(got, ref[name], atol=1e-12, err_msg=name)
+    # one document everywhere is the plain layer
+    O1, _ = orc.attn_fwd(q, kv, idx, snk, scale, W, r, doc_ids=np.zeros_like(doc))
+    O0, _ = orc.attn_fwd(q, kv, idx, snk, scale, W, r)
+    np.testing.assert_array_equal(O1, O0)
+
+
+def test_indexer_topk_docs_brute_force():
+    """Selectable set by explicit loops (j < vis(t) and doc[j*ratio] == doc[t])
+    and the brute-force top-k over it, with many exact ties."""
+    rng = np.random.default_rng(23)
+    b, sq, H, d_I, r, K = 2, 48, 2, 3, 3, 4
+    q_I = rng.integers(-1, 2, size=(b, sq, H, d_I)).astype(np.float64)
+    k_I = rng.integers(-1, 2, size=(b, sq // r, d_I)).astype(np.float64)
+    w = rng.integers(0, 3, size=(b, sq, H)).astype(np.float64)
+    doc = rng.integers(0, 3, size=(b, sq)).astype(np.int32)
+    I = orc.indexer_scores(q_I, k_I, w, r, doc_ids=doc)
+    idx = orc.topk_select(I, K)
+    for bi in range(b):
+        for t in range(sq):
+            cand = [j for j in range(sq // r) if j < (t + 1) // r and doc[bi, j * r] == doc[bi, t]]
+            vals = [sum(w[bi, t, h] * max(0.0, float(q_I[bi, t, h] @ k_I[bi, j])) for h in range(H))
+                    for j in cand]
+            sel = [cand[i] for i in _brute_topk(vals, K) if i >= 0]
+            assert idx[bi, t].tolist() == sorted(sel) + [-1] * (K - len(sel))
+
+
+def test_packed_documents_equal_separate_runs():
+    """Documents packed into one sequence (boundaries on multiples of ratio)
+    give, for every document, exactly the results of running that document
+    alone: indexer + top-k (block ids shifted by the document's first block),
+    attention forward and backward (dkv rows and dsink summed over documents)."""
+    from compressed_sparse_attention_sum_gb300.inputs import packed_doc_ids
+    rng = np.random.default_rng(24)
+    b, sq, H, d, r, W, K, H_I, d_I = 1, 40, 2, 4, 4, 6, 3, 2, 3
+    n_c = sq // r
+    doc = packed_doc_ids(b, sq, r, 3, seed=5).numpy()
+    q_I = rng.standard_normal((b, sq, H_I, d_I))
+    k_I = rng.standard_normal((b, n_c, d_I))
+    w = rng.standard_normal((b, sq, H_I))
+    q = rng.standard_normal((b, sq, H, d))
+    kv_raw = rng.standard_normal((b, sq, d))
+    kv_c = rng.standard_normal((b, n_c, d))
+    kv = np.concatenate([kv_raw, kv_c], axis=1)
+    snk = rng.standard_normal(H)
+    dO = rng.standard_normal((b, sq, H, d))
+    scale = d ** -0.5
+    idx = orc.topk_select(orc.indexer_scores(q_I, k_I, w, r, doc_ids=doc), K)
+    O, L = orc.attn_fwd(q, kv, idx, snk, scale, W, r, doc_ids=doc)
+    dq, dkv, dsink = orc.attn_bwd(q, kv, idx, snk, scale, W, r, dO, doc_ids=doc)
+    starts = [0] + [t for t in range(1, sq) if doc[0, t] != doc[0, t - 1]]
+    ends = starts[1:] + [sq]
+    assert len(starts) == 3
+    dsink_sum = np.zeros(H)
+    for a, e in zip(starts, ends):
+        ja, nc_s = a // r, (e - a) // r
+        idx_s = orc.topk_select(orc.indexer_scores(q_I[:, a:e], k_I[:, ja:ja + nc_s], w[:, a:e], r), K)
+        np.testing.assert_array_equal(np.where(idx_s >= 0, idx_s + ja, -1), idx[:, a:e])
+        kv_s = np.concatenate([kv_raw[:, a:e], kv_c[:, ja:ja + nc_s]], axis=1)
+        O_s, L_s = orc.attn_fwd(q[:, a:e], kv_s, idx_s, snk, scale, W, r)
+        dq_s, dkv_s, ds_s = orc.attn_bwd(q[:, a:e], kv_s, idx_s, snk, scale, W, r, dO[:, a:e])
+        np.testing.assert_allclose(O[:, a:e], O_s, atol=1e-12)
+        np.testing.assert_allclose(L[:, a:e], L_s, atol=1e-12)
+        np.testing.assert_allclose(dq[:, a:e], dq_s, atol=1e-12)
+        np.testing.assert_allclose(dkv[:, a:e], dkv_s[:, :e - a], atol=1e-12)
+        np.testing.assert_allclose(dkv[:, sq + ja:sq + ja + nc_s], dkv_s[:, e - a:], atol=1e-12)
+        dsink_sum += ds_s
+    np.testing.assert_allclose(dsink, dsink_sum, atol=1e-12)
