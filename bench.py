@@ -254,7 +254,7 @@ def run_gpu(args, rank, world, local_rank):
     from compressed_sparse_attention_sum_gb300 import build as _build
     _build.build()
     from compressed_sparse_attention_sum_gb300 import csa
-    from compressed_sparse_attention_sum_gb300.inputs import CONFIGS, make_inputs
+    from compressed_sparse_attention_sum_gb300.inputs import CONFIGS, make_inputs, packed_doc_ids
     lib = csa.load_library()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -277,20 +277,20 @@ def run_gpu(args, rank, world, local_rank):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(x):
+    def step(x, doc=None):
         kv_full[:, :sq].copy_(x["kv_raw"])          # raw rows of the KV buffer (layer input)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         ev[0].record(stream)
         csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:])
         ev[1].record(stream)
         csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio, workspace=ws,
-                             out_idx=idx)
+                             out_idx=idx, doc_ids=doc)
         ev[2].record(stream)
         csa.csa_attn_fwd(x["q"], kv_full, idx, x["sink"], cfg.scale, cfg.ratio, cfg.window, out=O,
-                         lse=L)
+                         lse=L, doc_ids=doc)
         ev[3].record(stream)
         csa.csa_attn_bwd(x["q"], kv_full, idx, x["sink"], cfg.scale, cfg.ratio, cfg.window, O, L,
-                         x["dO"], dq=dq, dkv=dkv, dsink=dsink)
+                         x["dO"], dq=dq, dkv=dkv, dsink=dsink, doc_ids=doc)
         ev[4].record(stream)
         # the compressed rows' gradient flows back through the pooling into the
         # raw rows (accumulated in place) and the pooling scores
@@ -326,6 +326,28 @@ def run_gpu(args, rank, world, local_rank):
     ms_max = max_over_ranks(ms, world, dev)
     queries = b * sq
     value = world * queries / (ms_max / 1e3)
+
+    # ---- variant: the same layer holding 4 packed documents -------------------
+    # (window and indexer restricted to each query's document; same timing rules)
+    doc = packed_doc_ids(b, sq, cfg.ratio, 4, seed=rank).to(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(d_in, doc)
+    evs_doc = []
+    for _ in range(args.steps):
+        flush.zero_()
+        evs_doc.append(step(d_in, doc))
+    torch.cuda.synchronize()
+    names = ("compress", "indexer_topk", "attn_fwd", "attn_bwd", "compress_bwd")
+    doc_ms = max_over_ranks(sum(e[0].elapsed_time(e[5]) for e in evs_doc) / len(evs_doc), world,
+                            dev)
+    variant_docs = {
+        "workload": f"{cfg.name} with 4 packed documents (boundaries on multiples of the ratio)",
+        "ms_per_step": round(doc_ms, 4), "value": round(world * queries / (doc_ms / 1e3), 1),
+        "unit": "queries/s",
+        "kernels_ms": {n: round(sum(e[i].elapsed_time(e[i + 1]) for e in evs_doc) / len(evs_doc), 4)
+                       for i, n in enumerate(names)},
+    }
 
     # ---- end-to-end through host buffers -------------------------------------
     # Every step copies all of its inputs host -> device (pinned) and all of its
@@ -448,6 +470,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roofline,
         "kernels": kernels,
         "targets": targets,
+        "variants": {"docs4": variant_docs},
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
     }

@@ -36,14 +36,14 @@ SIGNATURES = {
                          + [_c_int] * 5 + [_c_p]),
     "csa_indexer_topk_workspace_size": (_c_sz, [_c_int] * 6 + [_c_int]),
     "csa_indexer_topk_min_workspace": (_c_sz, [_c_int, _c_int]),
-    "csa_indexer_topk": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7 + [_c_int, _c_p, _c_sz,
-                                                                                   _c_p]),
+    "csa_indexer_topk": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
+                         + [_c_int, _c_p, _c_sz, _c_p]),
     "csa_indexer_topk_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
                                  + [_c_int, _c_p]),
-    "csa_attn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p] + [_c_int] * 8 + [_c_int,
-                                                                                         _c_p]),
-    "csa_attn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
-                     + [_c_int] * 8 + [_c_int, _c_p]),
+    "csa_attn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p] + [_c_int] * 8
+                     + [_c_int, _c_p]),
+    "csa_attn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p,
+                              _c_p] + [_c_int] * 8 + [_c_int, _c_p]),
     "csa_get_device_status": (_c_int, [_c_p, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
 }
 
@@ -166,12 +166,13 @@ def csa_indexer_topk(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, topk
                      workspace: Optional[torch.Tensor] = None,
                      out_idx: Optional[torch.Tensor] = None,
                      out_score: Optional[torch.Tensor] = None, return_scores: bool = False,
-                     stream=None):
+                     stream=None, doc_ids: Optional[torch.Tensor] = None):
     """Lightning-indexer scores + exact causal top-k.
 
-    q_I [b, sq, H_I, d_I], k_I [b, n_c, d_I] (same dtype), w [b, sq, H_I] fp32.
-    Returns idx [b, sq, K] int32 (and the fp32 scores [b, sq, K] when
-    return_scores or out_score is given).
+    q_I [b, sq, H_I, d_I], k_I [b, n_c, d_I] (same dtype), w [b, sq, H_I] fp32,
+    doc_ids [b, sq] int32 (optional: packed documents, a block is selectable
+    only by queries of its own document).  Returns idx [b, sq, K] int32 (and
+    the fp32 scores [b, sq, K] when return_scores or out_score is given).
     """
     lib = load_library()
     _need(q_I, "q_I")
@@ -192,8 +193,11 @@ def csa_indexer_topk(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, topk
         out_score = torch.empty(b, sq, K, dtype=torch.float32, device=dev)
     if out_score is not None:
         _need(out_score, "out_score", dtype=torch.float32)
+    if doc_ids is not None:
+        _need(doc_ids, "doc_ids", dtype=torch.int32)
     _check("csa_indexer_topk", lib.csa_indexer_topk(
-        q_I.data_ptr(), k_I.data_ptr(), w.data_ptr(), out_idx.data_ptr(), _ptr(out_score), b, sq,
+        q_I.data_ptr(), k_I.data_ptr(), w.data_ptr(), _ptr(doc_ids), out_idx.data_ptr(),
+        _ptr(out_score), b, sq,
         n_c, H_I, d_I, ratio, topk, _dt(q_I), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     if out_score is not None:
@@ -204,8 +208,11 @@ def csa_indexer_topk(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, topk
 def csa_attn_fwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Tensor],
                  sink: Optional[torch.Tensor], scale: float, ratio: int, window: int,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Sparse MQA forward; idx None = every visible compressed block."""
+                 stream=None, doc_ids: Optional[torch.Tensor] = None
+                 ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse MQA forward; idx None = every visible compressed block;
+    doc_ids [b, sq] int32 (optional) keeps only window rows of the query's
+    own document."""
     lib = load_library()
     _need(q, "q")
     _need(kv_full, "kv_full", dtype=q.dtype)
@@ -223,8 +230,11 @@ def csa_attn_fwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Ten
         lse = torch.empty(b, sq, H, dtype=torch.float32, device=q.device)
     _need(out, "out", dtype=q.dtype)
     _need(lse, "lse", dtype=torch.float32)
+    if doc_ids is not None:
+        _need(doc_ids, "doc_ids", dtype=torch.int32)
     _check("csa_attn_fwd", lib.csa_attn_fwd(
-        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), float(scale), out.data_ptr(),
+        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), _ptr(doc_ids), float(scale),
+        out.data_ptr(),
         lse.data_ptr(), b, sq, H, d, n_c, ratio, window, K, _dt(q), _stream(stream)))
     return out, lse
 
@@ -233,8 +243,10 @@ def csa_attn_bwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Ten
                  sink: Optional[torch.Tensor], scale: float, ratio: int, window: int,
                  o: torch.Tensor, lse: torch.Tensor, dO: torch.Tensor,
                  dq: Optional[torch.Tensor] = None, dkv: Optional[torch.Tensor] = None,
-                 dsink: Optional[torch.Tensor] = None, stream=None):
-    """Sparse MQA backward; returns (dq, dkv, dsink) in fp32."""
+                 dsink: Optional[torch.Tensor] = None, stream=None,
+                 doc_ids: Optional[torch.Tensor] = None):
+    """Sparse MQA backward; returns (dq, dkv, dsink) in fp32.  doc_ids as in
+    csa_attn_fwd."""
     lib = load_library()
     _need(q, "q")
     _need(kv_full, "kv_full", dtype=q.dtype)
@@ -257,8 +269,11 @@ def csa_attn_bwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Ten
         dsink = torch.empty(H, **f32)
     _need(dq, "dq", dtype=torch.float32)
     _need(dkv, "dkv", dtype=torch.float32)
+    if doc_ids is not None:
+        _need(doc_ids, "doc_ids", dtype=torch.int32)
     _check("csa_attn_bwd", lib.csa_attn_bwd(
-        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), float(scale), o.data_ptr(),
+        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), _ptr(doc_ids), float(scale),
+        o.data_ptr(),
         lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dkv.data_ptr(), _ptr(dsink), b, sq, H, d,
         n_c, ratio, window, K, _dt(q), _stream(stream)))
     return dq, dkv, dsink

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MT>::NT) attn_fwd_mma(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
     const int32_t* __restrict__ idx, const float* __restrict__ sink, float scale,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int sq, int H, int n_c, int ratio,
-    int window, int K) {
+    int window, int K, const int32_t* __restrict__ doc) {
   using C = FwdCfg<D, MT>;
   constexpr int NS = C::NS, LDQ = C::LDQ, LDS = C::LDS, LDP = C::LDP, NT = C::NT, NW = C::NW;
   constexpr int NQ = NS / 32;      // n8-tiles per warp in the score phase
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MT>::NT) attn_fwd_mma(
 
   if (w == 0) {
     const int c = build_slots_warp(rows, idx ? idx + ((long long)bi * sq + t) * K : nullptr, K, t,
-                                   sq, n_c, ratio, window);
+                                   sq, n_c, ratio, window, doc ? doc + (long long)bi * sq : nullptr);
     if (lane == 0) s_count = c;
   }
   load_heads<D, C::ROWS, LDQ, NT>(Qs, q + ((long long)bi * sq + t) * H * D, h0, H);
@@ -372,7 +372,8 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
     const int32_t* __restrict__ idx, const float* __restrict__ sink, float scale,
     const __nv_bfloat16* __restrict__ o, const float* __restrict__ lse,
     const __nv_bfloat16* __restrict__ dO, float* __restrict__ dq, float* __restrict__ dkv,
-    float* __restrict__ dsink, int sq, int H, int n_c, int ratio, int window, int K) {
+    float* __restrict__ dsink, int sq, int H, int n_c, int ratio, int window, int K,
+    const int32_t* __restrict__ doc) {
   using C = BwdCfg<D, MT>;
   constexpr int NS = C::NS, LDQ = C::LDQ, LDP = C::LDP, NT = C::NT;
   constexpr int NQ = NS / 32;
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
 
   if (w == 0) {
     const int c = build_slots_warp(rows, idx ? idx + ((long long)bi * sq + t) * K : nullptr, K, t,
-                                   sq, n_c, ratio, window);
+                                   sq, n_c, ratio, window, doc ? doc + (long long)bi * sq : nullptr);
     if (lane == 0) s_count = c;
   }
   load_heads<D, C::ROWS, LDQ, NT>(Qs, q + qrow * D, h0, H);
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
 template <int D, int MT>
 static cudaError_t run_fwd(const void* q, const void* kv, const int32_t* idx, const float* sink,
                            float scale, void* o, float* lse, int b, int sq, int H, int n_c,
-                           int ratio, int window, int K, cudaStream_t s) {
+                           int ratio, int window, int K, cudaStream_t s, const int32_t* doc) {
   using C = FwdCfg<D, MT>;
   const size_t smem = C::OFF_ROWS + (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   auto k = attn_fwd_mma<D, MT>;
@@ -611,7 +612,7 @@ static cudaError_t run_fwd(const void* q, const void* kv, const int32_t* idx, co
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)sq, (unsigned)b, (unsigned)((H + C::ROWS - 1) / C::ROWS));
   k<<<grid, C::NT, smem, s>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
-                              (__nv_bfloat16*)o, lse, sq, H, n_c, ratio, window, K);
+                              (__nv_bfloat16*)o, lse, sq, H, n_c, ratio, window, K, doc);
     count_launches(1);
   return cudaGetLastError();
 }
@@ -620,7 +621,7 @@ template <int D, int MT>
 static cudaError_t run_bwd(const void* q, const void* kv, const int32_t* idx, const float* sink,
                            float scale, const void* o, const float* lse, const void* dO, float* dq,
                            float* dkv, float* dsink, int b, int sq, int H, int n_c, int ratio,
-                           int window, int K, cudaStream_t s) {
+                           int window, int K, cudaStream_t s, const int32_t* doc) {
   using C = BwdCfg<D, MT>;
   const size_t smem = C::OFF_ROWS + (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   auto k = attn_bwd_mma<D, MT>;
@@ -629,7 +630,7 @@ static cudaError_t run_bwd(const void* q, const void* kv, const int32_t* idx, co
   dim3 grid((unsigned)sq, (unsigned)b, (unsigned)((H + C::ROWS - 1) / C::ROWS));
   k<<<grid, C::NT, smem, s>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
                               (const __nv_bfloat16*)o, lse, (const __nv_bfloat16*)dO, dq, dkv,
-                              dsink, sq, H, n_c, ratio, window, K);
+                              dsink, sq, H, n_c, ratio, window, K, doc);
     count_launches(1);
   return cudaGetLastError();
 }
@@ -645,10 +646,10 @@ bool attn_mma_supported(int H, int d, int window, int K) {
 cudaError_t launch_attn_fwd_mma(const void* q, const void* kv, const int32_t* idx,
                                 const float* sink, float scale, void* o, float* lse, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s) {
+                                cudaStream_t s, const int32_t* doc) {
   const int mt = (H + 15) / 16;
 #define CSA_FWD(DD, MM) \
-  return run_fwd<DD, MM>(q, kv, idx, sink, scale, o, lse, b, sq, H, n_c, ratio, window, K, s)
+  return run_fwd<DD, MM>(q, kv, idx, sink, scale, o, lse, b, sq, H, n_c, ratio, window, K, s, doc)
   switch (d) {
     case 64:
       if (mt <= 1) CSA_FWD(64, 1);
@@ -672,11 +673,11 @@ cudaError_t launch_attn_bwd_mma(const void* q, const void* kv, const int32_t* id
                                 const float* sink, float scale, const void* o, const float* lse,
                                 const void* dO, float* dq, float* dkv, float* dsink, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s) {
+                                cudaStream_t s, const int32_t* doc) {
   const int mt = (H + 15) / 16;
 #define CSA_BWD(DD, MM)                                                                       \
   return run_bwd<DD, MM>(q, kv, idx, sink, scale, o, lse, dO, dq, dkv, dsink, b, sq, H, n_c, \
-                         ratio, window, K, s)
+                         ratio, window, K, s, doc)
   switch (d) {
     case 64:
       if (mt <= 1) CSA_BWD(64, 1);

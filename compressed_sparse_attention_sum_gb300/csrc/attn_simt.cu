@@ -26,7 +26,8 @@ __global__ void __launch_bounds__(128) attn_fwd_simt(const T* __restrict__ q,
                                                      const float* __restrict__ sink, float scale,
                                                      T* __restrict__ o, float* __restrict__ lse,
                                                      int sq, int H, int d, int n_c, int ratio,
-                                                     int window, int K) {
+                                                     int window, int K,
+                                                     const int32_t* __restrict__ doc) {
   extern __shared__ int rows[];
   const int t = blockIdx.x, bi = blockIdx.y;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -34,7 +35,7 @@ __global__ void __launch_bounds__(128) attn_fwd_simt(const T* __restrict__ q,
   __shared__ int s_count;
   if (wid == 0) {
     const int c = build_slots_warp(rows, idx ? idx + ((long long)bi * sq + t) * K : nullptr, K, t,
-                                   sq, n_c, ratio, window);
+                                   sq, n_c, ratio, window, doc ? doc + (long long)bi * sq : nullptr);
     if (lane == 0) s_count = c;
   }
   __syncthreads();
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(128) attn_bwd_simt(
     const float* __restrict__ sink, float scale, const T* __restrict__ o,
     const float* __restrict__ lse, const T* __restrict__ dO, float* __restrict__ dq,
     float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H, int d, int n_c, int ratio,
-    int window, int K) {
+    int window, int K, const int32_t* __restrict__ doc) {
   extern __shared__ int rows[];
   const int t = blockIdx.x, bi = blockIdx.y;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(128) attn_bwd_simt(
   __shared__ int s_count;
   if (wid == 0) {
     const int c = build_slots_warp(rows, idx ? idx + ((long long)bi * sq + t) * K : nullptr, K, t,
-                                   sq, n_c, ratio, window);
+                                   sq, n_c, ratio, window, doc ? doc + (long long)bi * sq : nullptr);
     if (lane == 0) s_count = c;
   }
   __syncthreads();
@@ -157,18 +158,18 @@ __global__ void __launch_bounds__(128) attn_bwd_simt(
 cudaError_t launch_attn_fwd_simt(const void* q, const void* kv, const int32_t* idx,
                                  const float* sink, float scale, void* o, float* lse, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s) {
+                                 bool bf16, cudaStream_t s, const int32_t* doc) {
   dim3 grid((unsigned)sq, (unsigned)b);
   const size_t smem = (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   if (bf16) {
     attn_fwd_simt<__nv_bfloat16><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale, (__nv_bfloat16*)o,
-        lse, sq, H, d, n_c, ratio, window, K);
+        lse, sq, H, d, n_c, ratio, window, K, doc);
     count_launches(1);
   } else {
     attn_fwd_simt<float><<<grid, 32 * kSimtWarps, smem, s>>>((const float*)q, (const float*)kv,
                                                              idx, sink, scale, (float*)o, lse, sq,
-                                                             H, d, n_c, ratio, window, K);
+                                                             H, d, n_c, ratio, window, K, doc);
     count_launches(1);
   }
   return cudaGetLastError();
@@ -178,19 +179,19 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* i
                                  const float* sink, float scale, const void* o, const float* lse,
                                  const void* dO, float* dq, float* dkv, float* dsink, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s) {
+                                 bool bf16, cudaStream_t s, const int32_t* doc) {
   dim3 grid((unsigned)sq, (unsigned)b);
   const size_t smem = (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   if (bf16) {
     attn_bwd_simt<__nv_bfloat16><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
         (const __nv_bfloat16*)o, lse, (const __nv_bfloat16*)dO, dq, dkv, dsink, sq, H, d, n_c,
-        ratio, window, K);
+        ratio, window, K, doc);
     count_launches(1);
   } else {
     attn_bwd_simt<float><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const float*)q, (const float*)kv, idx, sink, scale, (const float*)o, lse,
-        (const float*)dO, dq, dkv, dsink, sq, H, d, n_c, ratio, window, K);
+        (const float*)dO, dq, dkv, dsink, sq, H, d, n_c, ratio, window, K, doc);
     count_launches(1);
   }
   return cudaGetLastError();

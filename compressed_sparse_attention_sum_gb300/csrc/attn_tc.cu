@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __nv_bfloat16* __restrict__ kv,
     const int32_t* __restrict__ idx, const float* __restrict__ sink, float scale,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int sq, int H, int n_c, int ratio,
-    int window, int K, int* __restrict__ status) {
+    int window, int K, int* __restrict__ status, const int32_t* __restrict__ doc) {
   constexpr int NW = (QB + 3) / 4;               // u64 count words per block id
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -163,7 +163,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
       if (tq < sq) {
         if (s < nwin) {
           const int raw = win0 + s;
-          if (raw <= tq && raw > tq - window) bv = 0.f;
+          if (raw <= tq && raw > tq - window &&
+              (doc == nullptr || __ldg(doc + (long long)bi * sq + raw) == __ldg(doc + (long long)bi * sq + tq)))
+            bv = 0.f;
         } else if (s < S_total) {
           const int j = ulist[s - nwin];
           const uint32_t cq = (uint32_t)(cnt[j * NW + (qq >> 2)] >> (16 * (qq & 3))) & 0xFFFFu;
@@ -362,7 +364,7 @@ bool attn_tc_supported(int H, int d, int n_c, int K) {
 cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx,
                                const float* sink, float scale, void* o, float* lse, int b, int sq,
                                int H, int n_c, int ratio, int window, int K, int* status,
-                               cudaStream_t s) {
+                               cudaStream_t s, const int32_t* doc) {
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   CUtensorMap tq;
@@ -383,7 +385,7 @@ cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);           \
     k<<<grid, atc::kThreads, smem, s>>>(tq, (const __nv_bfloat16*)kv, idx, sink, scale,       \
                                         (__nv_bfloat16*)o, lse, sq, H, n_c, ratio, window, K, \
-                                        status);                                                \
+                                        status, doc);                                           \
     count_launches(1);                                                                          \
   }
   if (QB == 8) CSA_TC_FWD(8)

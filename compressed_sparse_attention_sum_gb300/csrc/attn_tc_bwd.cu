@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     const int32_t* __restrict__ idx,
     const float* __restrict__ sink, float scale, const __nv_bfloat16* __restrict__ o,
     const float* __restrict__ lse, float* __restrict__ dq, float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H,
-    int n_c, int ratio, int window, int K, int* __restrict__ status) {
+    int n_c, int ratio, int window, int K, int* __restrict__ status,
+    const int32_t* __restrict__ doc) {
   constexpr int NW = (QB + 3) / 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -172,7 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       if (tq < sq) {
         if (s < nwin) {
           const int raw = win0 + s;
-          if (raw <= tq && raw > tq - window) bv = 0.f;
+          if (raw <= tq && raw > tq - window &&
+              (doc == nullptr || __ldg(doc + (long long)bi * sq + raw) == __ldg(doc + (long long)bi * sq + tq)))
+            bv = 0.f;
         } else if (s < S_total) {
           const int j = ulist[s - nwin];
           const uint32_t cq = (uint32_t)(cnt[j * NW + (qq >> 2)] >> (16 * (qq & 3))) & 0xFFFFu;
@@ -519,7 +522,8 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
                                const float* sink, float scale, const void* o, const float* lse,
                                const void* dO,
                                float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
-                               int ratio, int window, int K, int* status, cudaStream_t s) {
+                               int ratio, int window, int K, int* status, cudaStream_t s,
+                               const int32_t* doc) {
   CUtensorMap tq, tg;
   const long long rows = (long long)b * sq * H;
   if (!make_rows_map(&tq, q, rows) || !make_rows_map(&tg, dO, rows)) return cudaErrorInvalidValue;
@@ -533,7 +537,7 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
     k<<<grid, atb::kThreads, smem, s>>>(tq, tg, (const __nv_bfloat16*)kv,                   \
                                         (const __nv_bfloat16*)dO, idx, sink, scale,           \
                                         (const __nv_bfloat16*)o, lse, dq, dkv, dsink, sq, H,  \
-                                        n_c, ratio, window, K, status);                       \
+                                        n_c, ratio, window, K, status, doc);                  \
     count_launches(1);                                                                        \
   }
   if (QB == 8) CSA_TC_BWD(8)

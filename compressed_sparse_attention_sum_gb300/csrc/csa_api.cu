@@ -25,29 +25,30 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
                                const float* sink, float scale, const void* o, const float* lse,
                                const void* dO,
                                float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
-                               int ratio, int window, int K, int* status, cudaStream_t s);
+                               int ratio, int window, int K, int* status, cudaStream_t s,
+                               const int32_t* doc);
 cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx,
                                const float* sink, float scale, void* o, float* lse, int b, int sq,
                                int H, int n_c, int ratio, int window, int K, int* status,
-                               cudaStream_t s);
+                               cudaStream_t s, const int32_t* doc);
 cudaError_t launch_attn_fwd_mma(const void* q, const void* kv, const int32_t* idx,
                                 const float* sink, float scale, void* o, float* lse, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s);
+                                cudaStream_t s, const int32_t* doc);
 cudaError_t launch_attn_bwd_mma(const void* q, const void* kv, const int32_t* idx,
                                 const float* sink, float scale, const void* o, const float* lse,
                                 const void* dO, float* dq, float* dkv, float* dsink, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s);
+                                cudaStream_t s, const int32_t* doc);
 cudaError_t launch_attn_fwd_simt(const void* q, const void* kv, const int32_t* idx,
                                  const float* sink, float scale, void* o, float* lse, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s);
+                                 bool bf16, cudaStream_t s, const int32_t* doc);
 cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* idx,
                                  const float* sink, float scale, const void* o, const float* lse,
                                  const void* dO, float* dq, float* dkv, float* dsink, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s);
+                                 bool bf16, cudaStream_t s, const int32_t* doc);
 }  // namespace csa
 
 #include <atomic>
@@ -201,15 +202,16 @@ size_t csa_indexer_topk_workspace_size(int b, int sq, int n_c, int H_I, int d_I,
 }
 
 csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float* w,
-                              int32_t* topk_idx, float* topk_score, int b, int sq, int n_c,
-                              int H_I, int d_I, int ratio, int topk, csa_dtype_t dt,
-                              void* workspace, size_t workspace_bytes, csa_stream_t stream) {
+                              const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
+                              int b, int sq, int n_c, int H_I, int d_I, int ratio, int topk,
+                              csa_dtype_t dt, void* workspace, size_t workspace_bytes,
+                              csa_stream_t stream) {
   if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
   if (q_idx == nullptr || k_idx == nullptr || w == nullptr || topk_idx == nullptr ||
       workspace == nullptr)
     return CSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
-      !aligned16(topk_score) || !aligned16(workspace))
+      !aligned16(topk_score) || !aligned16(workspace) || !aligned16(doc_ids))
     return CSA_ERR_INVALID_ARG;
   if (b < 1 || sq < 1 || H_I < 1 || d_I < 8 || d_I % 8 != 0 || ratio < 1 || topk < 1)
     return CSA_ERR_INVALID_ARG;
@@ -240,19 +242,20 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
                                           H_I, d_I, ratio, dt == CSA_BF16, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     e = csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq, n_c,
-                                ratio, K, s);
+                                ratio, K, s, doc_ids);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   }
   return CSA_OK;
 }
 
 csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx,
-                          const float* sink, float scale, void* o, float* lse, int b, int sq,
-                          int H, int d, int n_c, int ratio, int window, int K, csa_dtype_t dt,
-                          csa_stream_t stream) {
+                          const float* sink, const int32_t* doc_ids, float scale, void* o,
+                          float* lse, int b, int sq, int H, int d, int n_c, int ratio, int window,
+                          int K, csa_dtype_t dt, csa_stream_t stream) {
   csa_status_t st = check_attn(q, kv_full, idx, scale, b, sq, H, d, n_c, ratio, window, K, dt);
   if (st != CSA_OK) return st;
-  if (o == nullptr || lse == nullptr || !aligned16(o) || !aligned16(lse) || !aligned16(sink))
+  if (o == nullptr || lse == nullptr || !aligned16(o) || !aligned16(lse) || !aligned16(sink) ||
+      !aligned16(doc_ids))
     return CSA_ERR_INVALID_ARG;
   const int Kl = idx ? K : n_c;
   cudaStream_t s = (cudaStream_t)stream;
@@ -262,26 +265,26 @@ csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx
   const bool warp_mma = wm && wm[0] == '1';
   if (dt == CSA_BF16 && !warp_mma && csa::attn_tc_supported(H, d, n_c, Kl))
     return from_cuda(csa::launch_attn_fwd_tc(q, kv_full, idx, sink, scale, o, lse, b, sq, H, n_c,
-                                             ratio, window, Kl, device_status_ptr(), s));
+                                             ratio, window, Kl, device_status_ptr(), s, doc_ids));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
     return from_cuda(csa::launch_attn_fwd_mma(q, kv_full, idx, sink, scale, o, lse, b, sq, H, d,
-                                              n_c, ratio, window, Kl, s));
+                                              n_c, ratio, window, Kl, s, doc_ids));
   return from_cuda(csa::launch_attn_fwd_simt(q, kv_full, idx, sink, scale, o, lse, b, sq, H, d,
-                                             n_c, ratio, window, Kl, dt == CSA_BF16, s));
+                                             n_c, ratio, window, Kl, dt == CSA_BF16, s, doc_ids));
 }
 
 csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx,
-                          const float* sink, float scale, const void* o, const float* lse,
-                          const void* dO, float* dq, float* dkv, float* dsink, int b, int sq,
-                          int H, int d, int n_c, int ratio, int window, int K, csa_dtype_t dt,
-                          csa_stream_t stream) {
+                          const float* sink, const int32_t* doc_ids, float scale, const void* o,
+                          const float* lse, const void* dO, float* dq, float* dkv, float* dsink,
+                          int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
+                          csa_dtype_t dt, csa_stream_t stream) {
   csa_status_t st = check_attn(q, kv_full, idx, scale, b, sq, H, d, n_c, ratio, window, K, dt);
   if (st != CSA_OK) return st;
   if (o == nullptr || lse == nullptr || dO == nullptr || dq == nullptr || dkv == nullptr)
     return CSA_ERR_INVALID_ARG;
   if (sink != nullptr && dsink == nullptr) return CSA_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(lse) || !aligned16(dO) || !aligned16(dq) || !aligned16(dkv) ||
-      !aligned16(dsink) || !aligned16(sink))
+      !aligned16(dsink) || !aligned16(sink) || !aligned16(doc_ids))
     return CSA_ERR_INVALID_ARG;
   const int Kl = idx ? K : n_c;
   cudaStream_t s = (cudaStream_t)stream;
@@ -294,13 +297,14 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
   if (dt == CSA_BF16 && !warp_mma && csa::attn_tc_bwd_supported(H, d, n_c, Kl))
     return from_cuda(csa::launch_attn_bwd_tc(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                              dsink, b, sq, H, n_c, ratio, window, Kl,
-                                             device_status_ptr(), s));
+                                             device_status_ptr(), s, doc_ids));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
     return from_cuda(csa::launch_attn_bwd_mma(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
-                                              dsink, b, sq, H, d, n_c, ratio, window, Kl, s));
+                                              dsink, b, sq, H, d, n_c, ratio, window, Kl, s,
+                                              doc_ids));
   return from_cuda(csa::launch_attn_bwd_simt(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                              dsink, b, sq, H, d, n_c, ratio, window, Kl,
-                                             dt == CSA_BF16, s));
+                                             dt == CSA_BF16, s, doc_ids));
 }
 
 csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out, int* site_out) {

@@ -90,16 +90,31 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Gather the attention slot rows of query t into `rows` (flat kv_full row ids
-// within the batch element): window rows max(0,t-W+1)..t, then sq+j for the
-// valid entries j of the index row (0 <= j < n_c and j < vis(t)), in index
-// order.  idx == nullptr means every visible block.  Executed by one warp;
-// returns the slot count to every lane.
+// within the batch element): window rows max(0,t-W+1)..t (with per-token
+// document ids doc_b, only those of t's document), then sq+j for the valid
+// entries j of the index row (0 <= j < n_c and j < vis(t)), in index order.
+// idx == nullptr means every visible block.  Executed by one warp; returns
+// the slot count to every lane.
 __device__ __forceinline__ int build_slots_warp(int* rows, const int32_t* idx_row, int K, int t,
-                                                int sq, int n_c, int ratio, int window) {
+                                                int sq, int n_c, int ratio, int window,
+                                                const int32_t* doc_b = nullptr) {
   const int lane = threadIdx.x & 31;
   const int w0 = max(0, t - window + 1);
-  const int nw = t - w0 + 1;
-  for (int i = lane; i < nw; i += 32) rows[i] = w0 + i;
+  int nw = t - w0 + 1;
+  if (doc_b == nullptr) {
+    for (int i = lane; i < nw; i += 32) rows[i] = w0 + i;
+  } else {
+    const int dt = doc_b[t];
+    int kept = 0;
+    for (int base = 0; base < nw; base += 32) {
+      const int k = w0 + base + lane;
+      const bool ok = base + lane < nw && doc_b[k] == dt;
+      const unsigned m = __ballot_sync(0xffffffffu, ok);
+      if (ok) rows[kept + __popc(m & ((1u << lane) - 1u))] = k;
+      kept += __popc(m);
+    }
+    nw = kept;
+  }
   const int vis = min((t + 1) / ratio, n_c);
   int count = nw;
   if (idx_row == nullptr) {

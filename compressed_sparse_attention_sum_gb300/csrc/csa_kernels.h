@@ -13,9 +13,11 @@ cudaError_t launch_compress(const void* kv, long long kv_bs, const void* score, 
                             bool bf16, cudaStream_t s);
 
 // Exact per-row top-K of the chunk of scores in ws (rows [t0, t0+nt) of every
-// batch element, laid out [b][nt][n_c]).
+// batch element, laid out [b][nt][n_c]).  doc (nullable, [b][sq]): per-token
+// document ids; a block is a candidate only for queries of its document.
 cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
-                               int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s);
+                               int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s,
+                               const int32_t* doc = nullptr);
 
 cudaError_t launch_compress_bwd(const void* kv, long long kv_bs, const void* score,
                                 int score_width, const float* g, long long g_bs, float* dkv,

@@ -108,7 +108,39 @@ __global__ void __launch_bounds__(256) indexer_scores_simt(
 // ----------------------------------------------------------------------------
 // Per-row exact top-K by 4-pass 8-bit radix select on order-preserving keys.
 // One warp per query row.
+//
+// Candidates of row t: blocks j < vis(t); with per-token document ids (packed
+// documents, "Refactor Deepseek v4 to use Attention Gym's Compressed Sparse
+// Attention": block j belongs to doc[j*ratio] and is selectable by t only in
+// t's document) only the blocks of t's document.  A non-candidate gets key 0,
+// which no finite score maps to.  Rows with at most K candidates emit all of
+// them, ascending, then -1.
 // ----------------------------------------------------------------------------
+
+// Emit every candidate (key != 0) of a row in ascending block order, then -1
+// up to K.  keys_at(j) gives the key of block j.
+template <typename KeyAt>
+__device__ __forceinline__ void emit_all_candidates(int vis, int K, KeyAt keys_at,
+                                                    const float* row, int32_t* oi, float* os) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int out_pos = 0;
+  for (int base = 0; base < vis; base += 32) {
+    const int j = base + lane;
+    const bool sel = j < vis && keys_at(j) != 0u;
+    const unsigned selm = __ballot_sync(0xffffffffu, sel);
+    if (sel) {
+      const int p = out_pos + __popc(selm & lt_mask);
+      oi[p] = j;
+      if (os) os[p] = row[j];
+    }
+    out_pos += __popc(selm);
+  }
+  for (int s = out_pos + lane; s < K; s += 32) {
+    oi[s] = -1;
+    if (os) os[s] = 0.f;
+  }
+}
 __device__ __forceinline__ uint32_t order_key(float f) {
   const uint32_t u = __float_as_uint(f + 0.0f);  // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -118,7 +150,8 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
                                                           int32_t* __restrict__ out_idx,
                                                           float* __restrict__ out_score, int t0,
                                                           int nt, int b, int sq, int n_c,
-                                                          int ratio, int K) {
+                                                          int ratio, int K,
+                                                          const int32_t* __restrict__ doc) {
   extern __shared__ uint32_t smk[];
   const int warps = blockDim.x / 32;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -133,15 +166,27 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
   const float* row = ws + (size_t)r * n_c;
   int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
   float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
-  if (vis <= K) {
+  if (doc == nullptr && vis <= K) {
     for (int s = lane; s < K; s += 32) {
       oi[s] = s < vis ? s : -1;
       if (os) os[s] = s < vis ? row[s] : 0.f;
     }
     return;
   }
-  for (int j = lane; j < vis; j += 32) keys[j] = order_key(row[j]);
+  const int32_t* docb = doc ? doc + (size_t)bi * sq : nullptr;
+  const int dt = docb ? docb[t] : 0;
+  int ncand = 0;
+  for (int j = lane; j < vis; j += 32) {
+    const bool ok = docb == nullptr || __ldg(docb + (size_t)j * ratio) == dt;
+    keys[j] = ok ? order_key(row[j]) : 0u;
+    ncand += ok;
+  }
   __syncwarp();
+  ncand = __reduce_add_sync(FULL, ncand);
+  if (ncand <= K) {
+    emit_all_candidates(vis, K, [&](int j) { return keys[j]; }, row, oi, os);
+    return;
+  }
   uint32_t prefix = 0, pmask = 0;
   int need = K;
   for (int shift = 24; shift >= 0; shift -= 8) {
@@ -149,7 +194,7 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
     __syncwarp();
     for (int j = lane; j < vis; j += 32) {
       const uint32_t u = keys[j];
-      if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+      if (u != 0u && (u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
     }
     __syncwarp();
     // lane l owns bins 8*(31-l) .. 8*(31-l)+7, so lane 0 holds the highest bins
@@ -196,8 +241,8 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
   for (int base = 0; base < vis; base += 32) {
     const int j = base + lane;
     const uint32_t u = (j < vis) ? keys[j] : 0u;
-    const bool gt = (j < vis) && (u > prefix);
-    const bool eq = (j < vis) && (u == prefix);
+    const bool gt = u != 0u && u > prefix;
+    const bool eq = u != 0u && u == prefix;
     const unsigned eqm = __ballot_sync(FULL, eq);
     const bool sel = gt || (eq && (eq_seen + __popc(eqm & lt_mask)) < need);
     const unsigned selm = __ballot_sync(FULL, sel);
@@ -215,12 +260,13 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
 // holds the keys of blocks l, l+32, ...  A pass whose chosen bin holds exactly
 // the remaining count ends the search early: every key with the selected
 // prefix is taken and no tie needs breaking.
-template <int PER>
+template <int PER, bool DOC>
 __global__ void __launch_bounds__(256) topk_select_reg_kernel(const float* __restrict__ ws,
                                                               int32_t* __restrict__ out_idx,
                                                               float* __restrict__ out_score,
                                                               int t0, int nt, int b, int sq,
-                                                              int n_c, int ratio, int K) {
+                                                              int n_c, int ratio, int K,
+                                                              const int32_t* __restrict__ doc) {
   __shared__ int hist_all[8][256];
   const int warps = blockDim.x / 32;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -234,18 +280,46 @@ __global__ void __launch_bounds__(256) topk_select_reg_kernel(const float* __res
   const float* row = ws + (size_t)r * n_c;
   int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
   float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
-  if (vis <= K) {
+  if (!DOC && vis <= K) {
     for (int s = lane; s < K; s += 32) {
       oi[s] = s < vis ? s : -1;
       if (os) os[s] = s < vis ? row[s] : 0.f;
     }
     return;
   }
+  const int32_t* docb = DOC ? doc + (size_t)bi * sq : nullptr;
+  const int dt = DOC ? docb[t] : 0;
   uint32_t key[PER];
+  int ncand = 0;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int j = lane + 32 * i;
-    key[i] = j < vis ? order_key(row[j]) : 0u;      // 0: below every valid key
+    const bool ok = j < vis && (!DOC || __ldg(docb + (size_t)j * ratio) == dt);
+    key[i] = ok ? order_key(row[j]) : 0u;           // 0: not a candidate
+    ncand += ok;
+  }
+  if (DOC) ncand = __reduce_add_sync(FULL, ncand);
+  if (DOC && ncand <= K) {
+    // blocks l, l+32, ...: fetch the key of block j from its owner lane
+    int out_pos = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (32 * i >= vis) break;
+      const int j = lane + 32 * i;
+      const bool sel = key[i] != 0u;
+      const unsigned selm = __ballot_sync(FULL, sel);
+      if (sel) {
+        const int p = out_pos + __popc(selm & lt_mask);
+        oi[p] = j;
+        if (os) os[p] = row[j];
+      }
+      out_pos += __popc(selm);
+    }
+    for (int s2 = out_pos + lane; s2 < K; s2 += 32) {
+      oi[s2] = -1;
+      if (os) os[s2] = 0.f;
+    }
+    return;
   }
   uint32_t prefix = 0, pmask = 0;
   int need = K;
@@ -256,7 +330,8 @@ __global__ void __launch_bounds__(256) topk_select_reg_kernel(const float* __res
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int j = lane + 32 * i;
-      if (j < vis && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+      const bool cand = DOC ? key[i] != 0u : j < vis;
+      if (cand && (key[i] & pmask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
     }
     __syncwarp();
     int cnt[8];
@@ -307,7 +382,7 @@ __global__ void __launch_bounds__(256) topk_select_reg_kernel(const float* __res
     const int j = lane + 32 * i;
     if (32 * i >= vis) break;
     const uint32_t u = key[i];
-    const bool valid = j < vis;
+    const bool valid = DOC ? u != 0u : j < vis;
     bool sel;
     unsigned eqm = 0u;
     if (exact) {
@@ -350,13 +425,18 @@ cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, con
 }
 
 cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
-                               int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s) {
+                               int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s,
+                               const int32_t* doc) {
   const int rows = b * nt;
   if (n_c <= 2048) {
     const unsigned grid = (unsigned)((rows + 7) / 8);
 #define CSA_SEL(P)                                                                            \
-  topk_select_reg_kernel<P><<<grid, 256, 0, s>>>(ws, topk_idx, topk_score, t0, nt, b, sq, n_c, \
-                                                 ratio, K);                                   \
+  if (doc)                                                                                    \
+    topk_select_reg_kernel<P, true><<<grid, 256, 0, s>>>(ws, topk_idx, topk_score, t0, nt, b, \
+                                                         sq, n_c, ratio, K, doc);             \
+  else                                                                                        \
+    topk_select_reg_kernel<P, false><<<grid, 256, 0, s>>>(ws, topk_idx, topk_score, t0, nt,   \
+                                                          b, sq, n_c, ratio, K, nullptr);     \
   count_launches(1);
     if (n_c <= 256) { CSA_SEL(8) }
     else if (n_c <= 512) { CSA_SEL(16) }
@@ -372,7 +452,7 @@ cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_s
   dim3 grid((unsigned)((rows + warps - 1) / warps));
   cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   topk_select_kernel<<<grid, warps * 32, smem, s>>>(ws, topk_idx, topk_score, t0, nt, b, sq, n_c,
-                                                    ratio, K);
+                                                    ratio, K, doc);
   count_launches(1);
   return cudaGetLastError();
 }

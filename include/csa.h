@@ -159,14 +159,21 @@ size_t csa_indexer_topk_min_workspace(int b, int n_c);
  *   folds any softmax scale into it).
  * Selection ("Add the min-memory DSA attention kernels": tie-exact routing,
  * support sorted by position): the K = min(topk, n_c) largest scores of the
- * row, ties to the lower j, written in ascending j; rows with vis(t) < K
- * hold all visible blocks followed by -1.
+ * row, ties to the lower j, written in ascending j; rows with fewer than K
+ * candidates hold all of them followed by -1.
+ * Packed documents ("Refactor Deepseek v4 ...", doc_ids isolation): with
+ * doc_ids, block j covers tokens [j*ratio, (j+1)*ratio), belongs to
+ * doc_ids[b, j*ratio], and is a candidate for query t only when
+ * doc_ids[b,t] == doc_ids[b, j*ratio] (and j < vis(t)).  Documents are
+ * expected to start on multiples of ratio, so that no block mixes two.
  * Products are bf16 x bf16 (or fp32 x fp32) with fp32 accumulation; the
  * selection compares the fp32 scores exactly (-0 equals +0).
  *
  *   q_idx       in   [b, sq, H_I, d_I] dt
  *   k_idx       in   [b, n_c, d_I]     dt
  *   w           in   [b, sq, H_I]      fp32
+ *   doc_ids     in   [b, sq]           int32 document id per token; NULL =
+ *                                      one document (every visible block)
  *   topk_idx    out  [b, sq, K]        int32
  *   topk_score  out  [b, sq, K]        fp32 scores of the selected blocks
  *                                      (0 at -1 slots); may be NULL
@@ -176,7 +183,7 @@ size_t csa_indexer_topk_min_workspace(int b, int n_c);
  * UNSUPPORTED (d_I > 256, n_c > 16384).
  */
 csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float* w,
-                              int32_t* topk_idx, float* topk_score,
+                              const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
                               int b, int sq, int n_c, int H_I, int d_I, int ratio, int topk,
                               csa_dtype_t dt, void* workspace, size_t workspace_bytes,
                               csa_stream_t stream);
@@ -237,11 +244,17 @@ csa_status_t csa_indexer_topk_noalloc(const void* q_idx, const void* k_idx, cons
  *   o[b,t,h,:] = sum_i exp(s_i - lse) * kv_full[b,row_i,:]
  * idx == NULL selects every visible block (dense compressed mode); K is then
  * ignored.  fp32 softmax and accumulation; o is cast once to dt.
+ * doc_ids ([b, sq] int32, NULL = one document): packed documents ("Refactor
+ * Deepseek v4 ...", doc_ids isolation) - a window row k is kept only when
+ * doc_ids[b,k] == doc_ids[b,t]; the compressed entries are taken as given
+ * (the indexer called with the same doc_ids selects only the query's own
+ * document).
  * Errors: INVALID_ARG (null/misaligned pointers, d % 8, window < 1,
  * H < 1, K < 0, n_c != sq / ratio); UNSUPPORTED (d > 512, H > 64).
  */
 csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx,
-                          const float* sink, float scale, void* o, float* lse,
+                          const float* sink, const int32_t* doc_ids, float scale, void* o,
+                          float* lse,
                           int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
                           csa_dtype_t dt, csa_stream_t stream);
 
@@ -264,7 +277,8 @@ csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx
  * Errors: as csa_attn_fwd.
  */
 csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx,
-                          const float* sink, float scale, const void* o, const float* lse,
+                          const float* sink, const int32_t* doc_ids, float scale,
+                          const void* o, const float* lse,
                           const void* dO, float* dq, float* dkv, float* dsink,
                           int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
                           csa_dtype_t dt, csa_stream_t stream);

@@ -62,39 +62,44 @@ def test_invalid_arguments_rejected_on_host(lib):
     INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 4
     fake = 0x10000  # never dereferenced: validation fails first
     # null pointers
-    assert lib.csa_attn_fwd(None, fake, None, None, 0.1, fake, fake, 1, 8, 1, 64, 2, 4, 4, 0, 1,
+    assert lib.csa_attn_fwd(None, fake, None, None, None, 0.1, fake, fake, 1, 8, 1, 64, 2, 4, 4, 0, 1,
                             None) == INVALID
     # misaligned pointer
-    assert lib.csa_attn_fwd(fake + 2, fake, None, None, 0.1, fake, fake, 1, 8, 1, 64, 2, 4, 4, 0, 1,
+    assert lib.csa_attn_fwd(fake + 2, fake, None, None, None, 0.1, fake, fake, 1, 8, 1, 64, 2, 4, 4, 0, 1,
                             None) == INVALID
     # d not a multiple of 8
-    assert lib.csa_attn_fwd(fake, fake, None, None, 0.1, fake, fake, 1, 8, 1, 60, 2, 4, 4, 0, 1,
+    assert lib.csa_attn_fwd(fake, fake, None, None, None, 0.1, fake, fake, 1, 8, 1, 60, 2, 4, 4, 0, 1,
                             None) == INVALID
     # n_c inconsistent with sq / ratio
-    assert lib.csa_attn_fwd(fake, fake, None, None, 0.1, fake, fake, 1, 8, 1, 64, 3, 4, 4, 0, 1,
+    assert lib.csa_attn_fwd(fake, fake, None, None, None, 0.1, fake, fake, 1, 8, 1, 64, 3, 4, 4, 0, 1,
                             None) == INVALID
     # window < 1
-    assert lib.csa_attn_bwd(fake, fake, None, None, 0.1, fake, fake, fake, fake, fake, None, 1, 8, 1,
+    assert lib.csa_attn_bwd(fake, fake, None, None, None, 0.1, fake, fake, fake, fake, fake, None, 1, 8, 1,
                             64, 2, 4, 0, 0, 1, None) == INVALID
     # sink without dsink
-    assert lib.csa_attn_bwd(fake, fake, None, fake, 0.1, fake, fake, fake, fake, fake, None, 1, 8, 1,
+    assert lib.csa_attn_bwd(fake, fake, None, fake, None, 0.1, fake, fake, fake, fake, fake, None, 1, 8, 1,
                             64, 2, 4, 4, 0, 1, None) == INVALID
     # d > 512
-    assert lib.csa_attn_fwd(fake, fake, None, None, 0.1, fake, fake, 1, 8, 1, 520, 2, 4, 4, 0, 1,
+    assert lib.csa_attn_fwd(fake, fake, None, None, None, 0.1, fake, fake, 1, 8, 1, 520, 2, 4, 4, 0, 1,
                             None) == UNSUPPORTED
     # bad dtype
-    assert lib.csa_attn_fwd(fake, fake, None, None, 0.1, fake, fake, 1, 8, 1, 64, 2, 4, 4, 0, 7,
+    assert lib.csa_attn_fwd(fake, fake, None, None, None, 0.1, fake, fake, 1, 8, 1, 64, 2, 4, 4, 0, 7,
                             None) == INVALID
     # compress: score width must be 1 or d
     assert lib.csa_compress(fake, 512, fake, 3, fake, 128, 1, 8, 64, 4, 1, None) == INVALID
     # compress: ratio larger than sq
     assert lib.csa_compress(fake, 512, fake, 64, fake, 128, 1, 8, 64, 16, 1, None) == INVALID
     # indexer: workspace too small
-    assert lib.csa_indexer_topk(fake, fake, fake, fake, None, 1, 512, 128, 4, 64, 4, 16, 1, fake,
+    assert lib.csa_indexer_topk(fake, fake, fake, None, fake, None, 1, 512, 128, 4, 64, 4, 16, 1, fake,
                                 64, None) == WORKSPACE
     # indexer: topk < 1
-    assert lib.csa_indexer_topk(fake, fake, fake, fake, None, 1, 512, 128, 4, 64, 4, 0, 1, fake,
+    assert lib.csa_indexer_topk(fake, fake, fake, None, fake, None, 1, 512, 128, 4, 64, 4, 0, 1, fake,
                                 1 << 20, None) == INVALID
+    # misaligned document ids
+    assert lib.csa_attn_fwd(fake, fake, None, None, fake + 4, 0.1, fake, fake, 1, 8, 1, 64, 2, 4, 4,
+                            0, 1, None) == INVALID
+    assert lib.csa_indexer_topk(fake, fake, fake, fake + 4, fake, None, 1, 512, 128, 4, 64, 4, 16,
+                                1, fake, 1 << 30, None) == INVALID
     # device status needs an output pointer
     assert lib.csa_get_device_status(None, None, None) == INVALID
 
