@@ -55,6 +55,8 @@ __all__ = [
     "visible_blocks", "compress", "compress_bwd",
     "indexer_selectable", "indexer_scores", "indexer_scores_row", "topk_select", "topk_select_row",
     "query_slots", "attn_fwd_query", "attn_fwd", "attn_bwd_query", "attn_bwd",
+    "selected_entries", "indexer_teacher_row", "indexer_teacher",
+    "indexer_student_row", "indexer_kl_row", "indexer_loss",
 ]
 
 
@@ -349,3 +351,127 @@ def attn_bwd(q, kv_full, idx, sink, scale: float, window: int, ratio: int, dO, r
     if rows is None:
         dq = dq.reshape(b, sq, H, d)
     return dq, dkv, dsink
+
+
+# ---------------------------------------------------------------------------
+# Indexer training path: teacher target from the attention LSE, student
+# rescoring of the selected entries, KL distillation loss and its gradients
+# ---------------------------------------------------------------------------
+#
+# "Refactor Deepseek v4 to use Attention Gym's Compressed Sparse Attention"
+# (selected_attention commit; indexer distillation): the teacher of query t
+# over its selected entries is exp(logit - lse) summed over the heads and
+# L1-normalized, with lse the attention's per-head LSE (window, selected
+# entries and sink in the denominator); the student is a second pass of the
+# indexer over the selected entries only.  "Add unfused SBHD compressed
+# sparse attention" (review of the teacher normalization): one common
+# per-row shift keeps the mass from underflowing and cancels in the L1
+# normalization; a row without mass stays zero; the KL gradient with respect
+# to the student scores is predict * sum(target) - target, so a zero row
+# gets zero gradient.
+
+def selected_entries(idx_row, t: int, n_c: int, ratio: int):
+    """(slot positions, block ids) of the valid entries of one index row:
+    0 <= j < n_c and j < vis(t); repeated entries are kept (one term each)."""
+    vis = visible_blocks(t, ratio)
+    pos = [s for s, j in enumerate(idx_row) if 0 <= int(j) < n_c and int(j) < vis]
+    return np.asarray(pos, np.int64), np.asarray([int(idx_row[s]) for s in pos], np.int64)
+
+
+def indexer_teacher_row(q_t, kv_b, idx_row, lse_t, t: int, sq: int, ratio: int, scale: float):
+    """Teacher target [K] of query t.
+
+    T_s = sum_h exp(scale * q_h . kv[sq + j_s] - lse_h) over the valid slots
+    s (0 elsewhere), then target = T / sum(T).  Evaluated as
+    exp(a - c) with a = logit - lse and c = max a over the row's valid
+    (h, s): the shift cancels in the normalization and keeps the largest
+    term at 1.  A row without valid slots is all zero.
+    """
+    K = len(idx_row)
+    n_c = kv_b.shape[0] - sq
+    out = np.zeros(K)
+    pos, js = selected_entries(idx_row, t, n_c, ratio)
+    if pos.size == 0:
+        return out
+    logits = scale * (np.asarray(q_t, np.float64) @ np.asarray(kv_b, np.float64)[sq + js].T)
+    a = logits - np.asarray(lse_t, np.float64)[:, None]            # [H, n_valid]
+    T = np.exp(a - a.max()).sum(axis=0)
+    out[pos] = T / T.sum()
+    return out
+
+
+def indexer_teacher(q, kv_full, idx, lse, scale: float, ratio: int):
+    """Teacher targets [b, sq, K] (fp64) from the attention inputs and LSE."""
+    b, sq = q.shape[:2]
+    K = idx.shape[2]
+    out = np.zeros((b, sq, K))
+    for bi in range(b):
+        for t in range(sq):
+            out[bi, t] = indexer_teacher_row(q[bi, t], kv_full[bi], idx[bi, t], lse[bi, t], t, sq,
+                                             ratio, scale)
+    return out
+
+
+def indexer_student_row(q_I_t, k_I_b, w_t, idx_row, t: int, ratio: int):
+    """Student scores [K] of query t: the indexer score of each valid slot's
+    block, I_s = sum_h w_h max(0, q_I_h . k_I[j_s]); -inf at invalid slots."""
+    n_c = k_I_b.shape[0]
+    out = np.full(len(idx_row), -np.inf)
+    pos, js = selected_entries(idx_row, t, n_c, ratio)
+    if pos.size:
+        dots = np.asarray(q_I_t, np.float64) @ np.asarray(k_I_b, np.float64)[js].T   # [H_I, n]
+        out[pos] = np.asarray(w_t, np.float64) @ np.maximum(dots, 0.0)
+    return out
+
+
+def indexer_kl_row(I_row, target_row):
+    """KL(target || softmax(I)) over the valid (finite) slots of one row and
+    its gradient with respect to I: predict * sum(target) - target (zero at
+    invalid slots).  Terms with target 0 contribute 0 to the loss."""
+    I_row = np.asarray(I_row, np.float64)
+    tg = np.asarray(target_row, np.float64)
+    v = np.isfinite(I_row)
+    dI = np.zeros_like(I_row)
+    if not v.any():
+        return 0.0, dI
+    x = I_row[v]
+    logp = x - x.max() - np.log(np.exp(x - x.max()).sum())
+    tv = tg[v]
+    nz = tv > 0
+    loss = float((tv[nz] * (np.log(tv[nz]) - logp[nz])).sum())
+    dI[v] = np.exp(logp) * tv.sum() - tv
+    return loss, dI
+
+
+def indexer_loss(q_I, k_I, w, idx, target, ratio: int):
+    """Per-row KL loss [b, sq] and its gradients dq_I [b, sq, H_I, d_I],
+    dk_I [b, n_c, d_I] (summed over every query and repeated slot that
+    selected the block) and dw [b, sq, H_I], through the student rescoring.
+
+    With G_hs = dI_s * w_h * [q_I_h . k_I[j_s] > 0]:
+      dq_I[t, h]   = sum_s G_hs k_I[j_s]
+      dk_I[j]     += sum_{t, s: j_s = j} sum_h G_hs q_I[t, h]
+      dw[t, h]     = sum_s dI_s max(0, q_I_h . k_I[j_s])
+    """
+    q_I = np.asarray(q_I, np.float64)
+    k_I = np.asarray(k_I, np.float64)
+    w = np.asarray(w, np.float64)
+    b, sq, H_I, d_I = q_I.shape
+    n_c = k_I.shape[1]
+    loss = np.zeros((b, sq))
+    dq = np.zeros_like(q_I)
+    dk = np.zeros_like(k_I)
+    dw = np.zeros_like(w)
+    for bi in range(b):
+        for t in range(sq):
+            I = indexer_student_row(q_I[bi, t], k_I[bi], w[bi, t], idx[bi, t], t, ratio)
+            loss[bi, t], dI = indexer_kl_row(I, target[bi, t])
+            pos, js = selected_entries(idx[bi, t], t, n_c, ratio)
+            if pos.size == 0:
+                continue
+            dots = q_I[bi, t] @ k_I[bi][js].T                    # [H_I, n]
+            g = dI[pos][None, :] * w[bi, t][:, None] * (dots > 0)
+            dq[bi, t] = g @ k_I[bi][js]
+            np.add.at(dk[bi], js, g.T @ q_I[bi, t])
+            dw[bi, t] = np.maximum(dots, 0.0) @ dI[pos]
+    return loss, dq, dk, dw

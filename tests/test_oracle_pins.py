@@ -515,3 +515,124 @@ def test_packed_documents_equal_separate_runs():
         np.testing.assert_allclose(dkv[:, sq + ja:sq + ja + nc_s], dkv_s[:, e - a:], atol=1e-12)
         dsink_sum += ds_s
     np.testing.assert_allclose(dsink, dsink_sum, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# indexer training path (teacher, student rescoring, KL)
+# ---------------------------------------------------------------------------
+
+def _teacher_by_head_mass(q, kv, idx, sink, scale, window, ratio):
+    """The teacher the other way round (review of the teacher normalization
+    in "Add unfused SBHD compressed sparse attention"): per head, the
+    compressed mass m_h = sigmoid(lse_compressed - lse_window_and_sink) times
+    the softmax over the compressed entries, summed over heads and
+    L1-normalized.  Log-space throughout; no attention LSE is used."""
+    b, sq, H, d = q.shape
+    n_c = kv.shape[1] - sq
+    K = idx.shape[2]
+    out = np.zeros((b, sq, K))
+    for bi in range(b):
+        for t in range(sq):
+            pos, js = orc.selected_entries(idx[bi, t], t, n_c, ratio)
+            if pos.size == 0:
+                continue
+            rows = list(range(max(0, t - window + 1), t + 1))
+            lw = scale * q[bi, t] @ kv[bi, rows].T                       # [H, W]
+            l_nc = np.logaddexp(np.log(np.exp(lw - lw.max(1, keepdims=True)).sum(1))
+                                + lw.max(1), sink)
+            lc = scale * q[bi, t] @ kv[bi, sq + js].T                    # [H, n]
+            l_c = np.log(np.exp(lc - lc.max(1, keepdims=True)).sum(1)) + lc.max(1)
+            soft = np.exp(lc - l_c[:, None])
+            log_m = -np.logaddexp(0.0, -(l_c - l_nc))                    # log sigmoid
+            T = (np.exp(log_m - log_m.max())[:, None] * soft).sum(0)
+            out[bi, t, pos] = T / T.sum()
+    return out
+
+
+def test_teacher_matches_head_mass_formula():
+    q, kv, idx, snk, scale, W, r, _ = _random_case(41, window=6, K=5)
+    _, L = orc.attn_fwd(q, kv, idx, snk, scale, W, r)
+    T = orc.indexer_teacher(q, kv, idx, L, scale, r)
+    np.testing.assert_allclose(T, _teacher_by_head_mass(q, kv, idx, snk, scale, W, r), atol=1e-12)
+    s = T.sum(axis=2)
+    assert np.all((np.abs(s - 1) < 1e-12) | (s == 0))
+
+
+def test_teacher_survives_window_dominated_rows():
+    """Window logits about 1000 above every compressed logit: exp(logit - lse)
+    underflows even in float64, yet the shifted teacher is the proper
+    distribution (the conditional softmax weighted by the log-space masses)."""
+    q, kv, idx, snk, scale, W, r, _ = _random_case(42, b=1, sq=24, H=2, window=4, K=3)
+    kv[:, :24] *= 0.0
+    kv[:, :24, 0] = 1.0
+    kv[:, 24:, 0] = 0.0
+    q[..., 0] = 1000.0 / scale                     # window logits = 1000, compressed ones O(1)
+    _, L = orc.attn_fwd(q, kv, idx, snk, scale, W, r)
+    lc = scale * np.einsum("hd,nd->hn", q[0, 23], kv[0, 24:])
+    assert np.all(np.exp(lc - L[0, 23][:, None]) == 0.0)       # the plain form underflows
+    T = orc.indexer_teacher(q, kv, idx, L, scale, r)
+    ref = _teacher_by_head_mass(q, kv, idx, snk, scale, W, r)
+    np.testing.assert_allclose(T, ref, atol=1e-12)
+    has = np.array([orc.selected_entries(idx[0, t], t, 24 // r, r)[0].size > 0 for t in range(24)])
+    assert has.any() and np.allclose(T[0, has].sum(1), 1.0)
+    assert np.all(T[0, ~has] == 0.0)
+
+
+def test_indexer_loss_matches_autograd():
+    """Student rescoring + KL against torch autograd in float64 (log_softmax
+    over each row's valid slots), with repeated and invalid entries."""
+    rng = np.random.default_rng(43)
+    b, sq, H_I, d_I, r, K = 2, 20, 3, 4, 2, 6
+    n_c = sq // r
+    q_I = rng.standard_normal((b, sq, H_I, d_I))
+    k_I = rng.standard_normal((b, n_c, d_I))
+    w = rng.standard_normal((b, sq, H_I))
+    idx = rng.integers(-1, n_c + 1, size=(b, sq, K)).astype(np.int32)
+    idx[:, :, 1] = idx[:, :, 0]
+    target = np.zeros((b, sq, K))
+    for bi in range(b):
+        for t in range(sq):
+            pos, _ = orc.selected_entries(idx[bi, t], t, n_c, r)
+            if pos.size:
+                v = rng.random(pos.size)
+                v[0] = 0.0                                   # a zero-target slot
+                target[bi, t, pos] = v / v.sum() if v.sum() > 0 else 0.0
+    loss, dq, dk, dw = orc.indexer_loss(q_I, k_I, w, idx, target, r)
+    qt = torch.tensor(q_I, requires_grad=True)
+    kt = torch.tensor(k_I, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    total = torch.zeros((), dtype=torch.float64)
+    ref_loss = np.zeros((b, sq))
+    for bi in range(b):
+        for t in range(sq):
+            pos, js = orc.selected_entries(idx[bi, t], t, n_c, r)
+            if pos.size == 0:
+                continue
+            dots = qt[bi, t] @ kt[bi, torch.tensor(js)].T
+            I = wt[bi, t] @ torch.relu(dots)
+            logp = torch.log_softmax(I, dim=0)
+            tg = torch.tensor(target[bi, t, pos])
+            nz = tg > 0
+            row = (tg[nz] * (torch.log(tg[nz]) - logp[nz])).sum()
+            ref_loss[bi, t] = row.item()
+            total = total + row
+    total.backward()
+    np.testing.assert_allclose(loss, ref_loss, atol=1e-12)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dw, wt.grad.numpy(), atol=1e-12)
+
+
+def test_indexer_loss_zero_target_row_has_zero_gradient():
+    rng = np.random.default_rng(44)
+    q_I = rng.standard_normal((1, 8, 2, 3))
+    k_I = rng.standard_normal((1, 4, 3))
+    w = rng.standard_normal((1, 8, 2))
+    idx = np.tile(np.arange(3, dtype=np.int32), (1, 8, 1))
+    loss, dq, dk, dw = orc.indexer_loss(q_I, k_I, w, idx, np.zeros((1, 8, 3)), 2)
+    assert np.all(loss == 0) and np.all(dq == 0) and np.all(dk == 0) and np.all(dw == 0)
+    # a normalized target equal to the student's own distribution: zero gradient
+    I = orc.indexer_student_row(q_I[0, 7], k_I[0], w[0, 7], idx[0, 7], 7, 2)
+    p = np.exp(I - I.max()) / np.exp(I - I.max()).sum()
+    l, dI = orc.indexer_kl_row(I, p)
+    assert abs(l) < 1e-14 and np.abs(dI).max() < 1e-15
