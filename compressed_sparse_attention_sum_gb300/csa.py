@@ -44,6 +44,9 @@ SIGNATURES = {
                      + [_c_int, _c_p]),
     "csa_attn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p,
                               _c_p] + [_c_int] * 8 + [_c_int, _c_p]),
+    "csa_indexer_teacher": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p] + [_c_int] * 7
+                            + [_c_int, _c_p]),
+    "csa_indexer_loss": (_c_int, [_c_p] * 9 + [_c_int] * 7 + [_c_int, _c_p]),
     "csa_get_device_status": (_c_int, [_c_p, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
 }
 
@@ -289,3 +292,50 @@ def csa_get_device_status(stream=None, with_site: bool = False):
     _check("csa_get_device_status", lib.csa_get_device_status(_stream(stream), ctypes.byref(v),
                                                               ctypes.byref(site)))
     return (v.value, site.value) if with_site else v.value
+
+
+def csa_indexer_teacher(q: torch.Tensor, kv_full: torch.Tensor, idx: torch.Tensor,
+                        lse: torch.Tensor, scale: float, ratio: int,
+                        out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Distillation target [b, sq, K] fp32 of the indexer: per valid slot,
+    sum over heads of exp(scale q.kv - lse), L1-normalized per row."""
+    lib = load_library()
+    _need(q, "q")
+    _need(kv_full, "kv_full", dtype=q.dtype)
+    _need(idx, "idx", dtype=torch.int32)
+    _need(lse, "lse", dtype=torch.float32)
+    b, sq, H, d = q.shape
+    n_c = kv_full.shape[1] - sq
+    K = idx.shape[2]
+    if out is None:
+        out = torch.empty(b, sq, K, dtype=torch.float32, device=q.device)
+    _need(out, "out", dtype=torch.float32)
+    _check("csa_indexer_teacher", lib.csa_indexer_teacher(
+        q.data_ptr(), kv_full.data_ptr(), idx.data_ptr(), lse.data_ptr(), float(scale),
+        out.data_ptr(), b, sq, H, d, n_c, ratio, K, _dt(q), _stream(stream)))
+    return out
+
+
+def csa_indexer_loss(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, idx: torch.Tensor,
+                     target: torch.Tensor, ratio: int, stream=None):
+    """KL distillation loss of the indexer over its selected entries and its
+    gradients: returns (loss [b, sq], dq_I, dk_I, dw), all fp32."""
+    lib = load_library()
+    _need(q_I, "q_I")
+    _need(k_I, "k_I", dtype=q_I.dtype)
+    _need(w, "w", dtype=torch.float32)
+    _need(idx, "idx", dtype=torch.int32)
+    _need(target, "target", dtype=torch.float32)
+    b, sq, H_I, d_I = q_I.shape
+    n_c = k_I.shape[1]
+    K = idx.shape[2]
+    f32 = dict(dtype=torch.float32, device=q_I.device)
+    loss = torch.empty(b, sq, **f32)
+    dq = torch.empty(b, sq, H_I, d_I, **f32)
+    dk = torch.empty(b, n_c, d_I, **f32)
+    dw = torch.empty(b, sq, H_I, **f32)
+    _check("csa_indexer_loss", lib.csa_indexer_loss(
+        q_I.data_ptr(), k_I.data_ptr(), w.data_ptr(), idx.data_ptr(), target.data_ptr(),
+        loss.data_ptr(), dq.data_ptr(), dk.data_ptr(), dw.data_ptr(), b, sq, n_c, H_I, d_I, ratio,
+        K, _dt(q_I), _stream(stream)))
+    return loss, dq, dk, dw

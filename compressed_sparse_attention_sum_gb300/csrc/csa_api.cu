@@ -49,6 +49,18 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* i
                                  const void* dO, float* dq, float* dkv, float* dsink, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
                                  bool bf16, cudaStream_t s, const int32_t* doc);
+bool indexer_teacher_mma_ok(int H, int d);
+bool indexer_loss_mma_ok(int H_I, int d_I);
+size_t indexer_teacher_smem(bool mma, int H, int d, int K);
+size_t indexer_loss_smem(bool mma, int H_I, int d_I, int K);
+cudaError_t launch_indexer_teacher(const void* q, const void* kv, const int32_t* idx,
+                                   const float* lse, float scale, float* target, int b, int sq,
+                                   int H, int d, int n_c, int ratio, int K, bool bf16,
+                                   cudaStream_t s);
+cudaError_t launch_indexer_loss(const void* q_I, const void* k_I, const float* w,
+                                const int32_t* idx, const float* target, float* loss, float* dq_I,
+                                float* dk_I, float* dw, int b, int sq, int H_I, int d_I, int n_c,
+                                int ratio, int K, bool bf16, cudaStream_t s);
 }  // namespace csa
 
 #include <atomic>
@@ -305,6 +317,53 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
   return from_cuda(csa::launch_attn_bwd_simt(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                              dsink, b, sq, H, d, n_c, ratio, window, Kl,
                                              dt == CSA_BF16, s, doc_ids));
+}
+
+csa_status_t csa_indexer_teacher(const void* q, const void* kv_full, const int32_t* idx,
+                                 const float* lse, float scale, float* target, int b, int sq,
+                                 int H, int d, int n_c, int ratio, int K, csa_dtype_t dt,
+                                 csa_stream_t stream) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (q == nullptr || kv_full == nullptr || idx == nullptr || lse == nullptr ||
+      target == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_full) || !aligned16(idx) || !aligned16(lse) ||
+      !aligned16(target))
+    return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || H < 1 || d < 8 || d % 8 != 0 || ratio < 1 || K < 1)
+    return CSA_ERR_INVALID_ARG;
+  if (sq < ratio || n_c != sq / ratio || !(scale == scale)) return CSA_ERR_INVALID_ARG;
+  if (d > kMaxD || H > kMaxH || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
+  const bool mma = dt == CSA_BF16 && csa::indexer_teacher_mma_ok(H, d);
+  if (csa::indexer_teacher_smem(mma, H, d, K) > 227 * 1024) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(csa::launch_indexer_teacher(q, kv_full, idx, lse, scale, target, b, sq, H, d,
+                                               n_c, ratio, K, dt == CSA_BF16,
+                                               (cudaStream_t)stream));
+}
+
+csa_status_t csa_indexer_loss(const void* q_idx, const void* k_idx, const float* w,
+                              const int32_t* idx, const float* target, float* loss,
+                              float* dq_idx, float* dk_idx, float* dw, int b, int sq, int n_c,
+                              int H_I, int d_I, int ratio, int K, csa_dtype_t dt,
+                              csa_stream_t stream) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (q_idx == nullptr || k_idx == nullptr || w == nullptr || idx == nullptr ||
+      target == nullptr || loss == nullptr || dq_idx == nullptr || dk_idx == nullptr ||
+      dw == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(idx) ||
+      !aligned16(target) || !aligned16(loss) || !aligned16(dq_idx) || !aligned16(dk_idx) ||
+      !aligned16(dw))
+    return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || H_I < 1 || d_I < 8 || d_I % 8 != 0 || ratio < 1 || K < 1)
+    return CSA_ERR_INVALID_ARG;
+  if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
+  if (d_I > kMaxDI || H_I > kMaxH || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
+  const bool mma = dt == CSA_BF16 && csa::indexer_loss_mma_ok(H_I, d_I);
+  if (csa::indexer_loss_smem(mma, H_I, d_I, K) > 227 * 1024) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(csa::launch_indexer_loss(q_idx, k_idx, w, idx, target, loss, dq_idx, dk_idx,
+                                            dw, b, sq, H_I, d_I, n_c, ratio, K, dt == CSA_BF16,
+                                            (cudaStream_t)stream));
 }
 
 csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out, int* site_out) {

@@ -284,6 +284,65 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
                           csa_dtype_t dt, csa_stream_t stream);
 
 /*
+ * csa_indexer_teacher - distillation target of the indexer.
+ *
+ * "Refactor Deepseek v4 to use Attention Gym's Compressed Sparse Attention"
+ * (indexer distillation): for query (b,t) and each slot s of its index row
+ * whose entry j is valid (0 <= j < n_c, j < vis(t)),
+ *   T[s] = sum_h exp(scale * q[b,t,h,:] . kv_full[b, sq+j, :] - lse[b,t,h])
+ * and target[b,t,:] = T / sum_s T (the teacher is detached: no gradient).
+ * lse is the attention forward's LSE (window, selected entries and sink in
+ * the denominator).  One common shift per row ("Add unfused SBHD compressed
+ * sparse attention", review of the teacher normalization) keeps the mass
+ * from underflowing; it cancels in the normalization.  Invalid slots and
+ * rows without valid slots hold 0.  A repeated entry gets the same value at
+ * each of its slots.
+ *
+ *   q        in  [b, sq, H, d] dt      kv_full in [b, sq+n_c, d] dt
+ *   idx      in  [b, sq, K] int32      lse     in [b, sq, H] fp32
+ *   target   out [b, sq, K] fp32
+ * Errors: INVALID_ARG (null/misaligned pointers, d % 8, K < 1,
+ * n_c != sq / ratio); UNSUPPORTED (d > 512, H > 64, K too large for the
+ * kernel's shared memory).
+ */
+csa_status_t csa_indexer_teacher(const void* q, const void* kv_full, const int32_t* idx,
+                                 const float* lse, float scale, float* target, int b, int sq,
+                                 int H, int d, int n_c, int ratio, int K, csa_dtype_t dt,
+                                 csa_stream_t stream);
+
+/*
+ * csa_indexer_loss - the indexer's KL distillation loss over its selected
+ * entries, and the gradients through a rescoring of those entries.
+ *
+ * Student ("Refactor Deepseek v4 ...", lightning indexer: a second pass over
+ * the selected entries only): for each valid slot s of query (b,t),
+ *   I[s] = sum_h w[b,t,h] * max(0, q_idx[b,t,h,:] . k_idx[b, idx[b,t,s], :]).
+ * loss[b,t] = sum_s target[s] * (log target[s] - log softmax(I)[s]) over the
+ * valid slots with target > 0; dI = softmax(I) * sum(target) - target ("Add
+ * unfused SBHD compressed sparse attention", review of the teacher
+ * normalization: a row without mass gets no gradient).  With
+ * G[h,s] = dI[s] w[h] [q_idx[h] . k_idx[j_s] > 0]:
+ *   dq_idx[b,t,h,:] = sum_s G[h,s] k_idx[j_s]
+ *   dw[b,t,h]       = sum_s dI[s] max(0, q_idx[h] . k_idx[j_s])
+ *   dk_idx[b,j,:]  += sum over (t, s with j_s = j) sum_h G[h,s] q_idx[b,t,h]
+ * All outputs fp32; dk_idx is zeroed by the call and accumulated with fp32
+ * atomics (reproducible to rounding only).  target is usually the output of
+ * csa_indexer_teacher for the same idx.
+ *
+ *   q_idx [b,sq,H_I,d_I] dt  k_idx [b,n_c,d_I] dt  w [b,sq,H_I] fp32
+ *   idx [b,sq,K] int32  target [b,sq,K] fp32
+ *   loss out [b,sq]  dq_idx out [b,sq,H_I,d_I]  dk_idx out [b,n_c,d_I]
+ *   dw out [b,sq,H_I]
+ * Errors: INVALID_ARG (null/misaligned pointers, d_I % 8, K < 1,
+ * n_c != sq / ratio); UNSUPPORTED (d_I > 256, H_I > 64, K too large).
+ */
+csa_status_t csa_indexer_loss(const void* q_idx, const void* k_idx, const float* w,
+                              const int32_t* idx, const float* target, float* loss,
+                              float* dq_idx, float* dk_idx, float* dw, int b, int sq, int n_c,
+                              int H_I, int d_I, int ratio, int K, csa_dtype_t dt,
+                              csa_stream_t stream);
+
+/*
  * Read and clear the device status word of the current device after the
  * work on `stream` has finished (this call synchronizes `stream`).
  * *status_out receives CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_CHECK (the

@@ -100,6 +100,16 @@ def test_invalid_arguments_rejected_on_host(lib):
                             0, 1, None) == INVALID
     assert lib.csa_indexer_topk(fake, fake, fake, fake + 4, fake, None, 1, 512, 128, 4, 64, 4, 16,
                                 1, fake, 1 << 30, None) == INVALID
+    # teacher: null lse; head dim not a multiple of 8
+    assert lib.csa_indexer_teacher(fake, fake, fake, None, 0.1, fake, 1, 8, 2, 64, 2, 4, 4, 1,
+                                   None) == INVALID
+    assert lib.csa_indexer_teacher(fake, fake, fake, fake, 0.1, fake, 1, 8, 2, 60, 2, 4, 4, 1,
+                                   None) == INVALID
+    # loss: null gradient output; d_I beyond the supported maximum
+    assert lib.csa_indexer_loss(fake, fake, fake, fake, fake, fake, fake, None, fake, 1, 8, 2, 4,
+                                64, 4, 4, 1, None) == INVALID
+    assert lib.csa_indexer_loss(fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 8, 2, 4,
+                                512, 4, 4, 1, None) == UNSUPPORTED
     # device status needs an output pointer
     assert lib.csa_get_device_status(None, None, None) == INVALID
 
