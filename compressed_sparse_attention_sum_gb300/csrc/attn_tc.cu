@@ -145,13 +145,17 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
       if (!ok) { site = kSiteFwdO; break; }
     }
     const int sbase = it * kSlots;
-    // gather KV rows of slots [sbase, sbase+128) into the swizzled tile
+    // gather KV rows of slots [sbase, sbase+128) into the swizzled tile; the
+    // padding slots past the union are zero-filled rather than all reading
+    // one row (which would pile every CTA's requests onto one L2 line)
     for (int c = tid; c < kSlots * 16; c += kThreads) {
       const int rr = c >> 4, ch = c & 15;
       const int s = sbase + rr;
-      int row = 0;
-      if (s < nwin) row = win0 + s;
-      else if (s < S_total) row = sq + ulist[s - nwin];
+      if (s >= S_total) {
+        *reinterpret_cast<uint4*>(sm + Layout::KV + sw_off(rr, ch)) = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const int row = s < nwin ? win0 + s : sq + ulist[s - nwin];
       cp_async_16(sm + Layout::KV + sw_off(rr, ch), kv_b + (long long)row * kD + ch * 8);
     }
     // per-query logit bias of the tile's slots: 0, log2(multiplicity) or -inf

@@ -161,6 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     unsigned char* dst = sm + Layout::KV + (it & 1) * 2 * kBlk;
     for (int c = tid; c < kSlots * 16; c += kThreads) {
       const int rr = c >> 4, ch = c & 15;
+      if (sbase + rr >= S_total) {       // padding: zeros, not a shared hot row
+        *reinterpret_cast<uint4*>(dst + sw_off(rr, ch)) = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
       cp_async_16(dst + sw_off(rr, ch), kv_b + (long long)slot_row(sbase + rr) * kD + ch * 8);
     }
     cp_async_commit_();

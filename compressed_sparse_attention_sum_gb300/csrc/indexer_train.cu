@@ -35,6 +35,16 @@ namespace {
 constexpr int kTrChunk = 64;     // selected slots per shared-memory chunk
 constexpr int kTrThreads = 128;  // 4 warps; warp w owns slots 16w..16w+15 of a chunk
 
+// First slot of the ci-th chunk a CTA visits.  Index rows are sorted, so
+// neighbouring queries select mostly the same blocks in the same order; CTAs
+// start at different chunks (rotated by the query index) so that the ones
+// running together do not all read the same few rows, which would pile the
+// requests onto one L2 slice.
+__device__ __forceinline__ int chunk_start(int ci, int K) {
+  const int n = (K + kTrChunk - 1) / kTrChunk;
+  return ((ci + (int)blockIdx.x) % n) * kTrChunk;
+}
+
 __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = is_max ? warp_max(v) : warp_sum(v);
@@ -46,16 +56,19 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
   return r;
 }
 
-// Gather rows `rows[c0 + r]` (or row 0 for invalid slots) of a [*, D] bf16
-// matrix into a [64][LD] shared tile with 16-byte copies.
+// Gather rows `rows[c0 + r]` of a [*, D] bf16 matrix into a [64][LD] shared
+// tile with 16-byte copies; invalid slots get zero rows (their results are
+// dropped, and zeros keep the products finite).
 template <int D, int LD>
 __device__ __forceinline__ void gather_rows(__nv_bfloat16* dst, const __nv_bfloat16* src,
                                             const int* rows, int c0, int K) {
   for (int e = threadIdx.x; e < kTrChunk * (D / 8); e += kTrThreads) {
     const int r = e / (D / 8), c8 = e % (D / 8);
     const int s = c0 + r;
-    const int row = (s < K && rows[s] >= 0) ? rows[s] : 0;
-    cp_async16(dst + r * LD + c8 * 8, src + (long long)row * D + c8 * 8);
+    if (s < K && rows[s] >= 0)
+      cp_async16(dst + r * LD + c8 * 8, src + (long long)rows[s] * D + c8 * 8);
+    else
+      *reinterpret_cast<uint4*>(dst + r * LD + c8 * 8) = make_uint4(0u, 0u, 0u, 0u);
   }
   cp_async_commit();
   cp_async_wait_all();
@@ -127,7 +140,10 @@ __global__ void __launch_bounds__(kTrThreads) teacher_mma_kernel(
   __syncthreads();
   const float sc2 = scale * kLog2e;
   const __nv_bfloat16* kv_b = kv + (long long)bi * (sq + n_c) * D;
-  for (int c0 = 0; c0 < K; c0 += kTrChunk) {
+  for (int ci = 0; ci * kTrChunk < K; ++ci) {
+    const int c0 = chunk_start(ci, K);
+    // a chunk without valid slots (the -1 tail of a short row) is skipped
+    if (!__syncthreads_or(tid < kTrChunk && c0 + tid < K && rows[c0 + tid] >= 0)) continue;
     gather_rows<D, LD>(Ks, kv_b, rows, c0, K);
     __syncthreads();
     float acc[MT][2][4];
@@ -317,7 +333,9 @@ __global__ void __launch_bounds__(kTrThreads) student_mma_kernel(
   const __nv_bfloat16* k_b = k_I + (long long)bi * n_c * DI;
 
   // ---- pass A: student scores of the selected slots ------------------------
-  for (int c0 = 0; c0 < K; c0 += kTrChunk) {
+  for (int ci = 0; ci * kTrChunk < K; ++ci) {
+    const int c0 = chunk_start(ci, K);
+    if (!__syncthreads_or(tid < kTrChunk && c0 + tid < K && blk[c0 + tid] >= 0)) continue;
     gather_rows<DI, LD>(Ks, k_b, blk, c0, K);
     __syncthreads();
     float acc[MT][2][4];
@@ -357,7 +375,9 @@ __global__ void __launch_bounds__(kTrThreads) student_mma_kernel(
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) dwl[mt][0] = dwl[mt][1] = 0.f;
   float* dk_b = dk_I + (long long)bi * n_c * DI;
-  for (int c0 = 0; c0 < K; c0 += kTrChunk) {
+  for (int ci = 0; ci * kTrChunk < K; ++ci) {
+    const int c0 = chunk_start(ci, K);
+    if (!__syncthreads_or(tid < kTrChunk && c0 + tid < K && blk[c0 + tid] >= 0)) continue;
     gather_rows<DI, LD>(Ks, k_b, blk, c0, K);
     __syncthreads();
     {
