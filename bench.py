@@ -327,54 +327,58 @@ def run_gpu(args, rank, world, local_rank):
     queries = b * sq
     value = world * queries / (ms_max / 1e3)
 
-    # ---- variant: the same layer holding 4 packed documents -------------------
-    # (window and indexer restricted to each query's document; same timing rules)
-    doc = packed_doc_ids(b, sq, cfg.ratio, 4, seed=rank).to(dev)
-    for _ in range(args.warmup):
-        flush.zero_()
-        step(d_in, doc)
-    evs_doc = []
-    for _ in range(args.steps):
-        flush.zero_()
-        evs_doc.append(step(d_in, doc))
-    torch.cuda.synchronize()
-    # ---- the indexer's training path on the same layer ---------------------------
-    # teacher target from the forward's LSE, then the student's KL loss and
-    # gradients over the selected entries (L2 flushed before each pair)
-    target = torch.empty(b, sq, cfg.K, dtype=torch.float32, device=dev)
-    step(d_in)
-    tr_ev = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        e3 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e3[0].record(stream)
-        csa.csa_indexer_teacher(d_in["q"], kv_full, idx, L, cfg.scale, cfg.ratio, out=target)
-        e3[1].record(stream)
-        csa.csa_indexer_loss(d_in["q_I"], d_in["k_I"], d_in["w"], idx, target, cfg.ratio)
-        e3[2].record(stream)
-        if i >= args.warmup:
-            tr_ev.append(e3)
-    torch.cuda.synchronize()
-    t_teach = sum(e[0].elapsed_time(e[1]) for e in tr_ev) / len(tr_ev)
-    t_loss = sum(e[1].elapsed_time(e[2]) for e in tr_ev) / len(tr_ev)
-    slots_sel = int((idx >= 0).sum().item())
-    variant_train = {
-        "workload": f"{cfg.name}: indexer distillation over the top-{cfg.K} entries",
-        "teacher_ms": round(t_teach, 4), "loss_ms": round(t_loss, 4),
-        "teacher_tflops": round(2.0 * H * d * slots_sel / (t_teach / 1e3) / 1e12, 2),
-        "loss_tflops": round(3 * 2.0 * cfg.H_I * cfg.d_I * slots_sel / (t_loss / 1e3) / 1e12, 2),
-        "kernels": "warp-level MMA (mma.sync), one CTA per query",
-    }
+    # ---- variants (skipped with --no-variants) ----------------------------------
+    variants = {}
     names = ("compress", "indexer_topk", "attn_fwd", "attn_bwd", "compress_bwd")
-    doc_ms = max_over_ranks(sum(e[0].elapsed_time(e[5]) for e in evs_doc) / len(evs_doc), world,
-                            dev)
-    variant_docs = {
-        "workload": f"{cfg.name} with 4 packed documents (boundaries on multiples of the ratio)",
-        "ms_per_step": round(doc_ms, 4), "value": round(world * queries / (doc_ms / 1e3), 1),
-        "unit": "queries/s",
-        "kernels_ms": {n: round(sum(e[i].elapsed_time(e[i + 1]) for e in evs_doc) / len(evs_doc), 4)
-                       for i, n in enumerate(names)},
-    }
+    if not args.no_variants:
+        # the same layer holding 4 packed documents (window and indexer restricted
+        # to each query's document; same timing rules)
+        doc = packed_doc_ids(b, sq, cfg.ratio, 4, seed=rank).to(dev)
+        for _ in range(args.warmup):
+            flush.zero_()
+            step(d_in, doc)
+        evs_doc = []
+        for _ in range(args.steps):
+            flush.zero_()
+            evs_doc.append(step(d_in, doc))
+        torch.cuda.synchronize()
+        doc_ms = max_over_ranks(sum(e[0].elapsed_time(e[5]) for e in evs_doc) / len(evs_doc),
+                                world, dev)
+        variants["docs4"] = {
+            "workload": f"{cfg.name} with 4 packed documents (boundaries on multiples of the ratio)",
+            "ms_per_step": round(doc_ms, 4), "value": round(world * queries / (doc_ms / 1e3), 1),
+            "unit": "queries/s",
+            "kernels_ms": {n: round(sum(e[i].elapsed_time(e[i + 1]) for e in evs_doc) / len(evs_doc),
+                                    4) for i, n in enumerate(names)},
+        }
+        # the indexer's training path on the same layer: teacher target from the
+        # forward's LSE, then the student's KL loss and gradients over the
+        # selected entries (L2 flushed before each pair)
+        target = torch.empty(b, sq, cfg.K, dtype=torch.float32, device=dev)
+        step(d_in)
+        tr_ev = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e3 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e3[0].record(stream)
+            csa.csa_indexer_teacher(d_in["q"], kv_full, idx, L, cfg.scale, cfg.ratio, out=target)
+            e3[1].record(stream)
+            csa.csa_indexer_loss(d_in["q_I"], d_in["k_I"], d_in["w"], idx, target, cfg.ratio)
+            e3[2].record(stream)
+            if i >= args.warmup:
+                tr_ev.append(e3)
+        torch.cuda.synchronize()
+        t_teach = sum(e[0].elapsed_time(e[1]) for e in tr_ev) / len(tr_ev)
+        t_loss = sum(e[1].elapsed_time(e[2]) for e in tr_ev) / len(tr_ev)
+        slots_sel = int((idx >= 0).sum().item())
+        variants["indexer_training"] = {
+            "workload": f"{cfg.name}: indexer distillation over the top-{cfg.K} entries",
+            "teacher_ms": round(t_teach, 4), "loss_ms": round(t_loss, 4),
+            "teacher_tflops": round(2.0 * H * d * slots_sel / (t_teach / 1e3) / 1e12, 2),
+            "loss_tflops": round(3 * 2.0 * cfg.H_I * cfg.d_I * slots_sel / (t_loss / 1e3) / 1e12,
+                                 2),
+            "kernels": "warp-level MMA (mma.sync), one CTA per query",
+        }
 
     # ---- end-to-end through host buffers -------------------------------------
     # Every step copies all of its inputs host -> device (pinned) and all of its
@@ -497,7 +501,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roofline,
         "kernels": kernels,
         "targets": targets,
-        "variants": {"docs4": variant_docs, "indexer_training": variant_train},
+        "variants": variants,
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
     }
@@ -565,6 +569,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=1024,
                     help="query rows per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the packed-documents and indexer-training timings")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
