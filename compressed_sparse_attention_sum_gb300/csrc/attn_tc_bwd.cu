@@ -399,8 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
         mma_bf16_ss(tmem + kColDQ, sw128_desc(ya + aoff), b, idesc_q, 1u);
       }
       mma_commit(bar_ds);
-      // S and dP of the next tile (S/dP were fully read above)
-      if (it + 1 < ntiles) issue_s_dp(it + 1);
     }
     ok = __syncthreads_and(mbar_wait(bar_ds, n_ds & 1));
     ++n_ds;
@@ -436,12 +434,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<float4*>(srow + ((c + lane) & 7) * 4) = ch[c];
       __syncthreads();
-      // one warp per staged row: its 32 lanes add the row's 512 B with one
-      // coalesced vector reduction (X|Y is free again once every thread has
-      // passed the next barrier)
+      // S and dP of the next tile (S/dP were fully read before the dS MMAs;
+      // its KV rows arrived before them): thread 0 issues them here, so that
+      // the issue, which blocks while the MMA queue drains, overlaps the
+      // reductions of the other warps instead of delaying everyone
+      if (tid == 0 && it + 1 < ntiles) {
+        fence_after();
+        issue_s_dp(it + 1);
+      }
+      // warps 1..15, one staged row each at a time: its 32 lanes add the
+      // row's 512 B with one coalesced vector reduction (X|Y is free again
+      // once every thread has passed the next barrier)
       const int nrow = min(kSlots, S_total - it * kSlots);
 #pragma unroll 4
-      for (int rr = warp; rr < nrow; rr += kThreads / 32) {
+      for (int rr = warp - 1; warp > 0 && rr < nrow; rr += kThreads / 32 - 1) {
         const float4 v4 = *reinterpret_cast<const float4*>(stg + rr * kD + lane * 4);
         red_add_v4(dkv_b + (long long)slot_row(it * kSlots + rr) * kD + lane * 4, v4.x, v4.y,
                    v4.z, v4.w);
