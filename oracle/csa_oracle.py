@@ -57,6 +57,7 @@ __all__ = [
     "query_slots", "attn_fwd_query", "attn_fwd", "attn_bwd_query", "attn_bwd",
     "selected_entries", "indexer_teacher_row", "indexer_teacher",
     "indexer_student_row", "indexer_kl_row", "indexer_loss",
+    "round_e4m3", "quantize_rows_e4m3", "indexer_scores_fp8",
 ]
 
 
@@ -475,3 +476,61 @@ def indexer_loss(q_I, k_I, w, idx, target, ratio: int):
             np.add.at(dk[bi], js, g.T @ q_I[bi, t])
             dw[bi, t] = np.maximum(dots, 0.0) @ dI[pos]
     return loss, dq, dk, dw
+
+
+# ---------------------------------------------------------------------------
+# FP8 indexer: q_I and k_I quantized per row to e4m3, scores from the codes
+# ---------------------------------------------------------------------------
+#
+# The pages list "indexer quantization" as not included ("Refactor Deepseek
+# v4 ...", model description); the quantization here is this repository's
+# reading: every q_I head row and every k_I row is scaled by 448 / absmax(row)
+# (448 = the largest finite e4m3 value), rounded to e4m3, and keeps the
+# scale absmax / 448.  Both quantities are computed in fp32 (the reciprocal
+# 448 / absmax, then x * reciprocal), so that both sides round the same fp32
+# value.  The scores use the dequantized rows:
+#   I[t, j] = sum_h w[t,h] * max(0, sq[t,h] sk[j] (q8[t,h] . k8[j]))
+#           = sk[j] * sum_h (w[t,h] sq[t,h]) max(0, q8[t,h] . k8[j])   (scales > 0)
+
+def round_e4m3(x):
+    """Round to the nearest e4m3 value (1 sign, 4 exponent bits with bias 7,
+    3 mantissa bits; no infinities), ties to even, saturating at +-448.
+    Normal numbers have 4 significant bits; below 2^-6 the grid is 2^-9."""
+    x = np.asarray(x, np.float64)
+    a = np.minimum(np.abs(x), 448.0)
+    _, e = np.frexp(a)                     # a = m 2^e, 0.5 <= m < 1
+    e = np.maximum(e, -5)                  # subnormal range shares the 2^-9 grid
+    step = np.ldexp(1.0, e - 4)
+    r = np.round(a / step) * step          # numpy rounds half to even
+    return np.sign(x) * np.minimum(r, 448.0)
+
+
+def quantize_rows_e4m3(x):
+    """Per-row (last axis) e4m3 codes (as float64 values) and fp32 scales."""
+    x32 = np.asarray(x, np.float32)
+    amax = np.abs(x32).max(axis=-1)
+    inv = np.where(amax > 0, np.float32(448.0) / np.where(amax > 0, amax, 1), 0).astype(np.float32)
+    y = (x32 * inv[..., None]).astype(np.float32)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    return round_e4m3(y.astype(np.float64)), scale
+
+
+def indexer_scores_fp8(q8, q_scale, k8, k_scale, w, ratio: int, doc_ids=None):
+    """Indexer scores [b, sq, n_c] from e4m3 codes and scales; entries a query
+    may not select are -inf (as indexer_scores)."""
+    q8 = np.asarray(q8, np.float64)
+    k8 = np.asarray(k8, np.float64)
+    b, sq, H_I, _ = q8.shape
+    n_c = k8.shape[1]
+    out = np.full((b, sq, n_c), -np.inf)
+    for bi in range(b):
+        for t in range(sq):
+            v = min(visible_blocks(t, ratio), n_c)
+            if v == 0:
+                continue
+            dots = q8[bi, t] @ k8[bi, :v].T                                # [H_I, v]
+            wq = np.asarray(w[bi, t], np.float64) * np.asarray(q_scale[bi, t], np.float64)
+            out[bi, t, :v] = np.asarray(k_scale[bi, :v], np.float64) * (wq @ np.maximum(dots, 0.0))
+            if doc_ids is not None:
+                out[bi, t, ~indexer_selectable(t, n_c, ratio, doc_ids[bi])] = -np.inf
+    return out

@@ -636,3 +636,54 @@ def test_indexer_loss_zero_target_row_has_zero_gradient():
     p = np.exp(I - I.max()) / np.exp(I - I.max()).sum()
     l, dI = orc.indexer_kl_row(I, p)
     assert abs(l) < 1e-14 and np.abs(dI).max() < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) indexer
+# ---------------------------------------------------------------------------
+
+def test_round_e4m3_matches_torch_float8():
+    """torch's float8_e4m3fn conversion (round to nearest even) on values
+    inside the finite range, including ties and subnormals."""
+    rng = np.random.default_rng(61)
+    vals = np.concatenate([
+        rng.standard_normal(4000) * 50,
+        rng.uniform(-2.0 ** -6, 2.0 ** -6, 1000),                  # subnormal range
+        np.array([0.0, 1.0625, 1.1875, 232.0, 448.0, -448.0, 2.0 ** -10, 3 * 2.0 ** -10]),
+    ])
+    vals = np.clip(vals, -448.0, 448.0).astype(np.float32)
+    ref = torch.from_numpy(vals).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(orc.round_e4m3(vals.astype(np.float64)), ref)
+
+
+def test_quantize_rows_e4m3_properties():
+    rng = np.random.default_rng(62)
+    x = (rng.standard_normal((50, 128)) * rng.uniform(0.01, 100, (50, 1))).astype(np.float32)
+    x[3] = 0.0
+    q, sc = orc.quantize_rows_e4m3(x)
+    amax_pos = np.abs(x).argmax(axis=1)
+    for i in range(50):
+        if i == 3:
+            assert sc[i] == 0 and np.all(q[i] == 0)
+            continue
+        assert abs(q[i, amax_pos[i]]) == 448.0                 # the largest entry maps to 448
+        # every code is an e4m3 value within half an e4m3 step of x * 448 / amax
+        y = x[i].astype(np.float64) * 448.0 / np.abs(x[i]).max()
+        assert np.all(np.abs(q[i] - y) <= np.maximum(np.abs(y) * 2.0 ** -4, 2.0 ** -10) + 1e-4)
+        np.testing.assert_array_equal(q[i], orc.round_e4m3(q[i]))
+
+
+def test_indexer_scores_fp8_reduce_to_plain_scores():
+    """With rows already on the e4m3 grid and unit scales, the fp8 scores are
+    the plain indexer scores; scales factor out of the ReLU."""
+    rng = np.random.default_rng(63)
+    b, sq, H, d, r = 1, 24, 3, 16, 4
+    q = orc.round_e4m3(rng.integers(-6, 7, (b, sq, H, d)).astype(np.float64))
+    k = orc.round_e4m3(rng.integers(-6, 7, (b, sq // r, d)).astype(np.float64))
+    w = rng.standard_normal((b, sq, H))
+    ones_q, ones_k = np.ones((b, sq, H)), np.ones((b, sq // r))
+    np.testing.assert_allclose(orc.indexer_scores_fp8(q, ones_q, k, ones_k, w, r),
+                               orc.indexer_scores(q, k, w, r), atol=1e-12)
+    sq_s, sk_s = rng.uniform(0.5, 2, (b, sq, H)), rng.uniform(0.5, 2, (b, sq // r))
+    ref = orc.indexer_scores(q * sq_s[..., None], k * sk_s[..., None], w, r)
+    np.testing.assert_allclose(orc.indexer_scores_fp8(q, sq_s, k, sk_s, w, r), ref, atol=1e-9)
