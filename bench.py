@@ -379,6 +379,39 @@ def run_gpu(args, rank, world, local_rank):
                                  2),
             "kernels": "warp-level MMA (mma.sync), one CTA per query",
         }
+        # the FP8 indexer: per-row e4m3 quantization of q_I and k_I, then the
+        # indexer top-k on the codes (tcgen05 kind::f8f6f4); the overlap is the
+        # mean fraction of the bf16 top-k that the FP8 top-k keeps
+        q8, qs = csa.csa_quantize_e4m3(d_in["q_I"])
+        k8, ks = csa.csa_quantize_e4m3(d_in["k_I"])
+        idx8 = torch.empty_like(idx)
+        f8_ev = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e3 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e3[0].record(stream)
+            csa.csa_quantize_e4m3(d_in["q_I"], codes=q8, scale=qs)
+            csa.csa_quantize_e4m3(d_in["k_I"], codes=k8, scale=ks)
+            e3[1].record(stream)
+            csa.csa_indexer_topk_fp8(q8, qs, k8, ks, d_in["w"], cfg.topk, cfg.ratio, workspace=ws,
+                                     out_idx=idx8)
+            e3[2].record(stream)
+            if i >= args.warmup:
+                f8_ev.append(e3)
+        torch.cuda.synchronize()
+        t_q = sum(e[0].elapsed_time(e[1]) for e in f8_ev) / len(f8_ev)
+        t_i8 = sum(e[1].elapsed_time(e[2]) for e in f8_ev) / len(f8_ev)
+        hit = torch.zeros(b, sq, n_c + 1, dtype=torch.int32, device=dev)
+        hit.scatter_(2, torch.where(idx >= 0, idx, n_c).long(), 1)
+        hit[:, :, n_c] = 0
+        kept = torch.gather(hit, 2, torch.where(idx8 >= 0, idx8, n_c).long()).sum().item()
+        variants["indexer_fp8"] = {
+            "workload": f"{cfg.name}: indexer top-{cfg.K} on per-row e4m3 codes of q_I and k_I",
+            "quantize_ms": round(t_q, 4), "indexer_topk_ms": round(t_i8, 4),
+            "indexer_topk_bf16_ms": round(sum(seg[1]) / len(seg[1]), 4),
+            "topk_overlap_with_bf16": round(kept / max(1, int((idx >= 0).sum().item())), 5),
+            "kernels": "quantize: warp per row; scores: tcgen05 kind::f8f6f4, same select",
+        }
 
     # ---- end-to-end through host buffers -------------------------------------
     # Every step copies all of its inputs host -> device (pinned) and all of its

@@ -40,6 +40,8 @@ SIGNATURES = {
                          + [_c_int, _c_p, _c_sz, _c_p]),
     "csa_indexer_topk_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
                                  + [_c_int, _c_p]),
+    "csa_quantize_e4m3": (_c_int, [_c_p, _c_ll, _c_int, _c_int, _c_p, _c_p, _c_p]),
+    "csa_indexer_topk_fp8": (_c_int, [_c_p] * 8 + [_c_int] * 7 + [_c_p, _c_sz, _c_p]),
     "csa_attn_fwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p] + [_c_int] * 8
                      + [_c_int, _c_p]),
     "csa_attn_bwd": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p, _c_p,
@@ -203,6 +205,69 @@ def csa_indexer_topk(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, topk
         _ptr(out_score), b, sq,
         n_c, H_I, d_I, ratio, topk, _dt(q_I), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    if out_score is not None:
+        return out_idx, out_score
+    return out_idx
+
+
+def csa_quantize_e4m3(x: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                      scale: Optional[torch.Tensor] = None, stream=None
+                      ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-row (last axis) e4m3 quantization of a bf16 / fp32 tensor.
+
+    Returns codes (uint8 e4m3 bit patterns, x's shape) and scale (fp32,
+    x.shape[:-1]) with x ~= e4m3(codes) * scale[..., None]."""
+    lib = load_library()
+    _need(x, "x")
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    _need(codes, "codes", dtype=torch.uint8)
+    _need(scale, "scale", dtype=torch.float32)
+    _check("csa_quantize_e4m3", lib.csa_quantize_e4m3(
+        x.data_ptr(), rows, d, _dt(x), codes.data_ptr(), scale.data_ptr(), _stream(stream)))
+    return codes, scale
+
+
+def csa_indexer_topk_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tensor,
+                         k_scale: torch.Tensor, w: torch.Tensor, topk: int, ratio: int,
+                         workspace: Optional[torch.Tensor] = None,
+                         out_idx: Optional[torch.Tensor] = None,
+                         out_score: Optional[torch.Tensor] = None, return_scores: bool = False,
+                         stream=None, doc_ids: Optional[torch.Tensor] = None):
+    """csa_indexer_topk on e4m3 codes: q8 [b, sq, H_I, d_I] and k8 [b, n_c, d_I]
+    uint8 with fp32 per-row scales q_scale [b, sq, H_I], k_scale [b, n_c]
+    (csa_quantize_e4m3); other arguments and the outputs as csa_indexer_topk."""
+    lib = load_library()
+    _need(q8, "q8", dtype=torch.uint8)
+    _need(k8, "k8", dtype=torch.uint8)
+    _need(q_scale, "q_scale", dtype=torch.float32)
+    _need(k_scale, "k_scale", dtype=torch.float32)
+    _need(w, "w", dtype=torch.float32)
+    b, sq, H_I, d_I = q8.shape
+    n_c = k8.shape[1]
+    K = min(topk, n_c)
+    dev = q8.device
+    if workspace is None:
+        nbytes = csa_indexer_topk_workspace_size(b, sq, n_c, H_I, d_I, topk)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace")
+    if out_idx is None:
+        out_idx = torch.empty(b, sq, K, dtype=torch.int32, device=dev)
+    _need(out_idx, "out_idx", dtype=torch.int32)
+    if out_score is None and return_scores:
+        out_score = torch.empty(b, sq, K, dtype=torch.float32, device=dev)
+    if out_score is not None:
+        _need(out_score, "out_score", dtype=torch.float32)
+    if doc_ids is not None:
+        _need(doc_ids, "doc_ids", dtype=torch.int32)
+    _check("csa_indexer_topk_fp8", lib.csa_indexer_topk_fp8(
+        q8.data_ptr(), q_scale.data_ptr(), k8.data_ptr(), k_scale.data_ptr(), w.data_ptr(),
+        _ptr(doc_ids), out_idx.data_ptr(), _ptr(out_score), b, sq, n_c, H_I, d_I, ratio, topk,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))
     if out_score is not None:
         return out_idx, out_score
     return out_idx

@@ -18,6 +18,18 @@ bool indexer_tc_supported(int H_I, int d_I);
 cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
                                      float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
                                      int d_I, int ratio, int* status, cudaStream_t s);
+bool indexer_tc_fp8_supported(int H_I, int d_I);
+cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
+                                     float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
+                                     int d_I, int ratio, int* status, cudaStream_t s,
+                                     const float* q_scale, const float* k_scale);
+cudaError_t launch_indexer_scores_simt_fp8(const uint8_t* q8, const float* q_scale,
+                                           const uint8_t* k8, const float* k_scale,
+                                           const float* w, float* ws, int t0, int nt, int b,
+                                           int sq, int n_c, int H_I, int d_I, int ratio,
+                                           cudaStream_t s);
+cudaError_t launch_quantize_e4m3(const void* x, long long rows, int d, bool bf16, uint8_t* out,
+                                 float* scale, cudaStream_t s);
 bool attn_mma_supported(int H, int d, int window, int K);
 bool attn_tc_supported(int H, int d, int n_c, int K);
 bool attn_tc_bwd_supported(int H, int d, int n_c, int K);
@@ -252,6 +264,61 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
     else
       e = csa::launch_indexer_scores_simt(q_idx, k_idx, w, (float*)workspace, t0, nt, b, sq, n_c,
                                           H_I, d_I, ratio, dt == CSA_BF16, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+    e = csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq, n_c,
+                                ratio, K, s, doc_ids);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  return CSA_OK;
+}
+
+csa_status_t csa_quantize_e4m3(const void* x, long long rows, int d, csa_dtype_t dt,
+                               uint8_t* codes, float* scale, csa_stream_t stream) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (rows < 0 || d < 8 || d % 8 != 0) return CSA_ERR_INVALID_ARG;
+  if (rows == 0) return CSA_OK;
+  if (x == nullptr || codes == nullptr || scale == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scale)) return CSA_ERR_INVALID_ARG;
+  if (rows > (1ll << 33)) return CSA_ERR_UNSUPPORTED;   // grid of rows / 8 CTAs
+  return from_cuda(csa::launch_quantize_e4m3(x, rows, d, dt == CSA_BF16, codes, scale,
+                                             (cudaStream_t)stream));
+}
+
+csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const uint8_t* k8,
+                                  const float* k_scale, const float* w, const int32_t* doc_ids,
+                                  int32_t* topk_idx, float* topk_score, int b, int sq, int n_c,
+                                  int H_I, int d_I, int ratio, int topk, void* workspace,
+                                  size_t workspace_bytes, csa_stream_t stream) {
+  if (q8 == nullptr || q_scale == nullptr || k8 == nullptr || k_scale == nullptr ||
+      w == nullptr || topk_idx == nullptr || workspace == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(q_scale) || !aligned16(k8) || !aligned16(k_scale) ||
+      !aligned16(w) || !aligned16(topk_idx) || !aligned16(topk_score) ||
+      !aligned16(workspace) || !aligned16(doc_ids))
+    return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || H_I < 1 || d_I < 16 || d_I % 16 != 0 || ratio < 1 || topk < 1)
+    return CSA_ERR_INVALID_ARG;
+  if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
+  if (d_I > kMaxDI || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
+  const size_t row_bytes = (size_t)b * n_c * sizeof(float);
+  if (workspace_bytes < csa_indexer_topk_min_workspace(b, n_c)) return CSA_ERR_WORKSPACE;
+  const int K = topk < n_c ? topk : n_c;
+  cudaStream_t s = (cudaStream_t)stream;
+  size_t rows = workspace_bytes / row_bytes;
+  rows = rows / kIndexerTileRows * kIndexerTileRows;
+  if (rows > (size_t)sq) rows = (size_t)sq;
+  const char* cc = getenv("CSA_INDEXER_CUDA_CORES");
+  const bool use_tc = !(cc && cc[0] == '1') && csa::indexer_tc_fp8_supported(H_I, d_I);
+  int* status = device_status_ptr();
+  for (int t0 = 0; t0 < sq; t0 += (int)rows) {
+    const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;
+    cudaError_t e;
+    if (use_tc)
+      e = csa::launch_indexer_scores_tc(q8, k8, w, (float*)workspace, t0, nt, b, sq, n_c, H_I,
+                                        d_I, ratio, status, s, q_scale, k_scale);
+    else
+      e = csa::launch_indexer_scores_simt_fp8(q8, q_scale, k8, k_scale, w, (float*)workspace, t0,
+                                              nt, b, sq, n_c, H_I, d_I, ratio, s);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
     e = csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq, n_c,
                                 ratio, K, s, doc_ids);

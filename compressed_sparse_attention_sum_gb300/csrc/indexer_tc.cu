@@ -23,6 +23,12 @@
 //               lane quarter and one half of the 128 columns
 // Every mbarrier wait is bounded; a wait that gives up records
 // CSA_ERR_TIMEOUT in the device status word and the CTA skips to teardown.
+//
+// The FP8 variant (F8) takes e4m3 codes of q_I and k_I with per-row scales
+// (csa_quantize_e4m3): rows of 128 bytes hold 128 codes, each MMA is
+// kind::f8f6f4 with K = 32 (the same 32-byte step along a row), and since the
+// scales are positive they leave the ReLU:
+//   I[t,j] = sk[j] * sum_h (w[t,h] sq[t,h]) max(0, q8[t,h] . k8[j]).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,13 +49,15 @@ constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kMaxHeads = 64;
 constexpr uint32_t kTmemCols = 256;
-template <int DI>
+template <int DI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const float* __restrict__ w, float* __restrict__ ws, int t0, int nt, int sq, int n_c,
-    int H_I, int ratio, int* __restrict__ status) {
-  constexpr int KB = DI / 64;                        // 64-wide K blocks
-  constexpr uint32_t kTileBytes = KB * kTileM * 128;  // one operand tile (128 rows x DI bf16)
+    int H_I, int ratio, int* __restrict__ status, const float* __restrict__ q_scale,
+    const float* __restrict__ k_scale) {
+  constexpr int EPB = F8 ? 128 : 64;                  // elements per 128-byte row block
+  constexpr int KB = DI / EPB;                        // 128-byte K blocks
+  constexpr uint32_t kTileBytes = KB * kTileM * 128;  // one operand tile (128 rows x DI)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
     if (lane == 0) {
       mbar_expect_tx(b_full, kTileBytes);
       for (int kb = 0; kb < KB; ++kb)
-        tma_load_2d(sB + kb * kTileM * 128, &tmap_k, b_full, kb * 64, bi * n_c + j0);
+        tma_load_2d(sB + kb * kTileM * 128, &tmap_k, b_full, kb * EPB, bi * n_c + j0);
       for (int h = 0; h < H_I; ++h) {
         const int s = h % kStages;
         const uint32_t par = ((h / kStages) & 1) ^ 1;
@@ -114,14 +122,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
         mbar_expect_tx(&full[s], kTileBytes);
         unsigned char* dst = sA + s * kTileBytes;
         for (int kb = 0; kb < KB; ++kb)
-          tma_load_3d(dst + kb * kTileM * 128, &tmap_q, &full[s], kb * 64, h,
+          tma_load_3d(dst + kb * kTileM * 128, &tmap_q, &full[s], kb * EPB, h,
                       bi * sq + tq0);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN);
+      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(kTileM, kTileN) : idesc_bf16_f32(kTileM, kTileN);
       bool ok = mbar_wait(b_full, 0);
       const uint32_t b_base = smem_addr(sB);
       for (int h = 0; ok && h < H_I; ++h) {
@@ -136,10 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
         const uint32_t a_base = smem_addr(sA + s * kTileBytes);
         const uint32_t d_tmem = tmem_base + a * kTileN;
 #pragma unroll
-        for (int k = 0; k < DI / 16; ++k) {
+        for (int k = 0; k < KB * 4; ++k) {              // 32-byte K steps
           const uint32_t off = (k / 4) * kTileM * 128 + (k % 4) * 32;
-          mma_bf16_ss(d_tmem, sw128_desc(a_base + off), sw128_desc(b_base + off), idesc,
+          if constexpr (F8)
+            mma_f8_ss(d_tmem, sw128_desc(a_base + off), sw128_desc(b_base + off), idesc,
                       k > 0 ? 1u : 0u);
+          else
+            mma_bf16_ss(d_tmem, sw128_desc(a_base + off), sw128_desc(b_base + off), idesc,
+                        k > 0 ? 1u : 0u);
         }
         mma_commit(&empty[s]);
         mma_commit(&acc_full[a]);
@@ -176,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[a]);
-      const float wv = __ldg(wrow + h);
+      float wv = __ldg(wrow + h);
+      if constexpr (F8) wv *= __ldg(q_scale + ((long long)bi * sq + tw) * H_I + h);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         acc[c] = fmaf(wv, fmaxf(__uint_as_float(v0[c]), 0.f), acc[c]);
@@ -192,6 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
       const int vis = min((t + 1) / ratio, n_c);
       const int jb = j0 + half * 64;
       float* dst = ws + ((long long)bi * nt + (t - t0)) * n_c + jb;
+      if constexpr (F8) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          acc[c] *= jb + c < n_c ? __ldg(k_scale + (long long)bi * n_c + jb + c) : 0.f;
+      }
       if (jb + 64 <= vis && (n_c & 3) == 0) {
 #pragma unroll
         for (int c = 0; c < 64; c += 4)
@@ -234,24 +252,31 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 bool indexer_tc_supported(int H_I, int d_I) {
   return (d_I == 64 || d_I == 128) && H_I >= 1 && H_I <= tc::kMaxHeads && get_encode() != nullptr;
 }
+bool indexer_tc_fp8_supported(int H_I, int d_I) {
+  return (d_I == 128 || d_I == 256) && H_I >= 1 && H_I <= tc::kMaxHeads && get_encode() != nullptr;
+}
 
-size_t indexer_tc_smem(int d_I) {
-  const size_t tile = (size_t)(d_I / 64) * tc::kTileM * 128;
+size_t indexer_tc_smem(int d_I, bool fp8 = false) {
+  const size_t tile = (size_t)(fp8 ? d_I / 128 : d_I / 64) * tc::kTileM * 128;
   return 1024 + tile * (1 + tc::kStages) + 16 * 8 + 16;
 }
 
 cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
                                      float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
-                                     int d_I, int ratio, int* status, cudaStream_t s) {
+                                     int d_I, int ratio, int* status, cudaStream_t s,
+                                     const float* q_scale, const float* k_scale) {
+  const bool f8 = q_scale != nullptr;     // e4m3 codes with per-row scales
+  const int eb = f8 ? 1 : 2, epb = f8 ? 128 : 64;
+  const CUtensorMapDataType dtp = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   auto encode = get_encode();
   if (encode == nullptr) return cudaErrorNotSupported;
   CUtensorMap tq, tk;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)d_I, (cuuint64_t)H_I, (cuuint64_t)b * sq};
-    const cuuint64_t strides[2] = {(cuuint64_t)d_I * 2, (cuuint64_t)H_I * d_I * 2};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)tc::kTileM};
+    const cuuint64_t strides[2] = {(cuuint64_t)d_I * eb, (cuuint64_t)H_I * d_I * eb};
+    const cuuint32_t box[3] = {(cuuint32_t)epb, 1, (cuuint32_t)tc::kTileM};
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q_idx), dims, strides,
+    if (encode(&tq, dtp, 3, const_cast<void*>(q_idx), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
@@ -259,30 +284,42 @@ cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const
   }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)d_I, (cuuint64_t)b * n_c};
-    const cuuint64_t strides[1] = {(cuuint64_t)d_I * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)tc::kTileN};
+    const cuuint64_t strides[1] = {(cuuint64_t)d_I * eb};
+    const cuuint32_t box[2] = {(cuuint32_t)epb, (cuuint32_t)tc::kTileN};
     const cuuint32_t estr[2] = {1, 1};
-    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k_idx), dims, strides,
+    if (encode(&tk, dtp, 2, const_cast<void*>(k_idx), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const size_t smem = indexer_tc_smem(d_I);
+  const size_t smem = indexer_tc_smem(d_I, f8);
   dim3 grid((unsigned)((n_c + tc::kTileN - 1) / tc::kTileN),
             (unsigned)((nt + tc::kTileM - 1) / tc::kTileM), (unsigned)b);
-  if (d_I == 128) {
-    auto k = tc::indexer_scores_tc_kernel<128>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, tc::kThreads, smem, s>>>(tq, tk, w, ws, t0, nt, sq, n_c, H_I, ratio, status);
-    count_launches(1);
-  } else {
-    auto k = tc::indexer_scores_tc_kernel<64>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<grid, tc::kThreads, smem, s>>>(tq, tk, w, ws, t0, nt, sq, n_c, H_I, ratio, status);
-    count_launches(1);
+#define CSA_IDX_TC(DD, FF)                                                                      \
+  {                                                                                             \
+    auto k = tc::indexer_scores_tc_kernel<DD, FF>;                                              \
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);           \
+    k<<<grid, tc::kThreads, smem, s>>>(tq, tk, w, ws, t0, nt, sq, n_c, H_I, ratio, status,    \
+                                       q_scale, k_scale);                                       \
+    count_launches(1);                                                                          \
   }
+  if (f8) {
+    if (d_I == 256) CSA_IDX_TC(256, true)
+    else CSA_IDX_TC(128, true)
+  } else {
+    if (d_I == 128) CSA_IDX_TC(128, false)
+    else CSA_IDX_TC(64, false)
+  }
+#undef CSA_IDX_TC
   return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
+                                     float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
+                                     int d_I, int ratio, int* status, cudaStream_t s) {
+  return launch_indexer_scores_tc(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I, d_I, ratio,
+                                  status, s, nullptr, nullptr);
 }
 
 }  // namespace csa

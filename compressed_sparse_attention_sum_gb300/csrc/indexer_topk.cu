@@ -14,14 +14,21 @@
 // chunk of query rows sit in a caller-provided fp32 workspace laid out
 // [b][chunk rows][n_c]; only the visible prefix of each row is written and
 // read, and a chunk is sized to stay resident in L2 between the two kernels.
+#include <cuda_fp8.h>
+
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 
 namespace csa {
 
+// e4m3 code -> its exact fp32 value
+__device__ __forceinline__ float to_f(__nv_fp8_e4m3 x) { return static_cast<float>(x); }
+
 // ----------------------------------------------------------------------------
 // CUDA-core score kernel: 64 query rows x 64 blocks per CTA, 256 threads,
-// 4x4 outputs per thread; loops over the indexer heads.
+// 4x4 outputs per thread; loops over the indexer heads.  With e4m3 codes
+// (T = __nv_fp8_e4m3) the per-row scales enter as w[t,h] * q_scale[t,h] and a
+// final factor k_scale[j] (both positive, so they commute with the ReLU).
 // ----------------------------------------------------------------------------
 constexpr int kSQ = 64;
 constexpr int kSK = 64;
@@ -29,7 +36,8 @@ constexpr int kSK = 64;
 template <typename T>
 __global__ void __launch_bounds__(256) indexer_scores_simt(
     const T* __restrict__ q_idx, const T* __restrict__ k_idx, const float* __restrict__ w,
-    float* __restrict__ ws, int t0, int nt, int sq, int n_c, int H_I, int d_I, int ratio) {
+    float* __restrict__ ws, int t0, int nt, int sq, int n_c, int H_I, int d_I, int ratio,
+    const float* __restrict__ q_scale, const float* __restrict__ k_scale) {
   extern __shared__ float sm[];
   float* q_s = sm;                    // [d_I][kSQ]
   float* k_s = sm + d_I * kSQ;        // [d_I][kSK]
@@ -66,7 +74,8 @@ __global__ void __launch_bounds__(256) indexer_scores_simt(
     }
     if (tid < kSQ) {
       const int t = tq0 + tid;
-      w_s[tid] = (t < tq_end) ? w[((long long)bi * sq + t) * H_I + h] : 0.f;
+      const long long wi = ((long long)bi * sq + t) * H_I + h;
+      w_s[tid] = (t < tq_end) ? (q_scale ? w[wi] * q_scale[wi] : w[wi]) : 0.f;
     }
     __syncthreads();
     float dot[4][4];
@@ -100,7 +109,7 @@ __global__ void __launch_bounds__(256) indexer_scores_simt(
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) {
       const int j = j0 + tx * 4 + cc;
-      if (j < vis) dst[j] = acc[a][cc];
+      if (j < vis) dst[j] = k_scale ? acc[a][cc] * k_scale[(long long)bi * n_c + j] : acc[a][cc];
     }
   }
 }
@@ -412,15 +421,30 @@ cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, con
     auto k = indexer_scores_simt<__nv_bfloat16>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, s>>>((const __nv_bfloat16*)q_idx, (const __nv_bfloat16*)k_idx, w, ws, t0,
-                              nt, sq, n_c, H_I, d_I, ratio);
+                              nt, sq, n_c, H_I, d_I, ratio, nullptr, nullptr);
     count_launches(1);
   } else {
     auto k = indexer_scores_simt<float>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     k<<<grid, 256, smem, s>>>((const float*)q_idx, (const float*)k_idx, w, ws, t0, nt, sq, n_c,
-                              H_I, d_I, ratio);
+                              H_I, d_I, ratio, nullptr, nullptr);
     count_launches(1);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_scores_simt_fp8(const uint8_t* q8, const float* q_scale,
+                                           const uint8_t* k8, const float* k_scale,
+                                           const float* w, float* ws, int t0, int nt, int b,
+                                           int sq, int n_c, int H_I, int d_I, int ratio,
+                                           cudaStream_t s) {
+  dim3 grid((unsigned)((n_c + kSK - 1) / kSK), (unsigned)((nt + kSQ - 1) / kSQ), (unsigned)b);
+  const size_t smem = (size_t)(d_I * (kSQ + kSK) + kSQ) * sizeof(float);
+  auto k = indexer_scores_simt<__nv_fp8_e4m3>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k<<<grid, 256, smem, s>>>((const __nv_fp8_e4m3*)q8, (const __nv_fp8_e4m3*)k8, w, ws, t0, nt,
+                            sq, n_c, H_I, d_I, ratio, q_scale, k_scale);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -101,6 +101,26 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t tmem_d, uint64_t a, uint64_
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | (0u << 7)                     // A format: e4m3
+         | (0u << 10)                    // B format: e4m3
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// D (+)= A B, 8-bit floating-point operands from shared memory (K = 32).
+__device__ __forceinline__ void mma_f8_ss(uint32_t tmem_d, uint64_t a, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -189,6 +189,60 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
                               csa_stream_t stream);
 
 /*
+ * csa_quantize_e4m3 - per-row e4m3 quantization, the input format of
+ * csa_indexer_topk_fp8.
+ *
+ * The pages name indexer quantization among the parts not yet included
+ * ("Refactor Deepseek v4 ...", the V4.1-Flash backbone's list of what is
+ * not included); this per-row rule is the library's own reading.  For each
+ * row r of x (the last axis, d elements):
+ *   amax     = max_c |x[r,c]|                     (fp32)
+ *   scale[r] = amax / 448                          (fp32, rounded once)
+ *   codes[r,c] = e4m3(x[r,c] * (448 / amax))       (fp32 reciprocal and
+ *                product, each rounded to nearest; then to nearest-even
+ *                e4m3, saturating at +-448; no NaN codes)
+ * An all-zero row gets scale 0 and zero codes.  Every step is a correctly
+ * rounded fp32 operation, so the result is reproducible bit for bit.
+ *
+ *   x      in   [rows, d] dt (bf16 or fp32), 16-byte aligned
+ *   codes  out  [rows, d] uint8 e4m3 bit patterns (OCP FP8 E4M3FN)
+ *   scale  out  [rows]    fp32
+ * For csa_indexer_topk_fp8, q_idx [b, sq, H_I, d_I] is quantized as
+ * rows = b*sq*H_I and k_idx [b, n_c, d_I] as rows = b*n_c.
+ * Errors: INVALID_ARG (null or misaligned pointers, d % 8 != 0, d < 8,
+ * rows < 0); UNSUPPORTED (rows > 2^33).  rows == 0 is a no-op.
+ */
+csa_status_t csa_quantize_e4m3(const void* x, long long rows, int d, csa_dtype_t dt,
+                               uint8_t* codes, float* scale, csa_stream_t stream);
+
+/*
+ * csa_indexer_topk_fp8 - csa_indexer_topk on e4m3 codes with per-row scales.
+ *
+ * Scores, with the codes' exact values q8, k8 and the scales q_scale,
+ * k_scale of csa_quantize_e4m3 (non-negative, so they commute with the ReLU):
+ *   I[b,t,j] = k_scale[b,j] * sum_h (w[b,t,h] * q_scale[b,t,h])
+ *                                   * max(0, q8[b,t,h,:] . k8[b,j,:])
+ * for the visible (and, with doc_ids, same-document) blocks; the selection,
+ * the output layout, doc_ids and the workspace rules are those of
+ * csa_indexer_topk.  The code products are exact in the fp32 accumulators
+ * (tcgen05 kind::f8f6f4 for d_I in {128, 256} and H_I <= 64, a CUDA-core
+ * kernel otherwise).
+ *
+ *   q8       in  [b, sq, H_I, d_I] uint8 e4m3 codes
+ *   q_scale  in  [b, sq, H_I]      fp32
+ *   k8       in  [b, n_c, d_I]     uint8 e4m3 codes
+ *   k_scale  in  [b, n_c]          fp32
+ *   other arguments as csa_indexer_topk
+ * Errors: as csa_indexer_topk, with d_I % 16 != 0 (instead of % 8) and a
+ * null scale pointer also INVALID_ARG.
+ */
+csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const uint8_t* k8,
+                                  const float* k_scale, const float* w, const int32_t* doc_ids,
+                                  int32_t* topk_idx, float* topk_score, int b, int sq, int n_c,
+                                  int H_I, int d_I, int ratio, int topk, void* workspace,
+                                  size_t workspace_bytes, csa_stream_t stream);
+
+/*
  * csa_indexer_topk_noalloc - csa_indexer_topk for callers that cannot
  * allocate device memory.
  *

@@ -110,6 +110,17 @@ def test_invalid_arguments_rejected_on_host(lib):
                                 64, 4, 4, 1, None) == INVALID
     assert lib.csa_indexer_loss(fake, fake, fake, fake, fake, fake, fake, fake, fake, 1, 8, 2, 4,
                                 512, 4, 4, 1, None) == UNSUPPORTED
+    # e4m3 quantization: row width not a multiple of 8; misaligned codes; no rows is a no-op
+    assert lib.csa_quantize_e4m3(fake, 4, 12, 1, fake, fake, None) == INVALID
+    assert lib.csa_quantize_e4m3(fake, 4, 64, 1, fake + 8, fake, None) == INVALID
+    assert lib.csa_quantize_e4m3(None, 0, 64, 1, None, None, None) == 0
+    # FP8 indexer: null scale; d_I not a multiple of 16; workspace too small
+    assert lib.csa_indexer_topk_fp8(fake, None, fake, fake, fake, None, fake, None, 1, 512, 128, 4,
+                                    128, 4, 16, fake, 1 << 20, None) == INVALID
+    assert lib.csa_indexer_topk_fp8(fake, fake, fake, fake, fake, None, fake, None, 1, 512, 128, 4,
+                                    40, 4, 16, fake, 1 << 20, None) == INVALID
+    assert lib.csa_indexer_topk_fp8(fake, fake, fake, fake, fake, None, fake, None, 1, 512, 128, 4,
+                                    128, 4, 16, fake, 64, None) == WORKSPACE
     # device status needs an output pointer
     assert lib.csa_get_device_status(None, None, None) == INVALID
 
