@@ -104,14 +104,23 @@ def visible_blocks(t: int, ratio: int) -> int:
     return (t + 1) // ratio
 
 
-def compress(kv, score, ratio: int, out_dtype: str = "fp64"):
-    """Pool each block of `ratio` consecutive tokens.
+def pooling_window(j: int, ratio: int, coff: int = 1):
+    """Tokens pooled into compressed entry j: the coff blocks of `ratio`
+    tokens ending with block j, clipped at token 0.  coff = 1 is the
+    non-overlapping compressor ("compress_ratio == 128 (non-overlapping,
+    coff = 1)", compressor review of PR #6400); coff = 2 lets each entry also
+    pool the previous block (the overlapping reading)."""
+    return slice(max(0, (j + 1 - coff) * ratio), (j + 1) * ratio)
+
+
+def compress(kv, score, ratio: int, out_dtype: str = "fp64", coff: int = 1):
+    """Pool the tokens of each entry's window (`pooling_window`).
 
     kv    [b, sq, d]   raw KV rows
     score [b, sq, d_s] pooling scores, d_s in {1, d} (d_s = 1 broadcasts)
     returns kv_c [b, n_c, d], n_c = sq // ratio, rounded once to out_dtype.
 
-    Per block j and channel c: weights = softmax over the block's tokens of
+    Per entry j and channel c: weights = softmax over the window's tokens of
     score[., c]; kv_c[j, c] = sum_t weights_t * kv[t, c].  The pages keep the
     weights, the products and the sum in fp32 and cast once (compressor
     review of PR #6400); the oracle does the same in fp64.
@@ -123,8 +132,8 @@ def compress(kv, score, ratio: int, out_dtype: str = "fp64"):
     out = np.zeros((b, n_c, d))
     for bi in range(b):
         for j in range(n_c):
-            rows = slice(j * ratio, (j + 1) * ratio)
-            s = score[bi, rows]                     # [ratio, d_s]
+            rows = pooling_window(j, ratio, coff)
+            s = score[bi, rows]                     # [window, d_s]
             s = s - s.max(axis=0, keepdims=True)
             e = np.exp(s)
             weights = e / e.sum(axis=0, keepdims=True)
@@ -132,12 +141,14 @@ def compress(kv, score, ratio: int, out_dtype: str = "fp64"):
     return round_to_storage(out, out_dtype)
 
 
-def compress_bwd(kv, score, ratio: int, g):
+def compress_bwd(kv, score, ratio: int, g, coff: int = 1):
     """Gradient of the pooling (unrounded) w.r.t. kv and score.
 
-    g [b, n_c, d] = dL/dkv_c.  With weights w_t of a block and channel:
-      dkv_t   = w_t * g
-      dscore_t = w_t * (g*kv_t - sum_t' w_t' * g*kv_t')
+    g [b, n_c, d] = dL/dkv_c.  With weights w_t of an entry's window and a
+    channel, each entry contributes
+      dkv_t    += w_t * g
+      dscore_t += w_t * (g*kv_t - sum_t' w_t' * g*kv_t')
+    (a token in several windows, coff > 1, sums their contributions).
     Tokens past the last complete block get zero gradient.  A d_s = 1 score
     sums its per-channel gradient over channels.
     """
@@ -151,15 +162,16 @@ def compress_bwd(kv, score, ratio: int, g):
     dscore = np.zeros_like(score)
     for bi in range(b):
         for j in range(n_c):
-            rows = slice(j * ratio, (j + 1) * ratio)
+            rows = pooling_window(j, ratio, coff)
+            n = rows.stop - rows.start
             s = score[bi, rows]
             s = s - s.max(axis=0, keepdims=True)
             e = np.exp(s)
-            weights = np.broadcast_to(e / e.sum(axis=0, keepdims=True), (ratio, d))
-            dkv[bi, rows] = weights * g[bi, j]
-            gk = g[bi, j] * kv[bi, rows]                      # [ratio, d]
+            weights = np.broadcast_to(e / e.sum(axis=0, keepdims=True), (n, d))
+            dkv[bi, rows] += weights * g[bi, j]
+            gk = g[bi, j] * kv[bi, rows]                      # [window, d]
             ds = weights * (gk - (weights * gk).sum(axis=0, keepdims=True))
-            dscore[bi, rows] = ds if d_s == d else ds.sum(axis=1, keepdims=True)
+            dscore[bi, rows] += ds if d_s == d else ds.sum(axis=1, keepdims=True)
     return dkv, dscore
 
 

@@ -137,6 +137,62 @@ def test_compress_bwd_finite_differences(d_s):
     assert np.all(dkv[0, 6] == 0) and np.all(dscore[0, 6] == 0)
 
 
+# overlapping compression (coff = 2): entry j pools blocks j-1 and j
+
+def test_compress_overlap_is_shifted_double_ratio_pooling():
+    """Odd entries pool the non-overlapping 2r-blocks of the sequence, even
+    entries (j >= 2) those of the sequence shifted by r tokens, entry 0 the
+    first r-block alone: three independent non-overlapping poolings."""
+    rng = np.random.default_rng(7)
+    r, sq, d = 4, 37, 5
+    kv = rng.standard_normal((2, sq, d))
+    score = rng.standard_normal((2, sq, d)) * 3
+    out = orc.compress(kv, score, r, coff=2)
+    n_c = sq // r
+    assert out.shape == (2, n_c, d)
+    odd = orc.compress(kv, score, 2 * r)                       # entries 1, 3, 5, ...
+    even = orc.compress(kv[:, r:], score[:, r:], 2 * r)        # entries 2, 4, ...
+    np.testing.assert_allclose(out[:, 1::2], odd[:, :len(range(1, n_c, 2))], atol=1e-14)
+    np.testing.assert_allclose(out[:, 2::2], even[:, :len(range(2, n_c, 2))], atol=1e-14)
+    np.testing.assert_allclose(out[:, 0], orc.compress(kv[:, :r], score[:, :r], r)[:, 0],
+                               atol=1e-14)
+
+
+def test_compress_overlap_constant_score_is_window_mean():
+    rng = np.random.default_rng(8)
+    kv = rng.standard_normal((1, 16, 3))
+    out = orc.compress(kv, np.full((1, 16, 1), -2.5), 4, coff=2)
+    np.testing.assert_allclose(out[0, 0], kv[0, 0:4].mean(axis=0), atol=1e-14)
+    for j in range(1, 4):
+        np.testing.assert_allclose(out[0, j], kv[0, 4 * j - 4:4 * j + 4].mean(axis=0), atol=1e-14)
+
+
+@pytest.mark.parametrize("d_s", [1, 3])
+def test_compress_overlap_bwd_finite_differences(d_s):
+    rng = np.random.default_rng(9)
+    b, sq, d, r = 1, 11, 3, 3   # tokens 9, 10 are past the last block: zero gradient
+    kv = rng.standard_normal((b, sq, d))
+    score = rng.standard_normal((b, sq, d_s))
+    g = rng.standard_normal((b, sq // r, d))
+    dkv, dscore = orc.compress_bwd(kv, score, r, g, coff=2)
+    h = 1e-6
+
+    def loss(kv_, sc_):
+        return float((orc.compress(kv_, sc_, r, coff=2) * g).sum())
+    for arr, grad in ((kv, dkv), (score, dscore)):
+        fd = np.zeros_like(arr)
+        for i in np.ndindex(arr.shape):
+            a0 = arr[i]
+            arr[i] = a0 + h
+            lp = loss(kv, score)
+            arr[i] = a0 - h
+            lm = loss(kv, score)
+            arr[i] = a0
+            fd[i] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(grad, fd, atol=1e-8)
+    assert np.all(dkv[0, 9:] == 0) and np.all(dscore[0, 9:] == 0)
+
+
 # ---------------------------------------------------------------------------
 # indexer and top-k
 # ---------------------------------------------------------------------------
