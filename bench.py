@@ -421,6 +421,30 @@ def run_gpu(args, rank, world, local_rank):
             "topk_overlap_with_bf16": round(kept / max(1, int((idx >= 0).sum().item())), 5),
             "kernels": "quantize: warp per row; scores: tcgen05 kind::f8f6f4, same select",
         }
+        # overlapping compression (coff = 2: each entry pools its own block and
+        # the previous one), forward and backward in the layer layout
+        kvc = torch.empty(b, n_c, d, dtype=cfg.torch_dtype, device=dev)
+        dkv_raw = torch.zeros(b, sq, d, dtype=torch.float32, device=dev)
+        ov_ev = []
+        for i in range(args.warmup + args.steps):
+            flush_l2()
+            e3 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e3[0].record(stream)
+            csa.csa_compress_overlap(kv_full[:, :sq], d_in["score"], cfg.ratio, 2, out=kvc)
+            e3[1].record(stream)
+            csa.csa_compress_overlap_bwd(kv_full[:, :sq], d_in["score"], cfg.ratio, 2,
+                                         dkv[:, sq:], dkv_raw, dscore=dscore)
+            e3[2].record(stream)
+            if i >= args.warmup:
+                ov_ev.append(e3)
+        torch.cuda.synchronize()
+        variants["compress_overlap"] = {
+            "workload": f"{cfg.name}: compressor with coff = 2 (windows of 2 x ratio tokens)",
+            "compress_ms": round(sum(e[0].elapsed_time(e[1]) for e in ov_ev) / len(ov_ev), 4),
+            "compress_bwd_ms": round(sum(e[1].elapsed_time(e[2]) for e in ov_ev) / len(ov_ev), 4),
+            "coff1_compress_ms": round(sum(seg[0]) / len(seg[0]), 4),
+            "coff1_compress_bwd_ms": round(sum(seg[4]) / len(seg[4]), 4),
+        }
 
     # ---- end-to-end through host buffers -------------------------------------
     # Every step copies all of its inputs host -> device (pinned) and all of its

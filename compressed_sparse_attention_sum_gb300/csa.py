@@ -34,6 +34,10 @@ SIGNATURES = {
                               _c_int, _c_p]),
     "csa_compress_bwd": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll, _c_p, _c_ll, _c_p]
                          + [_c_int] * 5 + [_c_p]),
+    "csa_compress_overlap": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll] + [_c_int] * 6
+                             + [_c_p]),
+    "csa_compress_overlap_bwd": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll, _c_p, _c_ll,
+                                          _c_p] + [_c_int] * 6 + [_c_p]),
     "csa_indexer_topk_workspace_size": (_c_sz, [_c_int] * 6 + [_c_int]),
     "csa_indexer_topk_min_workspace": (_c_sz, [_c_int, _c_int]),
     "csa_indexer_topk": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
@@ -108,15 +112,7 @@ def _stream(stream=None) -> int:
     return s.cuda_stream
 
 
-def csa_compress(kv: torch.Tensor, score: torch.Tensor, ratio: int,
-                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Softmax-weighted pooling of `ratio` consecutive tokens.
-
-    kv [b, sq, d] (rows contiguous; may be the raw-row view kv_full[:, :sq]),
-    score [b, sq, d] or [b, sq, 1] packed, out [b, sq//ratio, d] (rows
-    contiguous; may be the view kv_full[:, sq:]).
-    """
-    lib = load_library()
+def _compress_out(kv, score, ratio, out):
     _need(kv, "kv", contiguous=False)
     _need(score, "score", dtype=kv.dtype)
     b, sq, d = kv.shape
@@ -128,20 +124,40 @@ def csa_compress(kv: torch.Tensor, score: torch.Tensor, ratio: int,
     _need(out, "out", dtype=kv.dtype, contiguous=False)
     if out.shape != (b, n_c, d) or out.stride(2) != 1 or out.stride(1) != d:
         raise ValueError("out must be [b, sq//ratio, d] with contiguous rows")
+    return out
+
+
+def csa_compress(kv: torch.Tensor, score: torch.Tensor, ratio: int,
+                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Softmax-weighted pooling of `ratio` consecutive tokens.
+
+    kv [b, sq, d] (rows contiguous; may be the raw-row view kv_full[:, :sq]),
+    score [b, sq, d] or [b, sq, 1] packed, out [b, sq//ratio, d] (rows
+    contiguous; may be the view kv_full[:, sq:]).
+    """
+    lib = load_library()
+    out = _compress_out(kv, score, ratio, out)
+    b, sq, d = kv.shape
     _check("csa_compress", lib.csa_compress(kv.data_ptr(), kv.stride(0), score.data_ptr(),
                                             score.shape[2], out.data_ptr(), out.stride(0), b, sq,
                                             d, ratio, _dt(kv), _stream(stream)))
     return out
 
 
-def csa_compress_bwd(kv: torch.Tensor, score: torch.Tensor, ratio: int, dout: torch.Tensor,
-                     dkv: torch.Tensor, dscore: Optional[torch.Tensor] = None,
-                     stream=None) -> torch.Tensor:
-    """Gradient of the pooling: adds w*dout into dkv (in place) and returns
-    dscore.  kv [b, sq, d] and dkv [b, sq, d] (fp32) may be row-contiguous
-    views (kv_full[:, :sq], dkv_full[:, :sq]); dout [b, sq//ratio, d] fp32 may
-    be dkv_full[:, sq:]."""
+def csa_compress_overlap(kv: torch.Tensor, score: torch.Tensor, ratio: int, coff: int,
+                         out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """csa_compress with windows of `coff` blocks ending at each entry's own
+    block (coff = 1 is csa_compress)."""
     lib = load_library()
+    out = _compress_out(kv, score, ratio, out)
+    b, sq, d = kv.shape
+    _check("csa_compress_overlap", lib.csa_compress_overlap(
+        kv.data_ptr(), kv.stride(0), score.data_ptr(), score.shape[2], out.data_ptr(),
+        out.stride(0), b, sq, d, ratio, coff, _dt(kv), _stream(stream)))
+    return out
+
+
+def _compress_bwd_args(kv, score, dout, dkv, dscore):
     _need(kv, "kv", contiguous=False)
     _need(score, "score", dtype=kv.dtype)
     _need(dout, "dout", dtype=torch.float32, contiguous=False)
@@ -153,9 +169,36 @@ def csa_compress_bwd(kv: torch.Tensor, score: torch.Tensor, ratio: int, dout: to
     if dscore is None:
         dscore = torch.empty(b, sq, score.shape[2], dtype=torch.float32, device=kv.device)
     _need(dscore, "dscore", dtype=torch.float32)
+    return dscore
+
+
+def csa_compress_bwd(kv: torch.Tensor, score: torch.Tensor, ratio: int, dout: torch.Tensor,
+                     dkv: torch.Tensor, dscore: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """Gradient of the pooling: adds w*dout into dkv (in place) and returns
+    dscore.  kv [b, sq, d] and dkv [b, sq, d] (fp32) may be row-contiguous
+    views (kv_full[:, :sq], dkv_full[:, :sq]); dout [b, sq//ratio, d] fp32 may
+    be dkv_full[:, sq:]."""
+    lib = load_library()
+    dscore = _compress_bwd_args(kv, score, dout, dkv, dscore)
+    b, sq, d = kv.shape
     _check("csa_compress_bwd", lib.csa_compress_bwd(
         kv.data_ptr(), kv.stride(0), score.data_ptr(), score.shape[2], dout.data_ptr(),
         dout.stride(0), dkv.data_ptr(), dkv.stride(0), dscore.data_ptr(), b, sq, d, ratio,
+        _dt(kv), _stream(stream)))
+    return dscore
+
+
+def csa_compress_overlap_bwd(kv: torch.Tensor, score: torch.Tensor, ratio: int, coff: int,
+                             dout: torch.Tensor, dkv: torch.Tensor,
+                             dscore: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Gradient of csa_compress_overlap (arguments as csa_compress_bwd)."""
+    lib = load_library()
+    dscore = _compress_bwd_args(kv, score, dout, dkv, dscore)
+    b, sq, d = kv.shape
+    _check("csa_compress_overlap_bwd", lib.csa_compress_overlap_bwd(
+        kv.data_ptr(), kv.stride(0), score.data_ptr(), score.shape[2], dout.data_ptr(),
+        dout.stride(0), dkv.data_ptr(), dkv.stride(0), dscore.data_ptr(), b, sq, d, ratio, coff,
         _dt(kv), _stream(stream)))
     return dscore
 

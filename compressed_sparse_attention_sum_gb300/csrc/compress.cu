@@ -173,6 +173,94 @@ __global__ void __launch_bounds__(64) compress_bwd_kernel(
   }
 }
 
+// Overlapping compression: entry j pools the coff blocks ending with block j,
+// tokens [max(0, (j + 1 - coff) r), (j + 1) r), with one softmax over the
+// window ("Add unfused SBHD compressed sparse attention", compressor review:
+// coff = 1 is the non-overlapping case).  Online softmax over the window.
+template <typename T>
+__global__ void __launch_bounds__(64) compress_overlap_kernel(
+    const T* __restrict__ kv, long long kv_bs, const T* __restrict__ score, int score_width,
+    T* __restrict__ out, long long out_bs, int sq, int d, int ratio, int n_c, int coff) {
+  const int groups = d / 8;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int bi = blockIdx.y;
+  if (gid >= (long long)n_c * groups) return;
+  const int j = (int)(gid / groups);
+  const int c0 = (int)(gid % groups) * 8;
+  const int t0 = max(0, (j + 1 - coff) * ratio);
+  const T* kvp = kv + bi * kv_bs + (long long)t0 * d + c0;
+  const T* scp = score + ((long long)bi * sq + t0) * score_width;
+  float v[1][8], s[1][8], m[8], l[8], r[8];
+  pool_block<T, 0>(kvp, scp, (j + 1) * ratio - t0, d, score_width, c0, v, s, m, l, r);
+  store8(out + bi * out_bs + (long long)j * d + c0, r);
+}
+
+// Its backward.  The thread of block j owns the block's ratio tokens, which
+// lie in the windows of entries j .. j + C - 1; it forms those windows'
+// softmax statistics and pooled rows first, then sums the windows'
+// contributions per token, so every token is written by one thread.
+template <typename T, int C>
+__global__ void __launch_bounds__(64) compress_overlap_bwd_kernel(
+    const T* __restrict__ kv, long long kv_bs, const T* __restrict__ score, int score_width,
+    const float* __restrict__ g, long long g_bs, float* __restrict__ dkv, long long dkv_bs,
+    float* __restrict__ dscore, int sq, int d, int ratio, int n_c) {
+  const int groups = d / 8;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int bi = blockIdx.y;
+  if (gid >= (long long)n_c * groups) {
+    if (score_width == 1) return;  // zeroed before the launch
+    const long long tok = (long long)n_c * ratio + (gid - (long long)n_c * groups) / groups;
+    if (tok >= sq) return;
+    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    store8(dscore + ((long long)bi * sq + tok) * score_width + (gid % groups) * 8, z);
+    return;
+  }
+  const int j = (int)(gid / groups);
+  const int c0 = (int)(gid % groups) * 8;
+  const T* kvb = kv + bi * kv_bs + c0;
+  const T* scb = score + (long long)bi * sq * score_width;
+  float m[C][8], l[C][8], pooled[C][8], gv[C][8];
+#pragma unroll
+  for (int k = 0; k < C; ++k) {
+    const int w = j + k;
+    if (w >= n_c) continue;
+    const int t0 = max(0, (w + 1 - C) * ratio);
+    float v[1][8], s[1][8];
+    pool_block<T, 0>(kvb + (long long)t0 * d, scb + (long long)t0 * score_width,
+                     (w + 1) * ratio - t0, d, score_width, c0, v, s, m[k], l[k], pooled[k]);
+    load8(g + bi * g_bs + (long long)w * d + c0, gv[k]);
+  }
+  float* dkp = dkv + bi * dkv_bs + (long long)j * ratio * d + c0;
+  for (int t = 0; t < ratio; ++t) {
+    const long long tok = (long long)j * ratio + t;
+    float vt[8], st[8], dt[8], ds[8];
+    load_token(kvb + (long long)j * ratio * d, scb + (long long)j * ratio * score_width, t, d,
+               score_width, c0, vt, st);
+    load8(dkp + (long long)t * d, dt);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ds[i] = 0.f;
+#pragma unroll
+    for (int k = 0; k < C; ++k) {
+      if (j + k >= n_c) continue;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float w = expf(st[i] - m[k][i]) / l[k][i];
+        dt[i] = fmaf(w, gv[k][i], dt[i]);
+        ds[i] = fmaf(w * gv[k][i], vt[i] - pooled[k][i], ds[i]);
+      }
+    }
+    store8(dkp + (long long)t * d, dt);
+    if (score_width == 1) {
+      float dsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dsum += ds[i];
+      atomicAdd(dscore + (long long)bi * sq + tok, dsum);
+    } else {
+      store8(dscore + ((long long)bi * sq + tok) * score_width + c0, ds);
+    }
+  }
+}
+
 namespace {
 constexpr int kCompressThreads = 64;
 
@@ -247,6 +335,56 @@ cudaError_t launch_compress(const void* kv, long long kv_bs, const void* score, 
     else
       compress_fwd_t<float, 0>(kv, kv_bs, score, score_width, out, out_bs, b, sq, d, ratio, s);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress_overlap(const void* kv, long long kv_bs, const void* score,
+                                    int score_width, void* out, long long out_bs, int b, int sq,
+                                    int d, int ratio, int coff, bool bf16, cudaStream_t s) {
+  if (coff == 1)
+    return launch_compress(kv, kv_bs, score, score_width, out, out_bs, b, sq, d, ratio, bf16, s);
+  const int n_c = sq / ratio;
+  const long long work = (long long)n_c * (d / 8);
+  dim3 grid((unsigned)((work + kCompressThreads - 1) / kCompressThreads), (unsigned)b);
+  if (bf16)
+    compress_overlap_kernel<__nv_bfloat16><<<grid, kCompressThreads, 0, s>>>(
+        (const __nv_bfloat16*)kv, kv_bs, (const __nv_bfloat16*)score, score_width,
+        (__nv_bfloat16*)out, out_bs, sq, d, ratio, n_c, coff);
+  else
+    compress_overlap_kernel<float><<<grid, kCompressThreads, 0, s>>>(
+        (const float*)kv, kv_bs, (const float*)score, score_width, (float*)out, out_bs, sq, d,
+        ratio, n_c, coff);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress_overlap_bwd(const void* kv, long long kv_bs, const void* score,
+                                        int score_width, const float* g, long long g_bs,
+                                        float* dkv, long long dkv_bs, float* dscore, int b,
+                                        int sq, int d, int ratio, int coff, bool bf16,
+                                        cudaStream_t s) {
+  if (coff == 1)
+    return launch_compress_bwd(kv, kv_bs, score, score_width, g, g_bs, dkv, dkv_bs, dscore, b,
+                               sq, d, ratio, bf16, s);
+  if (coff != 2) return cudaErrorInvalidValue;
+  if (score_width == 1) {
+    cudaError_t e = launch_zero_f32(dscore, (size_t)b * sq, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int n_c = sq / ratio;
+  const int tail = score_width == 1 ? 0 : sq - n_c * ratio;
+  const long long work = (long long)(n_c + tail) * (d / 8);
+  if (work == 0) return cudaSuccess;
+  dim3 grid((unsigned)((work + kCompressThreads - 1) / kCompressThreads), (unsigned)b);
+  if (bf16)
+    compress_overlap_bwd_kernel<__nv_bfloat16, 2><<<grid, kCompressThreads, 0, s>>>(
+        (const __nv_bfloat16*)kv, kv_bs, (const __nv_bfloat16*)score, score_width, g, g_bs, dkv,
+        dkv_bs, dscore, sq, d, ratio, n_c);
+  else
+    compress_overlap_bwd_kernel<float, 2><<<grid, kCompressThreads, 0, s>>>(
+        (const float*)kv, kv_bs, (const float*)score, score_width, g, g_bs, dkv, dkv_bs, dscore,
+        sq, d, ratio, n_c);
+  count_launches(1);
   return cudaGetLastError();
 }
 

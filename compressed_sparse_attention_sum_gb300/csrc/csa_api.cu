@@ -209,6 +209,66 @@ csa_status_t csa_compress_bwd(const void* kv, long long kv_batch_stride, const v
                                             sq, d, ratio, dt == CSA_BF16, (cudaStream_t)stream));
 }
 
+csa_status_t csa_compress_overlap(const void* kv, long long kv_batch_stride, const void* score,
+                                  int score_width, void* out, long long out_batch_stride, int b,
+                                  int sq, int d, int ratio, int coff, csa_dtype_t dt,
+                                  csa_stream_t stream) {
+  if (coff < 1) return CSA_ERR_INVALID_ARG;
+  if (coff == 1)
+    return csa_compress(kv, kv_batch_stride, score, score_width, out, out_batch_stride, b, sq, d,
+                        ratio, dt, stream);
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (kv == nullptr || score == nullptr || out == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(kv) || !aligned16(score) || !aligned16(out)) return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || d < 8 || d % 8 != 0 || ratio < 1 || sq < ratio)
+    return CSA_ERR_INVALID_ARG;
+  if (score_width != 1 && score_width != d) return CSA_ERR_INVALID_ARG;
+  const int n_c = sq / ratio;
+  if (kv_batch_stride < (long long)sq * d || out_batch_stride < (long long)n_c * d)
+    return CSA_ERR_INVALID_ARG;
+  const int esz = dt == CSA_BF16 ? 2 : 4;
+  if ((kv_batch_stride * esz) % 16 != 0 || (out_batch_stride * esz) % 16 != 0)
+    return CSA_ERR_INVALID_ARG;
+  if (d > kMaxD || coff > 2) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(csa::launch_compress_overlap(kv, kv_batch_stride, score, score_width, out,
+                                                out_batch_stride, b, sq, d, ratio, coff,
+                                                dt == CSA_BF16, (cudaStream_t)stream));
+}
+
+csa_status_t csa_compress_overlap_bwd(const void* kv, long long kv_batch_stride,
+                                      const void* score, int score_width, const float* dout,
+                                      long long dout_batch_stride, float* dkv,
+                                      long long dkv_batch_stride, float* dscore, int b, int sq,
+                                      int d, int ratio, int coff, csa_dtype_t dt,
+                                      csa_stream_t stream) {
+  if (coff < 1) return CSA_ERR_INVALID_ARG;
+  if (coff == 1)
+    return csa_compress_bwd(kv, kv_batch_stride, score, score_width, dout, dout_batch_stride, dkv,
+                            dkv_batch_stride, dscore, b, sq, d, ratio, dt, stream);
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (kv == nullptr || score == nullptr || dout == nullptr || dkv == nullptr || dscore == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(kv) || !aligned16(score) || !aligned16(dout) || !aligned16(dkv) ||
+      !aligned16(dscore))
+    return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || d < 8 || d % 8 != 0 || ratio < 1 || sq < ratio)
+    return CSA_ERR_INVALID_ARG;
+  if (score_width != 1 && score_width != d) return CSA_ERR_INVALID_ARG;
+  const int n_c = sq / ratio;
+  if (kv_batch_stride < (long long)sq * d || dkv_batch_stride < (long long)sq * d ||
+      dout_batch_stride < (long long)n_c * d)
+    return CSA_ERR_INVALID_ARG;
+  const int esz = dt == CSA_BF16 ? 2 : 4;
+  if ((kv_batch_stride * esz) % 16 != 0 || (dout_batch_stride * 4) % 16 != 0 ||
+      (dkv_batch_stride * 4) % 16 != 0)
+    return CSA_ERR_INVALID_ARG;
+  if (d > kMaxD || coff > 2) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(csa::launch_compress_overlap_bwd(kv, kv_batch_stride, score, score_width, dout,
+                                                    dout_batch_stride, dkv, dkv_batch_stride,
+                                                    dscore, b, sq, d, ratio, coff,
+                                                    dt == CSA_BF16, (cudaStream_t)stream));
+}
+
 size_t csa_indexer_topk_min_workspace(int b, int n_c) {
   if (b < 1 || n_c < 1) return 0;
   return (size_t)b * kIndexerTileRows * (size_t)n_c * sizeof(float);

@@ -24,6 +24,16 @@ cudaError_t launch_compress_bwd(const void* kv, long long kv_bs, const void* sco
                                 long long dkv_bs, float* dscore, int b, int sq, int d, int ratio,
                                 bool bf16, cudaStream_t s);
 
+// Overlapping compression (coff blocks per pooling window; coff 1 = the above).
+cudaError_t launch_compress_overlap(const void* kv, long long kv_bs, const void* score,
+                                    int score_width, void* out, long long out_bs, int b, int sq,
+                                    int d, int ratio, int coff, bool bf16, cudaStream_t s);
+cudaError_t launch_compress_overlap_bwd(const void* kv, long long kv_bs, const void* score,
+                                        int score_width, const float* g, long long g_bs,
+                                        float* dkv, long long dkv_bs, float* dscore, int b,
+                                        int sq, int d, int ratio, int coff, bool bf16,
+                                        cudaStream_t s);
+
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
 
 }  // namespace csa

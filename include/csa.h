@@ -138,6 +138,44 @@ csa_status_t csa_compress_bwd(const void* kv, long long kv_batch_stride,
                               csa_dtype_t dt, csa_stream_t stream);
 
 /*
+ * csa_compress_overlap - csa_compress with overlapping pooling windows.
+ *
+ * The compressor review of "Add unfused SBHD compressed sparse attention"
+ * calls ratio 128 "non-overlapping, coff = 1"; this call takes coff, the
+ * number of ratio-blocks each compressed entry pools (the library's reading:
+ * the window ends with the entry's own block).  For entry j < n_c:
+ *   window(j) = tokens [max(0, (j + 1 - coff) * r), (j + 1) * r)
+ *   weights_t = softmax over t in window(j) of score[b, t, c'],
+ *   out[b, j, c] = sum_t weights_t * kv[b, t, c]
+ * in fp32, cast once.  coff = 1 is csa_compress; the first coff - 1 entries
+ * pool the tokens that exist.  Arguments as csa_compress.
+ * Errors: as csa_compress; INVALID_ARG for coff < 1, UNSUPPORTED for coff > 2.
+ */
+csa_status_t csa_compress_overlap(const void* kv, long long kv_batch_stride,
+                                  const void* score, int score_width,
+                                  void* out, long long out_batch_stride,
+                                  int b, int sq, int d, int ratio, int coff,
+                                  csa_dtype_t dt, csa_stream_t stream);
+
+/*
+ * csa_compress_overlap_bwd - gradient of csa_compress_overlap.
+ *
+ * Each entry j contributes, for t in window(j), with its weights w_t and
+ * g = dout[b, j, c]:
+ *   dkv[b, t, c]     += w_t * g
+ *   dscore[b, t, c'] += w_t * g * (kv[b, t, c] - out[b, j, c])
+ * so a token in several windows sums their contributions (dkv accumulates
+ * into what it holds; dscore is fully written).  Arguments and errors as
+ * csa_compress_bwd, plus coff as in csa_compress_overlap.
+ */
+csa_status_t csa_compress_overlap_bwd(const void* kv, long long kv_batch_stride,
+                                      const void* score, int score_width,
+                                      const float* dout, long long dout_batch_stride,
+                                      float* dkv, long long dkv_batch_stride, float* dscore,
+                                      int b, int sq, int d, int ratio, int coff,
+                                      csa_dtype_t dt, csa_stream_t stream);
+
+/*
  * Bytes of indexer workspace that csa_indexer_topk uses by default: the
  * fp32 score rows of one chunk of queries (n_c floats per query row, at
  * most 128 MiB, at least one 128-row tile).  Any workspace of at least

@@ -121,6 +121,13 @@ def test_invalid_arguments_rejected_on_host(lib):
                                     40, 4, 16, fake, 1 << 20, None) == INVALID
     assert lib.csa_indexer_topk_fp8(fake, fake, fake, fake, fake, None, fake, None, 1, 512, 128, 4,
                                     128, 4, 16, fake, 64, None) == WORKSPACE
+    # overlapping compression: coff < 1 invalid, coff > 2 unsupported
+    assert lib.csa_compress_overlap(fake, 512, fake, 64, fake, 128, 1, 8, 64, 4, 0, 1,
+                                    None) == INVALID
+    assert lib.csa_compress_overlap(fake, 512, fake, 64, fake, 128, 1, 8, 64, 4, 3, 1,
+                                    None) == UNSUPPORTED
+    assert lib.csa_compress_overlap_bwd(fake, 512, fake, 64, fake, 128, None, 512, fake, 1, 8,
+                                        64, 4, 2, 1, None) == INVALID
     # device status needs an output pointer
     assert lib.csa_get_device_status(None, None, None) == INVALID
 
