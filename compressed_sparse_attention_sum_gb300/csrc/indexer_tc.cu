@@ -10,14 +10,15 @@
 // One CTA computes a tile of 128 queries x 128 compressed blocks of one batch
 // element, for all indexer heads, and writes the fp32 tile to the score
 // workspace that the per-row select kernel reads.  Tiles entirely above the
-// causal boundary are skipped.  Roles (320 threads):
+// causal boundary are skipped.  Roles (352 threads):
 //   warp 0      TMA producer: the k_I tile once, then one q_I head tile per
 //               stage of a 6-deep ring (3D tensor map over [b*sq, H_I, d_I])
-//   warp 1      TMEM owner + MMA issuer: per head, d_I/16 tcgen05.mma
-//               (M=128 queries, N=128 blocks, K=16) into one of two TMEM
-//               accumulators, committed to the ring's "empty" barrier and to
-//               the accumulator's "full" barrier
-//   warps 2-9   epilogue: tcgen05.ld of the head's accumulator (row = query =
+//   warps 1-2   MMA issuers (warp 1 also owns TMEM): warp 1 the even heads,
+//               warp 2 the odd ones, each into its own TMEM accumulator:
+//               d_I/16 tcgen05.mma (M=128 queries, N=128 blocks, K=16) per
+//               head, committed to the ring's "empty" barrier and to the
+//               accumulator's "full" barrier
+//   warps 3-10  epilogue: tcgen05.ld of the head's accumulator (row = query =
 //               TMEM lane), release of the accumulator, then
 //               I += w[t,h] * max(S, 0) in registers; each warp owns one TMEM
 //               lane quarter and one half of the 128 columns
@@ -45,7 +46,7 @@ using namespace csa::umma;
 constexpr int kTileM = 128;     // queries per tile (TMEM lanes)
 constexpr int kTileN = 128;     // compressed blocks per tile (TMEM columns per accumulator)
 constexpr int kStages = 6;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kEpiWarps = 8;
 constexpr int kMaxHeads = 64;
 constexpr uint32_t kTmemCols = 256;
@@ -126,15 +127,20 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
                       bi * sq + tq0);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp <= 2) {
+    // ---------------- MMA issuers ----------------
+    // tcgen05.mma holds its issuing thread until the tensor core has taken
+    // the instruction, so the waits and commits of one thread would leave the
+    // tensor core idle between heads: two threads (warps 1 and 2) take the
+    // even and the odd heads, each with its own accumulator, and one issues
+    // while the other waits.
     if (lane == 0) {
       constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(kTileM, kTileN) : idesc_bf16_f32(kTileM, kTileN);
       bool ok = mbar_wait(b_full, 0);
       const uint32_t b_base = smem_addr(sB);
-      for (int h = 0; ok && h < H_I; ++h) {
+      const int a = warp - 1;                       // this issuer's accumulator
+      for (int h = a; ok && h < H_I; h += 2) {
         const int s = h % kStages;
-        const int a = h & 1;
         if (!mbar_wait(&full[s], (h / kStages) & 1) ||
             !mbar_wait(&acc_empty[a], ((h >> 1) & 1) ^ 1)) {
           ok = false;
@@ -164,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
   } else {
     // ---------------- epilogue ----------------
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;             // column half of the tile
+    const int half = (warp - 3) >> 2;             // column half of the tile
     const int row = quarter * 32 + lane;          // query within the tile
     // this query's head weights: one 4-byte read per head from its own
     // H_I-float row (L1-resident after the first touch)
