@@ -419,7 +419,7 @@ def run_gpu(args, rank, world, local_rank):
             "quantize_ms": round(t_q, 4), "indexer_topk_ms": round(t_i8, 4),
             "indexer_topk_bf16_ms": round(sum(seg[1]) / len(seg[1]), 4),
             "topk_overlap_with_bf16": round(kept / max(1, int((idx >= 0).sum().item())), 5),
-            "kernels": "quantize: warp per row; scores: tcgen05 kind::f8f6f4, same select",
+            "kernels": "quantize: a lane group per row; scores: tcgen05 kind::f8f6f4, same select",
         }
         # overlapping compression (coff = 2: each entry pools its own block and
         # the previous one), forward and backward in the layer layout
