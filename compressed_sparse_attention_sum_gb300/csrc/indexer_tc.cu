@@ -14,10 +14,11 @@
 //   warp 0      TMA producer: the k_I tile once, then one q_I head tile per
 //               stage of a 6-deep ring (3D tensor map over [b*sq, H_I, d_I])
 //   warps 1-2   MMA issuers (warp 1 also owns TMEM): warp 1 the even heads,
-//               warp 2 the odd ones, each into its own TMEM accumulator:
-//               d_I/16 tcgen05.mma (M=128 queries, N=128 blocks, K=16) per
-//               head, committed to the ring's "empty" barrier and to the
-//               accumulator's "full" barrier
+//               warp 2 the odd ones; head h goes to TMEM accumulator h % 4
+//               (four, so that the tensor core runs up to three heads ahead
+//               of the epilogue): d_I/16 tcgen05.mma (M=128 queries, N=128
+//               blocks, K=16) per head, committed to the ring's "empty"
+//               barrier and to the accumulator's "full" barrier
 //   warps 3-10  epilogue: tcgen05.ld of the head's accumulator (row = query =
 //               TMEM lane), release of the accumulator, then
 //               I += w[t,h] * max(S, 0) in registers; each warp owns one TMEM
@@ -49,7 +50,8 @@ constexpr int kStages = 6;
 constexpr int kThreads = 352;
 constexpr int kEpiWarps = 8;
 constexpr int kMaxHeads = 64;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kAcc = 4;                 // TMEM accumulators (128 columns each)
+constexpr uint32_t kTmemCols = kAcc * 128;
 template <int DI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -67,9 +69,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(sA + kStages * kTileBytes);
   uint64_t* full = bars;                 // [kStages]
   uint64_t* empty = bars + kStages;      // [kStages]
-  uint64_t* acc_full = bars + 2 * kStages;      // [2]
-  uint64_t* acc_empty = acc_full + 2;           // [2]
-  uint64_t* b_full = acc_empty + 2;
+  uint64_t* acc_full = bars + 2 * kStages;      // [kAcc]
+  uint64_t* acc_empty = acc_full + kAcc;        // [kAcc]
+  uint64_t* b_full = acc_empty + kAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(b_full + 1);
   __shared__ int s_abort;
 
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAcc; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], kEpiWarps);
     }
@@ -132,17 +134,16 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
     // tcgen05.mma holds its issuing thread until the tensor core has taken
     // the instruction, so the waits and commits of one thread would leave the
     // tensor core idle between heads: two threads (warps 1 and 2) take the
-    // even and the odd heads, each with its own accumulator, and one issues
-    // while the other waits.
+    // even and the odd heads, and one issues while the other waits.
     if (lane == 0) {
       constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(kTileM, kTileN) : idesc_bf16_f32(kTileM, kTileN);
       bool ok = mbar_wait(b_full, 0);
       const uint32_t b_base = smem_addr(sB);
-      const int a = warp - 1;                       // this issuer's accumulator
-      for (int h = a; ok && h < H_I; h += 2) {
+      for (int h = warp - 1; ok && h < H_I; h += 2) {
+        const int a = h % kAcc;
         const int s = h % kStages;
         if (!mbar_wait(&full[s], (h / kStages) & 1) ||
-            !mbar_wait(&acc_empty[a], ((h >> 1) & 1) ^ 1)) {
+            !mbar_wait(&acc_empty[a], ((h / kAcc) & 1) ^ 1)) {
           ok = false;
           break;
         }
@@ -181,9 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
     for (int c = 0; c < 64; ++c) acc[c] = 0.f;
     bool ok = true;
     for (int h = 0; h < H_I; ++h) {
-      const int a = h & 1;
+      const int a = h % kAcc;
       // warp-uniform decision: the TMEM loads below are .sync.aligned
-      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (h >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[a], (h / kAcc) & 1))) {
         ok = false;
         break;
       }
@@ -264,7 +265,7 @@ bool indexer_tc_fp8_supported(int H_I, int d_I) {
 
 size_t indexer_tc_smem(int d_I, bool fp8 = false) {
   const size_t tile = (size_t)(fp8 ? d_I / 128 : d_I / 64) * tc::kTileM * 128;
-  return 1024 + tile * (1 + tc::kStages) + 16 * 8 + 16;
+  return 1024 + tile * (1 + tc::kStages) + (2 * tc::kStages + 2 * tc::kAcc + 1) * 8 + 16;
 }
 
 cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const float* w,
