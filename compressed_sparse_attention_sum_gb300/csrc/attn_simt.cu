@@ -224,4 +224,29 @@ cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Zero a (na floats, 16-byte aligned, na % 4 == 0) and b (nb floats) in one
+// launch: the backward's dkv and dsink.
+__global__ void zero_f32_pair_kernel(float4* __restrict__ a, size_t na4, float* __restrict__ b,
+                                     size_t nb) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < nb) b[i] = 0.f;
+  for (; i < na4; i += stride) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+cudaError_t launch_zero_f32_pair(float* a, size_t na, float* b, size_t nb, cudaStream_t s) {
+  if (na % 4 != 0 || nb > 256 * 152) {
+    cudaError_t e = launch_zero_f32(a, na, s);
+    return e == cudaSuccess ? launch_zero_f32(b, nb, s) : e;
+  }
+  size_t blocks = (na / 4 + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks * 256 < nb) blocks = (nb + 255) / 256;
+  if (blocks == 0) return cudaSuccess;
+  zero_f32_pair_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<float4*>(a), na / 4, b,
+                                                       nb);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace csa

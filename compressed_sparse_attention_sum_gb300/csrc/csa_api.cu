@@ -428,8 +428,8 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
   const int Kl = idx ? K : n_c;
   cudaStream_t s = (cudaStream_t)stream;
   const int n_kv = sq + n_c;
-  cudaError_t e = csa::launch_zero_f32(dkv, (size_t)b * n_kv * d, s);
-  if (e == cudaSuccess && dsink != nullptr) e = csa::launch_zero_f32(dsink, (size_t)H, s);
+  cudaError_t e = csa::launch_zero_f32_pair(dkv, (size_t)b * n_kv * d, dsink,
+                                            dsink != nullptr ? (size_t)H : 0, s);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   const char* wm = getenv("CSA_ATTN_WARP_MMA");
   const bool warp_mma = wm && wm[0] == '1';

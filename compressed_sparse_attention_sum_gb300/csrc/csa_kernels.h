@@ -35,5 +35,7 @@ cudaError_t launch_compress_overlap_bwd(const void* kv, long long kv_bs, const v
                                         cudaStream_t s);
 
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
+// Two buffers in one launch (b may be null with nb = 0).
+cudaError_t launch_zero_f32_pair(float* a, size_t na, float* b, size_t nb, cudaStream_t s);
 
 }  // namespace csa
