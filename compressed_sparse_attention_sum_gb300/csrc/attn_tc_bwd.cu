@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
 
   // ---- set-up: barriers, TMEM, Q and dO tiles --------------------------------
   if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(bar_q + i, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar_q + i, 1);
+    mbar_init(bar_d1, 2);                // pass 1: S and dP issued by two threads
+    mbar_init(bar_d1 + 1, 2);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -222,16 +224,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
 
   // ---- pass 1: D = sum_i p_i dP_i (S/dP double-buffered in TMEM) --------------------
   {
-    auto issue_pass1 = [&](int it) {
+    // S (thread 0) and dP (thread 32) of tile `it`: tcgen05.mma holds its
+    // issuing thread while the tensor core works through it, so two issuers
+    // each keep their warp from its share of the sum for half as long
+    auto issue_pass1 = [&](int it, bool dp) {
       constexpr uint32_t idesc = idesc_bf16_f32_major(kRows, kSlots, 0, 0);
-      const uint32_t qa = smem_addr(sm + Layout::Q), ga = smem_addr(sm + Layout::DO);
+      const uint32_t aa = smem_addr(sm + (dp ? Layout::DO : Layout::Q));
       const uint32_t ka = smem_addr(sm + Layout::KV + (it & 1) * 2 * kBlk);
-      const uint32_t cs = (it & 1) * 256;
+      const uint32_t cs = (it & 1) * 256 + (dp ? 128 : 0);
 #pragma unroll
       for (int k = 0; k < kD / 16; ++k) {
         const uint32_t off = (k >> 2) * kBlk + (k & 3) * 32;
-        mma_bf16_ss(tmem + cs, sw128_desc(qa + off), sw128_desc(ka + off), idesc, k > 0);
-        mma_bf16_ss(tmem + cs + 128, sw128_desc(ga + off), sw128_desc(ka + off), idesc, k > 0);
+        mma_bf16_ss(tmem + cs, sw128_desc(aa + off), sw128_desc(ka + off), idesc, k > 0);
       }
       mma_commit(&bar_d1[it & 1]);
     };
@@ -247,9 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       fence_proxy_async_smem();
       fence_before();
       __syncthreads();
-      if (tid == 0) {
+      if (tid == 0 || tid == 32) {
         fence_after();
-        issue_pass1(0);
+        issue_pass1(0, tid == 32);
       }
     }
     for (int it = 0; it < ntiles && ok; ++it) {
@@ -259,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
         fence_proxy_async_smem();
         fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0 || tid == 32) {
           fence_after();
-          issue_pass1(it + 1);
+          issue_pass1(it + 1, tid == 32);
         }
       }
       ok = __syncthreads_and(mbar_wait(&bar_d1[it & 1], (it >> 1) & 1));
