@@ -19,7 +19,8 @@
 //   S = Q K^T, dP = dO V^T                       (K-major A and B)
 //   P as bf16 hi + lo -> smem X, Y;  dKV = P^T dO   (A = P^T and B = dO read
 //                                                  MN-major from the same tiles)
-//   dS*scale as bf16 hi + lo -> X, Y; dKV += dS^T Q; dQ += dS K
+//   dS*scale (computed while the tensor core forms P^T dO) as bf16 hi + lo
+//   -> X, Y; dKV += dS^T Q; dQ += dS K
 //   dKV (summed over the block's heads and queries inside the MMA) is
 //   scattered into the compact buffer with fp32 vector atomics.
 // The hi/lo split carries ~16 significant bits of P and dS into the
@@ -126,7 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
 
   // ---- set-up: barriers, TMEM, Q and dO tiles --------------------------------
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(bar_q + i, 1);
+    mbar_init(bar_q, 1);
+    mbar_init(bar_sp, 1);
+    mbar_init(bar_p, 2);                 // P^T dO: hi and lo parts issued by two threads
+    mbar_init(bar_ds, 1);
     mbar_init(bar_d1, 2);                // pass 1: S and dP issued by two threads
     mbar_init(bar_d1 + 1, 2);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -293,6 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     }
     red[hf * kRows + r] = dpart;
   }
+  // the tile's dKV accumulator starts from zero: every MMA into it accumulates,
+  // so that its hi and lo parts may be issued by two threads in any order
+  {
+    uint32_t z[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) z[c] = 0u;
+    CSA_TMEM_ST32(tDKV, z);
+    tmem_wait_st();
+  }
+  fence_before();
   __syncthreads();
   const float Drow = (red[r] + red[kRows + r]) + (red[2 * kRows + r] + red[3 * kRows + r]);
 
@@ -339,25 +353,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     fence_proxy_async_smem();
     fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0 || tid == 32) {
       fence_after();
-      // dKV = P^T dO: M = slots, N = d, K = rows; A = P^T (MN-major view of X/Y),
-      // B = dO (MN-major view of its K-major tile)
+      // dKV += P^T dO: M = slots, N = d, K = rows; A = P^T (MN-major view of
+      // X for the hi part, issued by thread 0, and of Y for the lo part,
+      // thread 32), B = dO (MN-major view of its K-major tile)
       constexpr uint32_t idesc = idesc_bf16_f32_major(kSlots, kD, 1, 1);
-      const uint32_t xa = smem_addr(X), ya = smem_addr(Y), ga = smem_addr(sm + Layout::DO);
+      const uint32_t pa = smem_addr(tid == 0 ? X : Y), ga = smem_addr(sm + Layout::DO);
 #pragma unroll
-      for (int k = 0; k < kRows / 16; ++k) {
-        const uint64_t b = sw128_desc_mn(ga + k * 2048, kBlk);
-        mma_bf16_ss(tmem + kColDKV, sw128_desc_mn(xa + k * 2048, kBlk), b, idesc, k > 0);
-        mma_bf16_ss(tmem + kColDKV, sw128_desc_mn(ya + k * 2048, kBlk), b, idesc, 1u);
-      }
+      for (int k = 0; k < kRows / 16; ++k)
+        mma_bf16_ss(tmem + kColDKV, sw128_desc_mn(pa + k * 2048, kBlk),
+                    sw128_desc_mn(ga + k * 2048, kBlk), idesc, 1u);
       mma_commit(bar_p);
     }
-    ok = __syncthreads_and(mbar_wait(bar_p, n_p & 1));
-    ++n_p;
-    if (!ok) { site = kSiteBwdP; break; }
-    fence_after();
-    // dS * scale (hi, lo) -> X, Y
+    // dS * scale from P (kept in the S columns) and dP while the tensor core
+    // works on P^T dO; it goes to X, Y once that product has read them
+    float dsv[32];
     {
       uint32_t vs[32], vp[32];
       CSA_TMEM_LD32(tS, vs);
@@ -366,16 +377,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       CSA_TMEM_WAIT32(vs);
       CSA_TMEM_WAIT32(vp);
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        float ds[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;         // vs now holds P
-          ds[e] = __uint_as_float(vs[c]) * (__uint_as_float(vp[c]) - Drow) * scale;
-        }
-        store_hi_lo8(X, Y, sw_off(r, hf * 4 + c8), ds);
-      }
+      for (int c = 0; c < 32; ++c)
+        dsv[c] = __uint_as_float(vs[c]) * (__uint_as_float(vp[c]) - Drow) * scale;
     }
+    ok = __syncthreads_and(mbar_wait(bar_p, n_p & 1));
+    ++n_p;
+    if (!ok) { site = kSiteBwdP; break; }
+    fence_after();
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8)
+      store_hi_lo8(X, Y, sw_off(r, hf * 4 + c8),
+                   *reinterpret_cast<const float(*)[8]>(dsv + c8 * 8));
     if (it + 1 < ntiles) cp_async_wait_group_<0>();
     fence_proxy_async_smem();
     fence_before();
@@ -416,6 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       float* stg = reinterpret_cast<float*>(X);          // [128 slots][128] fp32 = 64 KB
       uint32_t v[32];
       tmem_ld32_wait(tDKV, v);
+      {  // the next tile's dKV accumulates from zero
+        uint32_t z[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) z[c] = 0u;
+        CSA_TMEM_ST32(tDKV, z);
+        tmem_wait_st();
+      }
       float* srow = stg + r * kD + hf * 32;
       // Store chunk (c + lane) % 8 at step c so that the 32 lanes (32 rows,
       // 512 B apart) hit different banks: rotate the eight 4-float chunks by
