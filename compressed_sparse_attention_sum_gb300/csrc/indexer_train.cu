@@ -290,8 +290,10 @@ __device__ __forceinline__ float kl_row(const float* Is, const int* blk, const f
   return block_reduce(loss, red, false);
 }
 
+// Three CTAs per SM (168 registers, a few spilled) beat two at 179 registers:
+// the kernel is bound by the latency of its warp-level MMAs and gathers.
 template <int DI, int HIP>
-__global__ void __launch_bounds__(kTrThreads) student_mma_kernel(
+__global__ void __launch_bounds__(kTrThreads, 3) student_mma_kernel(
     const __nv_bfloat16* __restrict__ q_I, const __nv_bfloat16* __restrict__ k_I,
     const float* __restrict__ w, const int32_t* __restrict__ idx, const float* __restrict__ target,
     float* __restrict__ loss, float* __restrict__ dq_I, float* __restrict__ dk_I,
