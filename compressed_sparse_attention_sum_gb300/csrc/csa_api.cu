@@ -140,6 +140,29 @@ csa_status_t check_attn(const void* q, const void* kv_full, const int32_t* idx, 
   return CSA_OK;
 }
 
+// The indexer's chunk loop: the b*sq query rows go through the workspace in
+// chunks of whole 128-row tiles (all batch elements at once); per chunk, the
+// score kernel `score(ws, t0, nt)` fills the rows' visible scores and the
+// per-row select writes their top-K.  Arguments already validated.
+template <typename ScoreFn>
+csa_status_t indexer_chunks(int b, int sq, int n_c, int ratio, int topk,
+                            const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
+                            void* workspace, size_t workspace_bytes, cudaStream_t s,
+                            ScoreFn score) {
+  const size_t row_bytes = (size_t)b * n_c * sizeof(float);
+  const int K = topk < n_c ? topk : n_c;
+  size_t rows = workspace_bytes / row_bytes;
+  rows = rows / kIndexerTileRows * kIndexerTileRows;
+  if (rows > (size_t)sq) rows = (size_t)sq;
+  for (int t0 = 0; t0 < sq; t0 += (int)rows) {
+    const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;
+    if (score((float*)workspace, t0, nt) != cudaSuccess) return CSA_ERR_CUDA;
+    if (csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq,
+                                n_c, ratio, K, s, doc_ids) != cudaSuccess)
+      return CSA_ERR_CUDA;
+  }
+  return CSA_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -301,35 +324,21 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
     return CSA_ERR_INVALID_ARG;
   if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
   if (d_I > kMaxDI || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
-  const size_t row_bytes = (size_t)b * n_c * sizeof(float);
   if (workspace_bytes < csa_indexer_topk_min_workspace(b, n_c)) return CSA_ERR_WORKSPACE;
-  const int K = topk < n_c ? topk : n_c;
-  cudaStream_t s = (cudaStream_t)stream;
-  // query rows per chunk (all batch elements at once), a multiple of the tile
-  size_t rows = workspace_bytes / row_bytes;
-  rows = rows / kIndexerTileRows * kIndexerTileRows;
-  if (rows > (size_t)sq) rows = (size_t)sq;
   // CSA_INDEXER_CUDA_CORES=1 selects the CUDA-core score kernel for bf16 too
   // (same results up to fp32 summation order; used to compare the two).
   const char* cc = getenv("CSA_INDEXER_CUDA_CORES");
   const bool use_tc = dt == CSA_BF16 && !(cc && cc[0] == '1') &&
                       csa::indexer_tc_supported(H_I, d_I);
   int* status = device_status_ptr();
-  for (int t0 = 0; t0 < sq; t0 += (int)rows) {
-    const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;
-    cudaError_t e;
-    if (use_tc)
-      e = csa::launch_indexer_scores_tc(q_idx, k_idx, w, (float*)workspace, t0, nt, b, sq, n_c,
-                                        H_I, d_I, ratio, status, s);
-    else
-      e = csa::launch_indexer_scores_simt(q_idx, k_idx, w, (float*)workspace, t0, nt, b, sq, n_c,
-                                          H_I, d_I, ratio, dt == CSA_BF16, s);
-    if (e != cudaSuccess) return CSA_ERR_CUDA;
-    e = csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq, n_c,
-                                ratio, K, s, doc_ids);
-    if (e != cudaSuccess) return CSA_ERR_CUDA;
-  }
-  return CSA_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  return indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
+                        workspace_bytes, s, [&](float* ws, int t0, int nt) {
+    return use_tc ? csa::launch_indexer_scores_tc(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
+                                                  d_I, ratio, status, s)
+                  : csa::launch_indexer_scores_simt(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
+                                                    d_I, ratio, dt == CSA_BF16, s);
+  });
 }
 
 csa_status_t csa_quantize_e4m3(const void* x, long long rows, int d, csa_dtype_t dt,
@@ -360,31 +369,18 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
     return CSA_ERR_INVALID_ARG;
   if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
   if (d_I > kMaxDI || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
-  const size_t row_bytes = (size_t)b * n_c * sizeof(float);
   if (workspace_bytes < csa_indexer_topk_min_workspace(b, n_c)) return CSA_ERR_WORKSPACE;
-  const int K = topk < n_c ? topk : n_c;
-  cudaStream_t s = (cudaStream_t)stream;
-  size_t rows = workspace_bytes / row_bytes;
-  rows = rows / kIndexerTileRows * kIndexerTileRows;
-  if (rows > (size_t)sq) rows = (size_t)sq;
   const char* cc = getenv("CSA_INDEXER_CUDA_CORES");
   const bool use_tc = !(cc && cc[0] == '1') && csa::indexer_tc_fp8_supported(H_I, d_I);
   int* status = device_status_ptr();
-  for (int t0 = 0; t0 < sq; t0 += (int)rows) {
-    const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;
-    cudaError_t e;
-    if (use_tc)
-      e = csa::launch_indexer_scores_tc(q8, k8, w, (float*)workspace, t0, nt, b, sq, n_c, H_I,
-                                        d_I, ratio, status, s, q_scale, k_scale);
-    else
-      e = csa::launch_indexer_scores_simt_fp8(q8, q_scale, k8, k_scale, w, (float*)workspace, t0,
-                                              nt, b, sq, n_c, H_I, d_I, ratio, s);
-    if (e != cudaSuccess) return CSA_ERR_CUDA;
-    e = csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq, n_c,
-                                ratio, K, s, doc_ids);
-    if (e != cudaSuccess) return CSA_ERR_CUDA;
-  }
-  return CSA_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  return indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
+                        workspace_bytes, s, [&](float* ws, int t0, int nt) {
+    return use_tc ? csa::launch_indexer_scores_tc(q8, k8, w, ws, t0, nt, b, sq, n_c, H_I, d_I,
+                                                  ratio, status, s, q_scale, k_scale)
+                  : csa::launch_indexer_scores_simt_fp8(q8, q_scale, k8, k_scale, w, ws, t0, nt,
+                                                        b, sq, n_c, H_I, d_I, ratio, s);
+  });
 }
 
 csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx,
