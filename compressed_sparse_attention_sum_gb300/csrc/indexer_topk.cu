@@ -270,13 +270,13 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
 // the remaining count ends the search early: every key with the selected
 // prefix is taken and no tie needs breaking.
 template <int PER, bool DOC>
-__global__ void __launch_bounds__(256) topk_select_reg_kernel(const float* __restrict__ ws,
+__global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __restrict__ ws,
                                                               int32_t* __restrict__ out_idx,
                                                               float* __restrict__ out_score,
                                                               int t0, int nt, int b, int sq,
                                                               int n_c, int ratio, int K,
                                                               const int32_t* __restrict__ doc) {
-  __shared__ int hist_all[8][256];
+  __shared__ int hist_all[4][256];
   const int warps = blockDim.x / 32;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
@@ -453,13 +453,13 @@ cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_s
                                const int32_t* doc) {
   const int rows = b * nt;
   if (n_c <= 2048) {
-    const unsigned grid = (unsigned)((rows + 7) / 8);
+    const unsigned grid = (unsigned)((rows + 3) / 4);   // 4 rows (warps) per CTA
 #define CSA_SEL(P)                                                                            \
   if (doc)                                                                                    \
-    topk_select_reg_kernel<P, true><<<grid, 256, 0, s>>>(ws, topk_idx, topk_score, t0, nt, b, \
+    topk_select_reg_kernel<P, true><<<grid, 128, 0, s>>>(ws, topk_idx, topk_score, t0, nt, b, \
                                                          sq, n_c, ratio, K, doc);             \
   else                                                                                        \
-    topk_select_reg_kernel<P, false><<<grid, 256, 0, s>>>(ws, topk_idx, topk_score, t0, nt,   \
+    topk_select_reg_kernel<P, false><<<grid, 128, 0, s>>>(ws, topk_idx, topk_score, t0, nt,   \
                                                           b, sq, n_c, ratio, K, nullptr);     \
   count_launches(1);
     if (n_c <= 256) { CSA_SEL(8) }
