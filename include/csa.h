@@ -10,6 +10,12 @@
  *                     rows + per-head sink; returns O and LSE
  *   csa_attn_bwd      dQ, dKV, dSink, accumulated in fp32
  *
+ * Further calls: packed documents (the doc_ids argument of the indexer and
+ * the attention), the indexer's training path (csa_indexer_teacher,
+ * csa_indexer_loss), overlapping compression (csa_compress_overlap and its
+ * backward), an FP8 indexer (csa_quantize_e4m3, csa_indexer_topk_fp8) and an
+ * indexer that needs no caller workspace (csa_indexer_topk_noalloc).
+ *
  * Sources (page title, section):
  *   "Add unfused SBHD compressed sparse attention" (Megatron-LM PR #6400):
  *     compressor review, causal compressed mask, indexer / top-k block,
