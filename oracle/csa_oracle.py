@@ -42,7 +42,12 @@ the design notes of the repository):
   * top-k ties go to the lower block index; output ascending, -1 tail;
   * an index j is padding when j < 0, j >= n_c or j >= vis(t);
   * a repeated index is two separate softmax terms;
-  * LSE = natural log including the sink; sink absent = -inf.
+  * LSE = natural log including the sink; sink absent = -inf;
+  * overlapping compression: coff counts the ratio-blocks an entry pools,
+    ending with its own block (coff = 1 is the non-overlapping compressor the
+    compressor review names);
+  * FP8 indexer: per-row e4m3 codes with scale absmax / 448 (the pages list
+    indexer quantization only as not yet included).
 
 All functions take and return numpy arrays; floating results are float64.
 """
@@ -52,7 +57,7 @@ import numpy as np
 
 __all__ = [
     "round_to_storage", "round_bf16",
-    "visible_blocks", "compress", "compress_bwd",
+    "visible_blocks", "pooling_window", "compress", "compress_bwd",
     "indexer_selectable", "indexer_scores", "indexer_scores_row", "topk_select", "topk_select_row",
     "query_slots", "attn_fwd_query", "attn_fwd", "attn_bwd_query", "attn_bwd",
     "selected_entries", "indexer_teacher_row", "indexer_teacher",
