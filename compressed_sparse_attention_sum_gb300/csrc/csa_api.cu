@@ -4,10 +4,12 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/csa.h"
 #include "csa_common.cuh"
 #include "csa_kernels.h"
+#include "indexer_host.h"
 
 namespace csa {
 // kernels defined in the other translation units
@@ -87,26 +89,33 @@ static __device__ int g_csa_device_status[2] = {0, 0};
 
 namespace {
 
-constexpr int kMaxD = 512;
-constexpr int kMaxH = 64;
-constexpr int kMaxNc = 16384;
-constexpr int kMaxDI = 256;
 constexpr size_t kDefaultIndexerWorkspace = 128ull << 20;  // stays resident in L2
-constexpr int kIndexerTileRows = 128;
+using csa::aligned16;
+using csa::kMaxD;
+using csa::kMaxDI;
+using csa::kMaxH;
+using csa::kMaxNc;
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Device address of the current device's status word.  Host code cannot hand
+// g_csa_device_status to a kernel (on the host the name is only a stand-in
+// for the device symbol), so the address is looked up once per device, with
+// that device current, and cached.  The cache is guarded: two host threads
+// may make their first call at the same time.  It is not refreshed after a
+// cudaDeviceReset of that device.
+std::mutex g_status_mutex;
+int* g_status_ptrs[64] = {nullptr};
 
 int* device_status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  static int* ptrs[64] = {nullptr};
   if (dev < 0 || dev >= 64) return nullptr;
-  if (ptrs[dev] == nullptr) {
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  if (g_status_ptrs[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_csa_device_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
+    g_status_ptrs[dev] = static_cast<int*>(p);
   }
-  return ptrs[dev];
+  return g_status_ptrs[dev];
 }
 
 }  // namespace
@@ -140,29 +149,6 @@ csa_status_t check_attn(const void* q, const void* kv_full, const int32_t* idx, 
   return CSA_OK;
 }
 
-// The indexer's chunk loop: the b*sq query rows go through the workspace in
-// chunks of whole 128-row tiles (all batch elements at once); per chunk, the
-// score kernel `score(ws, t0, nt)` fills the rows' visible scores and the
-// per-row select writes their top-K.  Arguments already validated.
-template <typename ScoreFn>
-csa_status_t indexer_chunks(int b, int sq, int n_c, int ratio, int topk,
-                            const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
-                            void* workspace, size_t workspace_bytes, cudaStream_t s,
-                            ScoreFn score) {
-  const size_t row_bytes = (size_t)b * n_c * sizeof(float);
-  const int K = topk < n_c ? topk : n_c;
-  size_t rows = workspace_bytes / row_bytes;
-  rows = rows / kIndexerTileRows * kIndexerTileRows;
-  if (rows > (size_t)sq) rows = (size_t)sq;
-  for (int t0 = 0; t0 < sq; t0 += (int)rows) {
-    const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;
-    if (score((float*)workspace, t0, nt) != cudaSuccess) return CSA_ERR_CUDA;
-    if (csa::launch_topk_select((const float*)workspace, topk_idx, topk_score, t0, nt, b, sq,
-                                n_c, ratio, K, s, doc_ids) != cudaSuccess)
-      return CSA_ERR_CUDA;
-  }
-  return CSA_OK;
-}
 }  // namespace
 
 extern "C" {
@@ -294,7 +280,7 @@ csa_status_t csa_compress_overlap_bwd(const void* kv, long long kv_batch_stride,
 
 size_t csa_indexer_topk_min_workspace(int b, int n_c) {
   if (b < 1 || n_c < 1) return 0;
-  return (size_t)b * kIndexerTileRows * (size_t)n_c * sizeof(float);
+  return csa::indexer_min_chunk_bytes(b, n_c);
 }
 
 size_t csa_indexer_topk_workspace_size(int b, int sq, int n_c, int H_I, int d_I, int topk,
@@ -320,20 +306,15 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
   if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
       !aligned16(topk_score) || !aligned16(workspace) || !aligned16(doc_ids))
     return CSA_ERR_INVALID_ARG;
-  if (b < 1 || sq < 1 || H_I < 1 || d_I < 8 || d_I % 8 != 0 || ratio < 1 || topk < 1)
-    return CSA_ERR_INVALID_ARG;
-  if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
-  if (d_I > kMaxDI || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
-  if (workspace_bytes < csa_indexer_topk_min_workspace(b, n_c)) return CSA_ERR_WORKSPACE;
-  // CSA_INDEXER_CUDA_CORES=1 selects the CUDA-core score kernel for bf16 too
-  // (same results up to fp32 summation order; used to compare the two).
-  const char* cc = getenv("CSA_INDEXER_CUDA_CORES");
-  const bool use_tc = dt == CSA_BF16 && !(cc && cc[0] == '1') &&
+  const csa_status_t st = csa::check_indexer_shape(b, sq, n_c, H_I, d_I, ratio, topk, 8);
+  if (st != CSA_OK) return st;
+  if (workspace_bytes < csa::indexer_min_chunk_bytes(b, n_c)) return CSA_ERR_WORKSPACE;
+  const bool use_tc = dt == CSA_BF16 && !csa::indexer_cuda_cores_forced() &&
                       csa::indexer_tc_supported(H_I, d_I);
   int* status = device_status_ptr();
   cudaStream_t s = (cudaStream_t)stream;
-  return indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
-                        workspace_bytes, s, [&](float* ws, int t0, int nt) {
+  return csa::indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
+                             workspace_bytes, s, 0, sq, [&](float* ws, int t0, int nt) {
     return use_tc ? csa::launch_indexer_scores_tc(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
                                                   d_I, ratio, status, s)
                   : csa::launch_indexer_scores_simt(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
@@ -365,17 +346,14 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
       !aligned16(w) || !aligned16(topk_idx) || !aligned16(topk_score) ||
       !aligned16(workspace) || !aligned16(doc_ids))
     return CSA_ERR_INVALID_ARG;
-  if (b < 1 || sq < 1 || H_I < 1 || d_I < 16 || d_I % 16 != 0 || ratio < 1 || topk < 1)
-    return CSA_ERR_INVALID_ARG;
-  if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
-  if (d_I > kMaxDI || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
-  if (workspace_bytes < csa_indexer_topk_min_workspace(b, n_c)) return CSA_ERR_WORKSPACE;
-  const char* cc = getenv("CSA_INDEXER_CUDA_CORES");
-  const bool use_tc = !(cc && cc[0] == '1') && csa::indexer_tc_fp8_supported(H_I, d_I);
+  const csa_status_t st = csa::check_indexer_shape(b, sq, n_c, H_I, d_I, ratio, topk, 16);
+  if (st != CSA_OK) return st;
+  if (workspace_bytes < csa::indexer_min_chunk_bytes(b, n_c)) return CSA_ERR_WORKSPACE;
+  const bool use_tc = !csa::indexer_cuda_cores_forced() && csa::indexer_tc_fp8_supported(H_I, d_I);
   int* status = device_status_ptr();
   cudaStream_t s = (cudaStream_t)stream;
-  return indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
-                        workspace_bytes, s, [&](float* ws, int t0, int nt) {
+  return csa::indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
+                             workspace_bytes, s, 0, sq, [&](float* ws, int t0, int nt) {
     return use_tc ? csa::launch_indexer_scores_tc(q8, k8, w, ws, t0, nt, b, sq, n_c, H_I, d_I,
                                                   ratio, status, s, q_scale, k_scale)
                   : csa::launch_indexer_scores_simt_fp8(q8, q_scale, k8, k_scale, w, ws, t0, nt,

@@ -15,6 +15,10 @@
 // rows do not fit are processed in chunks of query rows; a problem whose
 // smallest chunk (128 query rows of every batch element) does not fit is
 // rejected with CSA_ERR_WORKSPACE before any work is enqueued.
+//
+// It takes no doc_ids: every batch row is one document (the candidates of
+// query t are all blocks j < vis(t)).  Limits, argument checks and the chunk
+// loop are those of csa_indexer_topk (indexer_host.h).
 #include <cstddef>
 #include <cstdlib>
 #include <mutex>
@@ -22,6 +26,7 @@
 #include "../../include/csa.h"
 #include "csa_common.cuh"
 #include "csa_kernels.h"
+#include "indexer_host.h"
 
 namespace csa {
 bool indexer_tc_supported(int H_I, int d_I);
@@ -40,13 +45,15 @@ static __device__ __align__(256) float g_noalloc_scores[CSA_NOALLOC_SCRATCH_BYTE
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kTileRows = 128;
 std::mutex g_setup_mutex;
 float* g_scores_ptr[kMaxDevices] = {nullptr};   // device address of the array, per device
 
 // Host code cannot hand g_noalloc_scores to a kernel directly: on the host
 // that name is only a stand-in for the device symbol.  The device address is
-// looked up once per device (with that device current) and cached.
+// looked up once per device (with that device current) and cached for the
+// life of the process; the cache is not refreshed after a cudaDeviceReset of
+// that device, so a caller that resets a device must not call this entry
+// point on it again.
 float* scratch_for_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -59,8 +66,6 @@ float* scratch_for_current_device() {
   return g_scores_ptr[dev];
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" csa_status_t csa_indexer_topk_noalloc(const void* q_idx, const void* k_idx,
@@ -68,45 +73,34 @@ extern "C" csa_status_t csa_indexer_topk_noalloc(const void* q_idx, const void* 
                                                   float* topk_score, int b, int sq, int n_c,
                                                   int H_I, int d_I, int ratio, int topk,
                                                   csa_dtype_t dt, csa_stream_t stream) {
+  using csa::aligned16;
   if (dt != CSA_FP32 && dt != CSA_BF16) return CSA_ERR_INVALID_ARG;
   if (q_idx == nullptr || k_idx == nullptr || w == nullptr || topk_idx == nullptr)
     return CSA_ERR_INVALID_ARG;
   if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
       !aligned16(topk_score))
     return CSA_ERR_INVALID_ARG;
-  if (b < 1 || sq < 1 || H_I < 1 || d_I < 8 || d_I % 8 != 0 || ratio < 1 || topk < 1)
-    return CSA_ERR_INVALID_ARG;
-  if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
-  if (d_I > 256 || n_c > 16384) return CSA_ERR_UNSUPPORTED;
+  const csa_status_t st = csa::check_indexer_shape(b, sq, n_c, H_I, d_I, ratio, topk, 8);
+  if (st != CSA_OK) return st;
   // the smallest chunk must fit in the fixed scratch
-  const size_t row_bytes = (size_t)b * (size_t)n_c * sizeof(float);
-  if (row_bytes * kTileRows > (size_t)CSA_NOALLOC_SCRATCH_BYTES) return CSA_ERR_WORKSPACE;
+  if (csa::indexer_min_chunk_bytes(b, n_c) > (size_t)CSA_NOALLOC_SCRATCH_BYTES)
+    return CSA_ERR_WORKSPACE;
   float* scratch = scratch_for_current_device();
   if (scratch == nullptr) return CSA_ERR_CUDA;
 
-  size_t rows = (size_t)CSA_NOALLOC_SCRATCH_BYTES / row_bytes;
-  rows = rows / kTileRows * kTileRows;
-  if (rows > (size_t)sq) rows = (size_t)sq;
-  const int K = topk < n_c ? topk : n_c;
-  const char* cc = getenv("CSA_INDEXER_CUDA_CORES");
-  const bool use_tc = dt == CSA_BF16 && !(cc && cc[0] == '1') &&
+  const bool use_tc = dt == CSA_BF16 && !csa::indexer_cuda_cores_forced() &&
                       csa::indexer_tc_supported(H_I, d_I);
+  int* status = csa::device_status_word();
   cudaStream_t s = (cudaStream_t)stream;
   // Every score the select kernel reads is first written by the score kernel
   // of the same chunk, so nothing left in the array by an earlier call is ever
   // read and the array needs no clearing.
-  for (int t0 = 0; t0 < sq; t0 += (int)rows) {
-    const int nt = (sq - t0) < (int)rows ? (sq - t0) : (int)rows;
-    cudaError_t e;
-    if (use_tc)
-      e = csa::launch_indexer_scores_tc(q_idx, k_idx, w, scratch, t0, nt, b, sq, n_c, H_I, d_I,
-                                        ratio, csa::device_status_word(), s);
-    else
-      e = csa::launch_indexer_scores_simt(q_idx, k_idx, w, scratch, t0, nt, b, sq, n_c, H_I, d_I,
-                                          ratio, dt == CSA_BF16, s);
-    if (e != cudaSuccess) return CSA_ERR_CUDA;
-    e = csa::launch_topk_select(scratch, topk_idx, topk_score, t0, nt, b, sq, n_c, ratio, K, s);
-    if (e != cudaSuccess) return CSA_ERR_CUDA;
-  }
-  return CSA_OK;
+  return csa::indexer_chunks(b, sq, n_c, ratio, topk, nullptr, topk_idx, topk_score, scratch,
+                             (size_t)CSA_NOALLOC_SCRATCH_BYTES, s, 0, sq,
+                             [&](float* ws, int t0, int nt) {
+    return use_tc ? csa::launch_indexer_scores_tc(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
+                                                  d_I, ratio, status, s)
+                  : csa::launch_indexer_scores_simt(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
+                                                    d_I, ratio, dt == CSA_BF16, s);
+  });
 }

@@ -295,10 +295,12 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
  * plugin or custom operator inside a framework that owns all device memory
  * and gives it no allocator, a serving loop that must not call cudaMalloc
  * once it runs (cudaMalloc may synchronize the whole device), a C caller
- * with no spare buffer.  This call takes the same arguments as
- * csa_indexer_topk minus the workspace and returns the same results; the
- * score rows it needs live in a fixed array of CSA_NOALLOC_SCRATCH_BYTES in
- * the library's own device memory.
+ * with no spare buffer.  This call takes the arguments of csa_indexer_topk
+ * minus the workspace and minus doc_ids, and returns the results that
+ * csa_indexer_topk returns with doc_ids == NULL: every batch row is one
+ * document (packed-document callers use csa_indexer_topk).  The score rows it
+ * needs live in a fixed array of CSA_NOALLOC_SCRATCH_BYTES in the library's
+ * own device memory.
  *
  *  - Memory: every GPU that loads the library holds the array until the
  *    process exits.  The call allocates nothing (no cudaMalloc, no cudaFree,
@@ -309,7 +311,10 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
  *    work is enqueued.
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress, no allocation) with that device current;
- *    make that first call before any stream capture.
+ *    make that first call before any stream capture.  The address is kept
+ *    for the life of the process and is not looked up again after a
+ *    cudaDeviceReset of that device: do not call this entry point on a
+ *    device after resetting it.
  *  - Sharing: all calls on a device use the same array, which keeps the last
  *    call's scores.  Every value a call reads is written earlier in the same
  *    call, so nothing needs clearing, but two calls whose work overlaps on the
