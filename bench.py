@@ -24,7 +24,6 @@ from __future__ import annotations
 import argparse
 import json
 import math
-import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -44,71 +43,57 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"
 # ---------------------------------------------------------------------------
 # oracle CPU baseline (spawned worker processes, one BLAS thread each)
 # ---------------------------------------------------------------------------
-_W = {}
 
-
-def _worker_init(cfg_name):
-    os.environ["OMP_NUM_THREADS"] = "1"
-    import numpy as np
-    from compressed_sparse_attention_sum_gb300.inputs import CONFIGS, make_inputs
-    from oracle import csa_oracle as orc
-    cfg = CONFIGS[cfg_name]
-    inp = make_inputs(cfg)
-    f = lambda t: t.double().numpy()
-    kv_raw = f(inp["kv_raw"])
-    t0 = time.perf_counter()
-    kv_c = orc.compress(kv_raw, f(inp["score"]), cfg.ratio, out_dtype=cfg.dtype)
-    _W.update(cfg=cfg, orc=orc, np=np, kv_full=np.concatenate([kv_raw, kv_c], axis=1),
-              q_I=f(inp["q_I"]), k_I=f(inp["k_I"]), w=f(inp["w"]), q=f(inp["q"]),
-              sink=f(inp["sink"]), dO=f(inp["dO"]), t_compress=time.perf_counter() - t0)
-
-
-def _worker_rows(ts):
-    """The oracle's work for query rows ts of batch element 0: indexer row,
-    top-k, attention forward, attention backward (with its dKV scatter)."""
-    cfg, orc, np = _W["cfg"], _W["orc"], _W["np"]
-    dkv = np.zeros_like(_W["kv_full"][0])
-    t0 = time.perf_counter()
-    for t in ts:
-        scores = orc.indexer_scores_row(_W["q_I"][0, t], _W["k_I"][0], _W["w"][0, t], t, cfg.ratio)
-        idx = orc.topk_select_row(scores, cfg.K)
-        slots = orc.query_slots(t, idx, cfg.sq, cfg.n_c, cfg.ratio, cfg.window)
-        orc.attn_fwd_query(_W["q"][0, t], _W["kv_full"][0], slots, _W["sink"], cfg.scale)
-        _, dkv_s, _ = orc.attn_bwd_query(_W["q"][0, t], _W["kv_full"][0], slots, _W["sink"],
-                                         cfg.scale, _W["dO"][0, t])
-        np.add.at(dkv, slots, dkv_s)
-    return time.perf_counter() - t0, _W["t_compress"]
+# Query rows of the oracle sample per workload: the whole layer where the
+# oracle finishes it in seconds, else a bounded sample (10-30 s of CPU work).
+CPU_ROWS = {"tiny_fp32": 256, "debug_bf16": 2048, "csa4_bf16": 4096, "hca_bf16": 16384,
+            "prod_bf16": 4096}
 
 
 class OraclePool:
-    """Spawned pool: the oracle runs on every host core, one process per core."""
+    """The oracle on every host core (oracle.rows_pool): one process per core
+    over memory-mapped inputs of one workload."""
 
     def __init__(self, cfg_name, procs=None):
-        self.procs = procs or (os.cpu_count() or 1)
-        os.environ.setdefault("OMP_NUM_THREADS", "1")
-        os.environ["OPENBLAS_NUM_THREADS"] = "1"
-        os.environ["MKL_NUM_THREADS"] = "1"
-        ctx = mp.get_context("spawn")
-        self.pool = ctx.Pool(self.procs, initializer=_worker_init, initargs=(cfg_name,))
-        self.pool.map(_worker_rows, [[0]] * self.procs)   # warm every worker
-
-    def run(self, rows_total, sq, seed):
-        """Time `rows_total` query rows spread evenly over the sequence (the
-        causal mix of short and long rows); returns (seconds, rows)."""
         import numpy as np
-        rng = np.random.default_rng(seed)
-        ts = np.sort(rng.choice(sq, size=rows_total, replace=False))
-        chunks = [ts[i::self.procs].tolist() for i in range(self.procs)]
+        from compressed_sparse_attention_sum_gb300.inputs import CONFIGS, make_inputs
+        from oracle import csa_oracle as orc
+        from oracle.rows_pool import RowPool
+        self.cfg = cfg = CONFIGS[cfg_name]
+        inp = make_inputs(cfg)
+        f = lambda t: t.double().numpy()
+        kv_raw = f(inp["kv_raw"])
         t0 = time.perf_counter()
-        res = self.pool.map(_worker_rows, chunks)
+        kv_c = orc.compress(kv_raw, f(inp["score"]), cfg.ratio, out_dtype=cfg.dtype)
+        self.t_compress = time.perf_counter() - t0          # whole sequence, all batch rows
+        arrays = {"kv_full": np.concatenate([kv_raw, kv_c], axis=1), "q": inp["q"],
+                  "dO": inp["dO"], "sink": inp["sink"].numpy(), "idx": inp.get("idx"),
+                  "q_I": inp.get("q_I"), "k_I": inp.get("k_I"), "w": inp.get("w")}
+        self.pool = RowPool(arrays, procs)
+        self.procs = self.pool.procs
+        self.run(self.procs, seed=12345)                     # warm every worker
+
+    def run(self, rows_total, seed):
+        """Time `rows_total` query rows drawn uniformly over (b, t) (the causal
+        mix of short and long rows); returns (seconds, rows)."""
+        import numpy as np
+        from oracle.rows_pool import split_rows
+        cfg = self.cfg
+        rng = np.random.default_rng(seed)
+        flat = np.sort(rng.choice(cfg.b * cfg.sq, size=min(rows_total, cfg.b * cfg.sq),
+                                  replace=False))
+        rows = [(int(i // cfg.sq), int(i % cfg.sq)) for i in flat]
+        kw = dict(scale=cfg.scale, window=cfg.window, ratio=cfg.ratio, K=cfg.K,
+                  indexer=cfg.H_I > 0)
+        t0 = time.perf_counter()
+        self.pool.map("oracle.rows_pool.layer_rows",
+                      [dict(rows=c, **kw) for c in split_rows(rows, self.procs)])
         wall = time.perf_counter() - t0
-        t_compress = res[0][1]
-        # the pooled rows of the whole sequence are charged pro rata
-        return wall + t_compress * rows_total / sq, rows_total
+        # the pooling of the whole layer is charged pro rata
+        return wall + self.t_compress * len(rows) / (cfg.b * cfg.sq), len(rows)
 
     def close(self):
         self.pool.close()
-        self.pool.join()
 
 
 # ---------------------------------------------------------------------------
@@ -250,7 +235,24 @@ def max_over_ranks(value_ms, world, device=None):
     return float(t.item())
 
 
-def run_gpu(args, rank, world, local_rank):
+def workload_string(cfg):
+    s = (f"{cfg.name}: b={cfg.b} sq={cfg.sq} H={cfg.H} d={cfg.d} ratio={cfg.ratio} "
+         f"n_c={cfg.n_c} window={cfg.window}")
+    if cfg.H_I > 0:
+        s += f" topk={cfg.topk} H_I={cfg.H_I} d_I={cfg.d_I}"
+    if cfg.index_source == "all_visible":
+        s += " (no indexer: every visible block, K=n_c)"
+    elif cfg.index_source == "zipf":
+        s += (f" (attention on synthetic Zipf-{cfg.zipf_exponent} top-{cfg.K} lists with "
+              f"{int(cfg.pad_fraction * 100)}% -1 padding; the indexer runs on its own inputs)")
+    return s
+
+
+def median(xs):
+    return statistics.median(xs)
+
+
+def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_on=True):
     import torch
     from compressed_sparse_attention_sum_gb300 import build as _build
     _build.build()
@@ -259,16 +261,21 @@ def run_gpu(args, rank, world, local_rank):
     lib = csa.load_library()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    cfg = rank_config(CONFIGS[args.workload], rank, world)
+    cfg = rank_config(CONFIGS[workload or args.workload], rank, world)
     inp = make_inputs(cfg)
     host = {k: v.pin_memory() for k, v in inp.items()}
     d_in = {k: v.to(dev) for k, v in inp.items()}
     b, sq, d, n_c, H = cfg.b, cfg.sq, cfg.d, cfg.n_c, cfg.H
+    has_indexer = cfg.H_I > 0
+    # the attention's index list: the indexer's output, or the workload's own
+    # list (every visible block; synthetic Zipf lists)
+    idx_given = "idx" in d_in
     kv_full = torch.empty(b, sq + n_c, d, dtype=cfg.torch_dtype, device=dev)
-    ws = torch.empty(csa.csa_indexer_topk_workspace_size(b, sq, n_c, cfg.H_I, cfg.d_I, cfg.topk,
-                                                          cfg.torch_dtype), dtype=torch.uint8,
-                     device=dev)
-    idx = torch.empty(b, sq, cfg.K, dtype=torch.int32, device=dev)
+    ws = (torch.empty(csa.csa_indexer_topk_workspace_size(b, sq, n_c, cfg.H_I, cfg.d_I, cfg.topk,
+                                                           cfg.torch_dtype), dtype=torch.uint8,
+                      device=dev) if has_indexer else None)
+    idx_out = torch.empty(b, sq, cfg.K, dtype=torch.int32, device=dev)
+    idx = d_in["idx"] if idx_given else idx_out
     O = torch.empty(b, sq, H, d, dtype=cfg.torch_dtype, device=dev)
     L = torch.empty(b, sq, H, dtype=torch.float32, device=dev)
     dq = torch.empty(b, sq, H, d, dtype=torch.float32, device=dev)
@@ -300,15 +307,17 @@ def run_gpu(args, rank, world, local_rank):
         ev[1].record(side)
         csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:], stream=side)
         ev[2].record(side)
-        csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio, workspace=ws,
-                             out_idx=idx, doc_ids=doc)
+        if has_indexer:
+            csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio, workspace=ws,
+                                 out_idx=idx_out, doc_ids=doc)
         ev[3].record(stream)
         stream.wait_event(ev[2])
         ev[4].record(stream)
-        csa.csa_attn_fwd(x["q"], kv_full, idx, x["sink"], cfg.scale, cfg.ratio, cfg.window, out=O,
+        ix = x["idx"] if idx_given else idx_out
+        csa.csa_attn_fwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio, cfg.window, out=O,
                          lse=L, doc_ids=doc)
         ev[5].record(stream)
-        csa.csa_attn_bwd(x["q"], kv_full, idx, x["sink"], cfg.scale, cfg.ratio, cfg.window, O, L,
+        csa.csa_attn_bwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio, cfg.window, O, L,
                          x["dO"], dq=dq, dkv=dkv, dsink=dsink, doc_ids=doc)
         ev[6].record(stream)
         # the compressed rows' gradient flows back through the pooling into the
@@ -351,7 +360,7 @@ def run_gpu(args, rank, world, local_rank):
         torch.distributed.barrier()
     seg = [list(c) for c in zip(*[segments(e) for e in evs])]
     step_ms = [step_time(e) for e in evs]
-    ms = sum(step_ms) / len(step_ms)
+    ms = median(step_ms)
     ms_max = max_over_ranks(ms, world, dev)
     queries = b * sq
     value = world * queries / (ms_max / 1e3)
@@ -359,7 +368,7 @@ def run_gpu(args, rank, world, local_rank):
     # ---- variants (skipped with --no-variants) ----------------------------------
     variants = {}
     names = ("compress", "indexer_topk", "attn_fwd", "attn_bwd", "compress_bwd")
-    if not args.no_variants:
+    if variants_on and not args.no_variants and has_indexer and not idx_given:
         # the same layer holding 4 packed documents (window and indexer restricted
         # to each query's document; same timing rules)
         doc = packed_doc_ids(b, sq, cfg.ratio, 4, seed=rank).to(dev)
@@ -371,13 +380,13 @@ def run_gpu(args, rank, world, local_rank):
             flush_l2()
             evs_doc.append(step(d_in, doc))
         torch.cuda.synchronize()
-        doc_ms = max_over_ranks(sum(step_time(e) for e in evs_doc) / len(evs_doc),
+        doc_ms = max_over_ranks(median([step_time(e) for e in evs_doc]),
                                 world, dev)
         variants["docs4"] = {
             "workload": f"{cfg.name} with 4 packed documents (boundaries on multiples of the ratio)",
             "ms_per_step": round(doc_ms, 4), "value": round(world * queries / (doc_ms / 1e3), 1),
             "unit": "queries/s",
-            "kernels_ms": {n: round(sum(segments(e)[i] for e in evs_doc) / len(evs_doc),
+            "kernels_ms": {n: round(median([segments(e)[i] for e in evs_doc]),
                                     4) for i, n in enumerate(names)},
         }
         # the indexer's training path on the same layer: teacher target from the
@@ -397,8 +406,8 @@ def run_gpu(args, rank, world, local_rank):
             if i >= args.warmup:
                 tr_ev.append(e3)
         torch.cuda.synchronize()
-        t_teach = sum(e[0].elapsed_time(e[1]) for e in tr_ev) / len(tr_ev)
-        t_loss = sum(e[1].elapsed_time(e[2]) for e in tr_ev) / len(tr_ev)
+        t_teach = median([e[0].elapsed_time(e[1]) for e in tr_ev])
+        t_loss = median([e[1].elapsed_time(e[2]) for e in tr_ev])
         slots_sel = int((idx >= 0).sum().item())
         variants["indexer_training"] = {
             "workload": f"{cfg.name}: indexer distillation over the top-{cfg.K} entries",
@@ -428,8 +437,8 @@ def run_gpu(args, rank, world, local_rank):
             if i >= args.warmup:
                 f8_ev.append(e3)
         torch.cuda.synchronize()
-        t_q = sum(e[0].elapsed_time(e[1]) for e in f8_ev) / len(f8_ev)
-        t_i8 = sum(e[1].elapsed_time(e[2]) for e in f8_ev) / len(f8_ev)
+        t_q = median([e[0].elapsed_time(e[1]) for e in f8_ev])
+        t_i8 = median([e[1].elapsed_time(e[2]) for e in f8_ev])
         hit = torch.zeros(b, sq, n_c + 1, dtype=torch.int32, device=dev)
         hit.scatter_(2, torch.where(idx >= 0, idx, n_c).long(), 1)
         hit[:, :, n_c] = 0
@@ -437,7 +446,7 @@ def run_gpu(args, rank, world, local_rank):
         variants["indexer_fp8"] = {
             "workload": f"{cfg.name}: indexer top-{cfg.K} on per-row e4m3 codes of q_I and k_I",
             "quantize_ms": round(t_q, 4), "indexer_topk_ms": round(t_i8, 4),
-            "indexer_topk_bf16_ms": round(sum(seg[1]) / len(seg[1]), 4),
+            "indexer_topk_bf16_ms": round(median(seg[1]), 4),
             "topk_overlap_with_bf16": round(kept / max(1, int((idx >= 0).sum().item())), 5),
             "kernels": "quantize: a lane group per row; scores: tcgen05 kind::f8f6f4, same select",
         }
@@ -460,86 +469,99 @@ def run_gpu(args, rank, world, local_rank):
         torch.cuda.synchronize()
         variants["compress_overlap"] = {
             "workload": f"{cfg.name}: compressor with coff = 2 (windows of 2 x ratio tokens)",
-            "compress_ms": round(sum(e[0].elapsed_time(e[1]) for e in ov_ev) / len(ov_ev), 4),
-            "compress_bwd_ms": round(sum(e[1].elapsed_time(e[2]) for e in ov_ev) / len(ov_ev), 4),
-            "coff1_compress_ms": round(sum(seg[0]) / len(seg[0]), 4),
-            "coff1_compress_bwd_ms": round(sum(seg[4]) / len(seg[4]), 4),
+            "compress_ms": round(median([e[0].elapsed_time(e[1]) for e in ov_ev]), 4),
+            "compress_bwd_ms": round(median([e[1].elapsed_time(e[2]) for e in ov_ev]), 4),
+            "coff1_compress_ms": round(median(seg[0]), 4),
+            "coff1_compress_bwd_ms": round(median(seg[4]), 4),
         }
 
     # ---- end-to-end through host buffers -------------------------------------
     # Every step copies all of its inputs host -> device (pinned) and all of its
     # results device -> host.  Three streams pipeline consecutive steps: step
     # i+1's inputs arrive while step i computes and step i-1's results leave;
-    # inputs and results are double-buffered.  Each step moves 137.6 MB in,
-    # which is larger than L2, so no flush is added here.
-    def make_out():
-        return {"idx": torch.empty_like(idx), "O": torch.empty_like(O), "L": torch.empty_like(L),
-                "dq": torch.empty_like(dq), "dkv": torch.empty_like(dkv),
-                "dsink": torch.empty_like(dsink), "dscore": torch.empty_like(dscore)}
-    d_out = [make_out(), make_out()]
-    d_e2e = [{k: torch.empty_like(v) for k, v in d_in.items()} for _ in range(2)]
-    out_host = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in o.items()}
-                for o in d_out]
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = sum(v.numel() * v.element_size() for v in d_out[0].values())
-    s_in = torch.cuda.Stream(dev)
-    s_out = torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_comp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    # inputs and results are double-buffered.  Each step moves more bytes in
+    # than L2 holds (137.6 MB at CSA-4), so no flush is added here.
+    e2e_res = None
+    if e2e_on:
+        def make_out():
+            o = {"O": torch.empty_like(O), "L": torch.empty_like(L), "dq": torch.empty_like(dq),
+                 "dkv": torch.empty_like(dkv), "dsink": torch.empty_like(dsink),
+                 "dscore": torch.empty_like(dscore)}
+            if has_indexer:
+                o["idx"] = torch.empty_like(idx_out)
+            return o
+        d_out = [make_out(), make_out()]
+        d_e2e = [{k: torch.empty_like(v) for k, v in d_in.items()} for _ in range(2)]
+        out_host = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                     for n, t in o.items()} for o in d_out]
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in d_out[0].values())
+        s_in = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step(i):
-        sl = i & 1
-        x, y = d_e2e[sl], d_out[sl]
-        with torch.cuda.stream(s_in):
+        def e2e_step(i):
+            sl = i & 1
+            x, y = d_e2e[sl], d_out[sl]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[sl])          # inputs of slot free again
+                for k in host:
+                    x[k].copy_(host[k], non_blocking=True)
+                ev_in[sl].record(s_in)
+            stream.wait_event(ev_in[sl])
             if i >= 2:
-                s_in.wait_event(ev_comp[sl])          # inputs of slot free again
-            for k in host:
-                x[k].copy_(host[k], non_blocking=True)
-            ev_in[sl].record(s_in)
-        stream.wait_event(ev_in[sl])
-        if i >= 2:
-            stream.wait_event(ev_out[sl])             # results of slot read back
-        kv_full[:, :sq].copy_(x["kv_raw"])
-        csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:])
-        csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio, workspace=ws,
-                             out_idx=y["idx"])
-        csa.csa_attn_fwd(x["q"], kv_full, y["idx"], x["sink"], cfg.scale, cfg.ratio, cfg.window,
-                         out=y["O"], lse=y["L"])
-        csa.csa_attn_bwd(x["q"], kv_full, y["idx"], x["sink"], cfg.scale, cfg.ratio, cfg.window,
-                         y["O"], y["L"], x["dO"], dq=y["dq"], dkv=y["dkv"], dsink=y["dsink"])
-        csa.csa_compress_bwd(kv_full[:, :sq], x["score"], cfg.ratio, y["dkv"][:, sq:],
-                             y["dkv"][:, :sq], dscore=y["dscore"])
-        ev_comp[sl].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_comp[sl])
-            for n in y:
-                out_host[sl][n].copy_(y[n], non_blocking=True)
-            ev_out[sl].record(s_out)
+                stream.wait_event(ev_out[sl])             # results of slot read back
+            kv_full[:, :sq].copy_(x["kv_raw"])
+            csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:])
+            if has_indexer:
+                csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio,
+                                     workspace=ws, out_idx=y["idx"])
+            ix = x["idx"] if idx_given else y["idx"]
+            csa.csa_attn_fwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio, cfg.window,
+                             out=y["O"], lse=y["L"])
+            csa.csa_attn_bwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio, cfg.window,
+                             y["O"], y["L"], x["dO"], dq=y["dq"], dkv=y["dkv"], dsink=y["dsink"])
+            csa.csa_compress_bwd(kv_full[:, :sq], x["score"], cfg.ratio, y["dkv"][:, sq:],
+                                 y["dkv"][:, :sq], dscore=y["dscore"])
+            ev_comp[sl].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[sl])
+                for n in y:
+                    out_host[sl][n].copy_(y[n], non_blocking=True)
+                ev_out[sl].record(s_out)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(s_in)
-    for i in range(args.warmup, args.warmup + args.steps):
-        e2e_step(i)
-    t_end.record(s_out)
-    torch.cuda.synchronize()
-    e2e_ms = [t_start.elapsed_time(t_end) / args.steps]
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(s_in)
+        for i in range(args.warmup, args.warmup + args.steps):
+            e2e_step(i)
+        t_end.record(s_out)
+        torch.cuda.synchronize()
+        e2e = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world, dev)
+        e2e_res = {"value": round(world * queries / (e2e / 1e3), 1), "unit": "queries/s",
+                   "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h,
+                   "method": "pinned host buffers; every step copies all inputs in and all "
+                             "results out; copy-in / compute / copy-out streams pipelined "
+                             "across steps"}
     clk.__exit__(None, None, None)
-    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world, dev)
 
     # ---- roofline ---------------------------------------------------------------
     peaks = load_peaks()
     traffic = load_traffic()
-    k_ms = {n: sum(s) / len(s) for n, s in zip(("compress", "indexer_topk", "attn_fwd",
-                                                  "attn_bwd", "compress_bwd"), seg)}
+    names = ("compress", "indexer_topk", "attn_fwd", "attn_bwd", "compress_bwd")
+    k_ms = {n: median(s) for n, s in zip(names, seg)}
+    if not has_indexer:
+        del k_ms["indexer_topk"]
     per = {
         "compress": ("hbm", work["compress_bytes"] / (k_ms["compress"] / 1e3) / 1e9,
                      peaks["hbm_gbs"], "GB/s"),
-        "indexer_topk": ("tensor", work["indexer_flops"] / (k_ms["indexer_topk"] / 1e3) / 1e12,
-                         peaks["bf16_tflops"], "TFLOP/s"),
         "attn_fwd": ("hbm", work["fwd_gathered_bytes"] / (k_ms["attn_fwd"] / 1e3) / 1e9,
                      peaks["hbm_gbs"], "GB/s"),
         "attn_bwd": ("hbm", work["bwd_gathered_bytes"] / (k_ms["attn_bwd"] / 1e3) / 1e9,
@@ -547,43 +569,49 @@ def run_gpu(args, rank, world, local_rank):
         "compress_bwd": ("hbm", work["compress_bwd_bytes"] / (k_ms["compress_bwd"] / 1e3) / 1e9,
                          peaks["hbm_gbs"], "GB/s"),
     }
+    if has_indexer:
+        per["indexer_topk"] = ("tensor",
+                               work["indexer_flops"] / (k_ms["indexer_topk"] / 1e3) / 1e12,
+                               peaks["bf16_tflops"], "TFLOP/s")
     kernels = {}
-    for n, (bound, ach, peak, unit) in per.items():
+    for n in names:
+        if n not in per:
+            continue
+        bound, ach, peak, unit = per[n]
         kernels[n] = {"ms": round(k_ms[n], 4), "share": round(k_ms[n] / ms, 4), "bound": bound,
                       "achieved": round(ach, 2), "peak": peak, "unit": unit,
                       "frac": round(ach / peak, 4)}
-    kernels["attn_fwd"]["tflops"] = round(work["fwd_flops"] / (k_ms["attn_fwd"] / 1e3) / 1e12, 2)
-    kernels["attn_bwd"]["tflops"] = round(work["bwd_flops"] / (k_ms["attn_bwd"] / 1e3) / 1e12, 2)
+    # the attention's contraction, against the sustained bf16 peak (a kernel
+    # timed inside a long step)
+    for n, key in (("attn_fwd", "fwd_flops"), ("attn_bwd", "bwd_flops")):
+        tf = work[key] / (k_ms[n] / 1e3) / 1e12
+        kernels[n]["tflops"] = round(tf, 2)
+        kernels[n]["tensor_frac_sustained"] = round(tf / peaks["bf16_tflops_sustained"], 4)
     dom = max(k_ms, key=k_ms.get)
     bound, ach, peak, unit = per[dom]
-    tr = traffic.get(dom)
+    tr = traffic.get(f"{dom}@{cfg.name}") or (traffic.get(dom) if cfg.name == WORKLOAD else None)
     roofline = {"kernel": dom, "bound": bound, "achieved": round(ach, 2), "peak": peak,
                 "unit": unit, "frac": round(ach / peak, 4),
                 "traffic": tr["dram_bytes_per_launch"] if tr else None,
                 "peak_source": peaks["source"]}
     attn_ms = k_ms["attn_fwd"] + k_ms["attn_bwd"]
     attn_gb = (work["fwd_gathered_bytes"] + work["bwd_gathered_bytes"]) / (attn_ms / 1e3) / 1e9
-    targets = {
-        "indexer_tensor_frac": kernels["indexer_topk"]["frac"],
-        "attn_fwd_bwd_hbm_frac": round(attn_gb / peaks["hbm_gbs"], 4),
-    }
+    targets = {"attn_fwd_bwd_hbm_frac": round(attn_gb / peaks["hbm_gbs"], 4)}
+    if has_indexer:
+        targets["indexer_tensor_frac"] = kernels["indexer_topk"]["frac"]
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: b={cfg.b} sq={sq} H={H} d={d} ratio={cfg.ratio} "
-                               f"n_c={n_c} window={cfg.window} topk={cfg.topk} H_I={cfg.H_I} "
-                               f"d_I={cfg.d_I}",
+        "config": {"workload": workload_string(cfg),
                    "global_batch": world * b, "seq_len": sq,
                    "parallelism": "replicas" if world == 1 else f"dp{world} (independent layers)",
                    "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)"},
         "ms_per_layer": round(ms_max, 4),
-        "e2e": {"value": round(world * queries / (e2e / 1e3), 1), "unit": "queries/s",
-                "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "method": "pinned host buffers; every step copies all inputs in and all results "
-                          "out; copy-in / compute / copy-out streams pipelined across steps"},
+        "step_stat": f"median of {args.steps} timed steps",
+        "e2e": e2e_res,
         "roofline": roofline,
         "kernels": kernels,
         "targets": targets,
@@ -599,43 +627,56 @@ def run_cpu_baseline(cfg_name, rows, seed=0):
     cfg = CONFIGS[cfg_name]
     pool = OraclePool(cfg_name)
     try:
-        sec, n = pool.run(rows, cfg.sq, seed)
+        sec, n = pool.run(rows, seed)
     finally:
         pool.close()
+    what = ("indexer scores + top-k + " if cfg.H_I > 0 else "") + "attention fwd + bwd"
+    if cfg.index_source == "zipf":
+        what += " (attention on the workload's Zipf lists)"
     return {"value": round(n / sec, 2), "unit": "queries/s", "cores": pool.procs,
             "kind": "oracle",
-            "sample": f"{n} of {cfg.b * cfg.sq} query rows of {cfg_name} (uniform over t), each "
-                      "row: indexer scores + top-k + attention fwd + bwd in fp64; pooling of the "
-                      "whole sequence charged pro rata; one process per host core"}
+            "sample": f"{n} of {cfg.b * cfg.sq} query rows of {cfg_name} (uniform over b, t), "
+                      f"each row: {what} in fp64; pooling of the whole layer charged pro rata; "
+                      "one process per host core"}
+
+
+# Query rows per step of the reference arm, per workload.
+REF_ROWS = {"tiny_fp32": 256, "debug_bf16": 1024, "csa4_bf16": 1024, "hca_bf16": 2048,
+            "prod_bf16": 256}
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the fp64 oracle on the host cores."""
+    """The reference arm: the fp64 oracle on the host cores.  Each step is a
+    bounded sample of the workload's query rows (drawn uniformly over b and t);
+    `value` is those rows over the measured time, `ms_per_step` the measured
+    time of one sampled step."""
     from compressed_sparse_attention_sum_gb300.inputs import CONFIGS
     cfg = CONFIGS[args.workload]
+    rows = args.ref_rows or REF_ROWS.get(args.workload, 256)
     pool = OraclePool(args.workload)
     try:
         for i in range(args.warmup):
-            pool.run(args.ref_rows, cfg.sq, seed=100 + i)
+            pool.run(rows, seed=100 + i)
         times = []
         for i in range(args.steps):
-            sec, n = pool.run(args.ref_rows, cfg.sq, seed=i)
-            times.append(sec * cfg.sq / n)       # seconds per full layer (extrapolated)
+            sec, n = pool.run(rows, seed=i)
+            times.append(sec)
     finally:
         pool.close()
-    ms = 1e3 * sum(times) / len(times)
-    value = cfg.b * cfg.sq / (ms / 1e3)
-    sample = (f"{args.ref_rows} of {cfg.b * cfg.sq} query rows per step (uniform over t), "
-              "fp64 oracle, one process per host core; ms_per_step extrapolated to the full layer")
+    ms = 1e3 * median(times)
+    value = n / (ms / 1e3)
+    sample = (f"{n} of {cfg.b * cfg.sq} query rows per step (uniform over b, t), fp64 oracle, "
+              "one process per host core; ms_per_step is the measured time of one such step")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "queries/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: b={cfg.b} sq={cfg.sq} H={cfg.H} d={cfg.d} "
-                               f"ratio={cfg.ratio} n_c={cfg.n_c} window={cfg.window} "
-                               f"topk={cfg.topk} H_I={cfg.H_I} d_I={cfg.d_I}",
-                   "global_batch": cfg.b, "seq_len": cfg.sq, "parallelism": "host cores"},
+        "config": {"workload": workload_string(cfg), "global_batch": cfg.b, "seq_len": cfg.sq,
+                   "parallelism": "replicas",
+                   "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)"},
+        "ms_per_layer_extrapolated": round(ms * cfg.b * cfg.sq / n, 2),
+        "step_stat": f"median of {args.steps} timed steps",
         "cpu_baseline": {"value": round(value, 2), "unit": "queries/s", "cores": pool.procs,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "queries/s", "h2d_bytes_per_step": 0,
@@ -650,13 +691,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--cpu-rows", type=int, default=4096,
-                    help="query rows of the oracle CPU baseline sample")
-    ap.add_argument("--ref-rows", type=int, default=1024,
-                    help="query rows per step of the reference arm")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="query rows of the oracle CPU baseline sample (0: per-workload default)")
+    ap.add_argument("--ref-rows", type=int, default=0,
+                    help="query rows per step of the reference arm (0: per-workload default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the packed-documents and indexer-training timings")
+                    help="skip the packed-documents, indexer-training, FP8 and overlap timings")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every workload (one JSON line each, no variants, no e2e)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -666,15 +710,25 @@ def main():
             return
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return
+    if args.sweep:
+        from compressed_sparse_attention_sum_gb300.inputs import CONFIG_ORDER
+        for name in CONFIG_ORDER:
+            cpu = None
+            if not args.no_cpu_baseline:
+                cpu = run_cpu_baseline(name, args.cpu_rows or CPU_ROWS.get(name, 1024))
+            res = run_gpu(args, 0, 1, local_rank, workload=name, variants_on=False, e2e_on=False)
+            res["cpu_baseline"] = cpu
+            print(json.dumps(res), flush=True)
+        return
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle pool is spawned before the first GPU call
-        cpu = run_cpu_baseline(args.workload, args.cpu_rows)
+        cpu = run_cpu_baseline(args.workload, args.cpu_rows or CPU_ROWS.get(args.workload, 1024))
     if world > 1:
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    res = run_gpu(args, rank, world, local_rank)
+    res = run_gpu(args, rank, world, local_rank, e2e_on=not args.no_e2e)
     res["cpu_baseline"] = cpu
     if world > 1:
         import torch

@@ -1,9 +1,10 @@
 """GPU parity of the four CSA entry points against the fp64 oracle, on the
 five seeded workloads, through the C ABI (Python binding).
 
-Full-size comparisons where the oracle finishes in seconds; on the
-production-width workload (b=2, sq=8192, H=64, d=512) sampled rows that the
-oracle computes one by one, plus identities that hold at any size.
+Full-size comparisons: the oracle finishes the small workloads in seconds,
+and the production-width workload (b=2, sq=8192, H=64, d=512) in about a
+minute on every host core (spawned processes over shared inputs); its
+indexer is checked on sampled rows (its attention runs on synthetic lists).
 Tolerances: max abs error 2e-3 (fp32 inputs) / 2e-2 (bf16 inputs) for O,
 LSE and gradients; top-k sets bit-exact wherever the K-th/(K+1)-th score gap
 exceeds 1e-3 or the boundary is an exact tie (lower index wins).
@@ -170,52 +171,53 @@ def test_attn_fwd_bwd_parity_full(name):
     assert max(errs) <= tol, errs
 
 
-def test_attn_parity_production_sampled():
-    """b=2, sq=8192, H=64, d=512, Zipf-skewed indices with 10% padding: sampled
-    query rows (O, LSE, dq), complete dKV rows (raw rows from their window
-    queries, cold compressed rows from their selecting queries), and two
-    identities that hold at any size."""
+def test_attn_parity_production_full():
+    """b=2, sq=8192, H=64, d=512, Zipf-skewed indices with 10% padding, the
+    whole layer against the oracle: O, LSE and dq of every query row, every
+    row of dKV (raw and compressed, including the hottest Zipf rows, which
+    sum thousands of repeated-index terms in fp32) and dsink.  The oracle runs
+    over all 16384 query rows in spawned processes on every host core
+    (oracle.rows_pool); each process returns the dKV / dsink contributions of
+    its rows, which are summed here in float64."""
+    from oracle.rows_pool import RowPool, split_rows
     cfg, q, kv_full, idx, sink, dO = _attn_inputs("prod_bf16")
     qc, kvc, ic, sc, gc = q.cuda(), kv_full.cuda(), idx.cuda(), sink.cuda(), dO.cuda()
     O, L = csa.csa_attn_fwd(qc, kvc, ic, sc, cfg.scale, cfg.ratio, cfg.window)
     dq, dkv, dsink = csa.csa_attn_bwd(qc, kvc, ic, sc, cfg.scale, cfg.ratio, cfg.window, O, L, gc)
     torch.cuda.synchronize()
-    qn, kvn, idn, sn, gn = f64(q), f64(kv_full), idx.numpy(), f64(sink), f64(dO)
+    assert csa.csa_get_device_status() == 0
+    idn = idx.numpy()
+    arrays = {"q": q, "dO": dO, "kv_full": kv_full, "idx": idn, "sink": sink.numpy(),
+              "O": O.cpu(), "L": L.cpu().numpy(), "dq": dq.cpu().numpy()}
+    del qc, gc
+    rows = [(bi, t) for bi in range(cfg.b) for t in range(cfg.sq)]
+    with RowPool(arrays) as pool:
+        parts = pool.map("oracle.rows_pool.attn_rows_vs",
+                         [dict(rows=r, scale=cfg.scale, window=cfg.window, ratio=cfg.ratio)
+                          for r in split_rows(rows, pool.procs)])
     tol = TOL[cfg.dtype]
-    rng = np.random.default_rng(1)
-    rows = [(int(rng.integers(0, 2)), int(t)) for t in rng.integers(0, cfg.sq, 20)]
-    rows += [(0, 0), (1, cfg.sq - 1), (0, 4095)]
-    O_ref, L_ref = orc.attn_fwd(qn, kvn, idn, sn, cfg.scale, cfg.window, cfg.ratio, rows=rows)
-    bi_l = [r[0] for r in rows]
-    t_l = [r[1] for r in rows]
-    assert maxabs(f64(O[bi_l, t_l]), O_ref) <= tol
-    assert maxabs(f64(L[bi_l, t_l]), L_ref) <= tol
-    dq_ref, _, _ = orc.attn_bwd(qn, kvn, idn, sn, cfg.scale, cfg.window, cfg.ratio, gn, rows=rows)
-    assert maxabs(f64(dq[bi_l, t_l]), dq_ref) <= tol
-    # complete dKV rows: raw row r gets contributions only from queries r..r+W-1
-    for (bi, r) in [(0, 5000), (1, cfg.sq - 1)]:
-        qs = [(bi, t) for t in range(r, min(cfg.sq, r + cfg.window))]
-        _, dkv_part, _ = orc.attn_bwd(qn, kvn, idn, sn, cfg.scale, cfg.window, cfg.ratio, gn,
-                                      rows=qs)
-        assert maxabs(f64(dkv[bi, r]), dkv_part[bi, r]) <= tol
-    # a cold compressed row: every query that selects it
-    for bi in range(2):
-        t_all = np.arange(cfg.sq)
-        vis = (t_all + 1) // cfg.ratio
-        sel = []
-        for j in range(cfg.n_c - 1, 0, -1):
-            sel = np.nonzero(((idn[bi] == j) & (j < vis[:, None])).any(axis=1))[0]
-            if 0 < len(sel) <= 64:
-                break
-        assert 0 < len(sel) <= 64
-        _, dkv_part, _ = orc.attn_bwd(qn, kvn, idn, sn, cfg.scale, cfg.window, cfg.ratio, gn,
-                                      rows=[(bi, int(t)) for t in sel])
-        assert maxabs(f64(dkv[bi, cfg.sq + j]), dkv_part[bi, cfg.sq + j]) <= tol
-    # identity 1 (scaling kv): sum_rows kv.dkv = sum_{t,h} (dO.O + q.dq)
-    lhs = (kv_full.cuda().double() * dkv.double()).sum().item()
-    rhs = ((gc.double() * O.double()).sum() + (qc.double() * dq.double()).sum()).item()
-    assert abs(lhs - rhs) <= 1e-2 * max(1.0, abs(rhs)), (lhs, rhs)
-    # identity 2 (sink gradient): dsink_h = -sum_{b,t} exp(sink_h - LSE) (dO.O)
-    Dh = (gc.double() * O.double()).sum(-1)
-    ds_id = -(torch.exp(sc.double().view(1, 1, -1) - L.double()) * Dh).sum((0, 1))
-    assert maxabs(f64(dsink), f64(ds_id)) <= tol * max(1.0, float(ds_id.abs().max()))
+    e_o = max(p[0] for p in parts)
+    e_l = max(p[1] for p in parts)
+    e_dq = max(p[2] for p in parts)
+    dkv_ref = sum(p[3] for p in parts)
+    ds_ref = sum(p[4] for p in parts)
+    dkv_g = f64(dkv)
+    err_rows = np.abs(dkv_g - dkv_ref).max(axis=2)              # [b, n_kv]
+    e_dkv = float(err_rows.max())
+    e_ds = maxabs(f64(dsink), ds_ref)
+    # the hottest compressed rows: most (query, slot) selections
+    vis = (np.arange(cfg.sq) + 1) // cfg.ratio
+    valid = (idn >= 0) & (idn < vis[None, :, None])
+    counts = np.zeros((cfg.b, cfg.n_c), np.int64)
+    for bi in range(cfg.b):
+        counts[bi] = np.bincount(idn[bi][valid[bi]], minlength=cfg.n_c)
+    hot = np.argsort(counts.ravel())[::-1][:10]
+    print(f"prod_bf16 full: O {e_o:.2e} LSE {e_l:.2e} dq {e_dq:.2e} dkv {e_dkv:.2e} "
+          f"(|dkv|max {np.abs(dkv_ref).max():.1f}) dsink {e_ds:.2e} "
+          f"(|dsink|max {np.abs(ds_ref).max():.1f})")
+    for h in hot:
+        bi, j = divmod(int(h), cfg.n_c)
+        print(f"  hot compressed row b={bi} j={j}: selected {counts[bi, j]} times, "
+              f"|dkv| max {np.abs(dkv_ref[bi, cfg.sq + j]).max():.2f}, "
+              f"err {err_rows[bi, cfg.sq + j]:.2e}")
+    assert max(e_o, e_l, e_dq, e_dkv, e_ds) <= tol, (e_o, e_l, e_dq, e_dkv, e_ds)
