@@ -54,6 +54,7 @@ SIGNATURES = {
                             + [_c_int, _c_p]),
     "csa_indexer_loss": (_c_int, [_c_p] * 9 + [_c_int] * 7 + [_c_int, _c_p]),
     "csa_get_device_status": (_c_int, [_c_p, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
+    "csa_debug_arm_fault": (_c_int, [_c_int]),
 }
 
 
@@ -400,6 +401,13 @@ def csa_get_device_status(stream=None, with_site: bool = False):
     _check("csa_get_device_status", lib.csa_get_device_status(_stream(stream), ctypes.byref(v),
                                                               ctypes.byref(site)))
     return (v.value, site.value) if with_site else v.value
+
+
+def csa_debug_arm_fault(site: int):
+    """Test hook: make later tensor-core attention forwards fake a failure at
+    `site` (0x21: the Q-tile wait runs out; 0x25: the union check trips);
+    0 disarms.  Synchronizes the device."""
+    _check("csa_debug_arm_fault", load_library().csa_debug_arm_fault(int(site)))
 
 
 def csa_indexer_teacher(q: torch.Tensor, kv_full: torch.Tensor, idx: torch.Tensor,

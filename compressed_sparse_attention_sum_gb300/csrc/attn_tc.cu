@@ -105,7 +105,11 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (tid == 0) {
+  // Test hook (csa_debug_arm_fault): with kSiteFwdQ armed the Q tile is never
+  // requested, so the bounded wait on it runs out with nothing in flight;
+  // with kSiteFwdUnion armed the union-size check below trips.
+  const int armed = armed_fault(status);
+  if (tid == 0 && armed != kSiteFwdQ) {
     mbar_expect_tx(bar_q, 2 * kBlk);
     const int row0 = (bi * sq + t0) * H;
     tma_load_2d(sm + Layout::Q, &tmap_q, bar_q, 0, row0);
@@ -138,6 +142,16 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
   // whole CTA (__syncthreads_and), so no thread leaves a barrier loop alone.
   bool ok = __syncthreads_and(mbar_wait(bar_q, 0));
   int site = ok ? 0 : kSiteFwdQ;
+  int code = kDevTimeout;
+  // Device check: the union is a subset of the block's visible blocks, so it
+  // fits the n_c-entry list the shared memory was sized for (the decision is
+  // CTA-uniform: nu and the limit are the same in every thread).
+  const int union_limit = armed == kSiteFwdUnion ? -1 : n_c;
+  if (ok && nu > union_limit) {
+    ok = false;
+    site = kSiteFwdUnion;
+    code = kDevCheck;
+  }
 
   for (int it = 0; it < ntiles && ok; ++it) {
     if (it > 0) {
@@ -298,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
     ok = __syncthreads_and(mbar_wait(bar_o, (ntiles - 1) & 1));
     if (!ok) site = kSiteFwdLast;
   }
-  if (!ok && tid == 0) set_status(status, kDevTimeout, site);
+  if (!ok && tid == 0) set_status(status, code, site);
   fence_after();
   // ---- epilogue: O = O / l, LSE ------------------------------------------------
   lsum[hf * kRows + r] = l_run;

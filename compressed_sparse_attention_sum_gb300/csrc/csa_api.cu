@@ -84,8 +84,10 @@ static std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n); }
 }  // namespace csa
 
-// Device status word (one per device that loads the library).
-static __device__ int g_csa_device_status[2] = {0, 0};
+// Device status word (one per device that loads the library): [0] the first
+// error code, [1] its site, [2] the site of a faked failure armed by
+// csa_debug_arm_fault (0 = none), [3] unused.
+static __device__ int g_csa_device_status[4] = {0, 0, 0, 0};
 
 namespace {
 
@@ -313,6 +315,9 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
                       csa::indexer_tc_supported(H_I, d_I);
   int* status = device_status_ptr();
   cudaStream_t s = (cudaStream_t)stream;
+  if (doc_ids != nullptr &&
+      csa::launch_doc_boundary_check(doc_ids, b, sq, ratio, status, s) != cudaSuccess)
+    return CSA_ERR_CUDA;
   return csa::indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
                              workspace_bytes, s, 0, sq, [&](float* ws, int t0, int nt) {
     return use_tc ? csa::launch_indexer_scores_tc(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
@@ -352,6 +357,9 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
   const bool use_tc = !csa::indexer_cuda_cores_forced() && csa::indexer_tc_fp8_supported(H_I, d_I);
   int* status = device_status_ptr();
   cudaStream_t s = (cudaStream_t)stream;
+  if (doc_ids != nullptr &&
+      csa::launch_doc_boundary_check(doc_ids, b, sq, ratio, status, s) != cudaSuccess)
+    return CSA_ERR_CUDA;
   return csa::indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
                              workspace_bytes, s, 0, sq, [&](float* ws, int t0, int nt) {
     return use_tc ? csa::launch_indexer_scores_tc(q8, k8, w, ws, t0, nt, b, sq, n_c, H_I, d_I,
@@ -465,6 +473,14 @@ csa_status_t csa_indexer_loss(const void* q_idx, const void* k_idx, const float*
   return from_cuda(csa::launch_indexer_loss(q_idx, k_idx, w, idx, target, loss, dq_idx, dk_idx,
                                             dw, b, sq, H_I, d_I, n_c, ratio, K, dt == CSA_BF16,
                                             (cudaStream_t)stream));
+}
+
+csa_status_t csa_debug_arm_fault(int site) {
+  if (site < 0) return CSA_ERR_INVALID_ARG;
+  int* p = device_status_ptr();
+  if (p == nullptr) return CSA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CSA_ERR_CUDA;
+  return from_cuda(cudaMemcpy(p + 2, &site, sizeof(int), cudaMemcpyHostToDevice));
 }
 
 csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out, int* site_out) {

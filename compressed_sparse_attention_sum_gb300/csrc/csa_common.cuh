@@ -28,6 +28,16 @@ __device__ __forceinline__ void set_status(int* status, int code, int site = 0) 
 constexpr int kSiteIdxProducer = 0x11, kSiteIdxMma = 0x12, kSiteIdxEpilogue = 0x13;
 constexpr int kSiteFwdQ = 0x21, kSiteFwdS = 0x22, kSiteFwdO = 0x23, kSiteFwdLast = 0x24;
 constexpr int kSiteBwdQ = 0x31, kSiteBwdS = 0x32, kSiteBwdP = 0x33, kSiteBwdDS = 0x34;
+// Sites recorded with CSA_ERR_DEVICE_CHECK: the tensor-core forward's union
+// of selected blocks larger than its n_c-entry list; a packed document that
+// starts inside a compressed block.
+constexpr int kSiteFwdUnion = 0x25, kSiteDocBoundary = 0x41;
+
+// The status word's third int holds a test hook (csa_debug_arm_fault): the
+// site at which a kernel fakes a failure (0 = none).  Kernels read it once.
+__device__ __forceinline__ int armed_fault(const int* status) {
+  return status != nullptr ? *(volatile const int*)(status + 2) : 0;
+}
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }

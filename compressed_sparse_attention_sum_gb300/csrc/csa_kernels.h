@@ -19,6 +19,11 @@ cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_s
                                int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s,
                                const int32_t* doc = nullptr);
 
+// Record CSA_ERR_DEVICE_CHECK when a packed document starts inside a
+// compressed block (doc [b][sq]).
+cudaError_t launch_doc_boundary_check(const int32_t* doc, int b, int sq, int ratio, int* status,
+                                      cudaStream_t s);
+
 cudaError_t launch_compress_bwd(const void* kv, long long kv_bs, const void* score,
                                 int score_width, const float* g, long long g_bs, float* dkv,
                                 long long dkv_bs, float* dscore, int b, int sq, int d, int ratio,

@@ -448,6 +448,35 @@ cudaError_t launch_indexer_scores_simt_fp8(const uint8_t* q8, const float* q_sca
   return cudaGetLastError();
 }
 
+// Packed documents must start on multiples of the ratio, so that no pooled
+// block mixes two documents ("Refactor Deepseek v4 to use Attention Gym's
+// Compressed Sparse Attention": packing pads every document to a multiple of
+// the compress ratio).  A document id that changes inside a block records
+// CSA_ERR_DEVICE_CHECK at kSiteDocBoundary; the results are still computed
+// under the rule that a block belongs to the document of its first token.
+__global__ void doc_boundary_check_kernel(const int32_t* __restrict__ doc, long long n, int sq,
+                                          int ratio, int* __restrict__ status) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i % sq);
+    if (t % ratio != 0 && __ldg(doc + i) != __ldg(doc + i - 1)) {
+      set_status(status, kDevCheck, kSiteDocBoundary);
+      return;
+    }
+  }
+}
+
+cudaError_t launch_doc_boundary_check(const int32_t* doc, int b, int sq, int ratio, int* status,
+                                      cudaStream_t s) {
+  const long long n = (long long)b * sq;
+  const int threads = 256;
+  const long long want = (n + threads - 1) / threads;
+  const unsigned grid = (unsigned)(want < 1024 ? (want < 1 ? 1 : want) : 1024);
+  doc_boundary_check_kernel<<<grid, threads, 0, s>>>(doc, n, sq, ratio, status);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
                                int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s,
                                const int32_t* doc) {

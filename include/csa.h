@@ -49,9 +49,9 @@
  * CUDA call, so an invalid call has no effect on the device.
  *
  * Errors: the return value covers host-side validation and launch errors.
- * Conditions found on the device (a bounded wait that gave up, a failed
- * bounds check in a checking build) are recorded in a per-device status
- * word, read and cleared by csa_get_device_status().
+ * Conditions found on the device (a bounded wait that gave up, a device
+ * check that failed) are recorded in a per-device status word, read and
+ * cleared by csa_get_device_status().
  */
 #ifndef CSA_H_
 #define CSA_H_
@@ -70,7 +70,7 @@ typedef enum {
   CSA_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed */
   CSA_ERR_WORKSPACE = 4,    /* indexer workspace too small */
   CSA_ERR_TIMEOUT = 5,      /* device: a bounded wait gave up */
-  CSA_ERR_DEVICE_CHECK = 6  /* device: an index or offset check failed */
+  CSA_ERR_DEVICE_CHECK = 6  /* device: a consistency or input check failed */
 } csa_status_t;
 
 typedef enum { CSA_FP32 = 0, CSA_BF16 = 1 } csa_dtype_t;
@@ -450,16 +450,38 @@ csa_status_t csa_indexer_loss(const void* q_idx, const void* k_idx, const float*
  * work on `stream` has finished (this call synchronizes `stream`).
  * *status_out receives CSA_OK, CSA_ERR_TIMEOUT or CSA_ERR_DEVICE_CHECK (the
  * first error recorded since the last read).  site_out (nullable) receives
- * where it was recorded: 0x11-0x13 the indexer's TMA producer, MMA issuer or
- * epilogue waits; 0x21-0x24 the tensor-core attention forward's waits for the
- * Q tile, the score MMA, the PV MMA inside the loop and the last PV MMA;
- * 0x31-0x34 the tensor-core backward's waits for the Q/dO tiles, the S/dP
- * MMAs, the P^T dO MMAs and the dS MMAs.
+ * where it was recorded:
+ *   CSA_ERR_TIMEOUT: 0x11-0x13 the indexer's TMA producer, MMA issuer or
+ *   epilogue waits; 0x21-0x24 the tensor-core attention forward's waits for
+ *   the Q tile, the score MMA, the PV MMA inside the loop and the last PV
+ *   MMA; 0x31-0x34 the tensor-core backward's waits for the Q/dO tiles, the
+ *   S/dP MMAs, the P^T dO MMAs and the dS MMAs.
+ *   CSA_ERR_DEVICE_CHECK: 0x25 the tensor-core forward found the union of a
+ *   query block's selected blocks larger than its n_c-entry list; 0x41 a
+ *   packed document (doc_ids of csa_indexer_topk / csa_indexer_topk_fp8)
+ *   starts inside a compressed block (documents must start on multiples of
+ *   ratio; the results follow the rule that a block belongs to the document
+ *   of its first token).
  * Every device wait of the library is bounded (about one second of wall
  * time); a wait that gives up records CSA_ERR_TIMEOUT here and its CTA skips
- * the rest of its work, so the results of that call are not valid.
+ * the rest of its work, as does a CTA whose check at 0x25 fails, so the
+ * results of that call are not valid.
  */
 csa_status_t csa_get_device_status(csa_stream_t stream, int* status_out, int* site_out);
+
+/*
+ * csa_debug_arm_fault - test hook of the failure-detection paths (not part
+ * of the method; the pages have no counterpart).
+ *
+ * With site = 0x21 every later tensor-core attention forward on the current
+ * device never requests its Q tile, so its bounded wait runs out (about one
+ * second) with no copy or MMA in flight and records CSA_ERR_TIMEOUT at 0x21;
+ * with site = 0x25 its union-size check trips and records
+ * CSA_ERR_DEVICE_CHECK at 0x25.  site = 0 disarms.  The call synchronizes
+ * the device.  Use it only in tests.
+ * Errors: INVALID_ARG for site < 0; CSA_ERR_CUDA if the device is unusable.
+ */
+csa_status_t csa_debug_arm_fault(int site);
 
 #ifdef __cplusplus
 }

@@ -128,8 +128,9 @@ def test_invalid_arguments_rejected_on_host(lib):
                                     None) == UNSUPPORTED
     assert lib.csa_compress_overlap_bwd(fake, 512, fake, 64, fake, 128, None, 512, fake, 1, 8,
                                         64, 4, 2, 1, None) == INVALID
-    # device status needs an output pointer
+    # device status needs an output pointer; the test hook takes no negative site
     assert lib.csa_get_device_status(None, None, None) == INVALID
+    assert lib.csa_debug_arm_fault(-1) == INVALID
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -86,6 +86,11 @@ def test_indexer_docs_small(dtype, H_I, d_I, docs):
     doc = _random_doc_ids(32, b, sq, 3) if docs == "random" else packed_doc_ids(b, sq, ratio, 5)
     idx = csa.csa_indexer_topk(q_I.cuda(), k_I.cuda(), w.cuda(), topk, ratio,
                                doc_ids=doc.cuda()).cpu().numpy()
+    # documents starting inside a block are reported (CSA_ERR_DEVICE_CHECK at
+    # the document-boundary site 0x41); the selection still follows the rule
+    # that a block belongs to the document of its first token
+    status = csa.csa_get_device_status(with_site=True)
+    assert status == ((6, 0x41) if docs == "random" else (0, 0)), status
     I = orc.indexer_scores(f64(q_I), f64(k_I), f64(w), ratio, doc_ids=doc.numpy())
     short = 0
     for bi in range(b):
