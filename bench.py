@@ -1,8 +1,8 @@
 """Benchmark of the CSA hot path on GB300: one step = one CSA layer,
 forward + backward: csa_compress -> csa_indexer_topk -> csa_attn_fwd ->
 csa_attn_bwd -> csa_compress_bwd (the compressed rows' gradient flowing back
-through the pooling), on the CSA-4 workload (b=1, sq=4096, H=32, d=128, ratio 4,
-n_c=1024, window 128, topk 512, indexer 64 heads x 128).
+through the pooling), by default on the CSA-4 workload (b=1, sq=4096, H=32,
+d=128, ratio 4, n_c=1024, window 128, topk 512, indexer 64 heads x 128).
 
 Prints one JSON line.  `value` is queries/s of the whole job (all ranks),
 device-timed with CUDA events around each step on the launching stream; the
@@ -15,9 +15,11 @@ step.  `cpu_baseline` is the fp64 oracle on the host cores over a bounded
 sample of query rows of the same workload.
 
 --impl reference times the oracle itself (the reference arm of this build).
-Multi-GPU: one process per GPU (torchrun); each rank runs its own layer
-(independent batch element), so per-rank work is fixed (weak scaling) and no
-data-path collective exists; timing takes the max over ranks.
+--workload picks one of the five workloads; --sweep times all of them.
+Multi-GPU: one process per GPU (torchrun); the ranks split the layer's query
+rows into contiguous ranges of equal estimated work (row-range calls of the
+library) and sum their dkv / dsink contributions with one all-reduce, so the
+layer is fixed as N grows (strong scaling); timing takes the max over ranks.
 """
 from __future__ import annotations
 
@@ -194,18 +196,24 @@ class ClockSampler:
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def algorithmic_work(cfg, idx):
+def algorithmic_work(cfg, idx, ranges=None):
     """Algorithmic units of one step (valid slots only; MQA rows gathered once
-    per query and shared by the heads)."""
+    per query and shared by the heads); with `ranges`, of those query rows
+    only (the attention and indexer units; the compressor runs whole)."""
     import torch
     sq, ratio, W, d, H = cfg.sq, cfg.ratio, cfg.window, cfg.d, cfg.H
     t = torch.arange(sq, device=idx.device)
+    keep = torch.ones(sq, dtype=torch.bool, device=idx.device)
+    if ranges is not None:
+        keep = torch.zeros_like(keep)
+        for lo, hi in ranges:
+            keep[lo:hi] = True
     vis = ((t + 1) // ratio).view(1, sq, 1)
-    valid_c = ((idx >= 0) & (idx < vis)).sum().item()
-    n_win = cfg.b * int(torch.clamp(t + 1, max=W).sum().item())
+    valid_c = (((idx >= 0) & (idx < vis)) & keep.view(1, sq, 1)).sum().item()
+    n_win = cfg.b * int((torch.clamp(t + 1, max=W) * keep).sum().item())
     slots = valid_c + n_win
     e = 2 if cfg.dtype == "bf16" else 4
-    vis_sum = cfg.b * int(((t + 1) // ratio).clamp(max=cfg.n_c).sum().item())
+    vis_sum = cfg.b * int((((t + 1) // ratio).clamp(max=cfg.n_c) * keep).sum().item())
     return {
         "slots": slots,
         "compress_bytes": cfg.b * (2 * cfg.sq * d + cfg.n_c * d) * e,
@@ -218,11 +226,6 @@ def algorithmic_work(cfg, idx):
         "fwd_flops": 4.0 * d * H * slots,
         "bwd_flops": 10.0 * d * H * slots,
     }
-
-
-def rank_config(cfg, rank, world):
-    """The layer a rank runs: every rank gets its own seeded batch element."""
-    return cfg.with_(seed=cfg.seed + rank) if world > 1 else cfg
 
 
 def max_over_ranks(value_ms, world, device=None):
@@ -261,7 +264,12 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
     lib = csa.load_library()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    cfg = rank_config(CONFIGS[workload or args.workload], rank, world)
+    from compressed_sparse_attention_sum_gb300.shard import config_ranges, layer_rows
+    cfg = CONFIGS[workload or args.workload]
+    # N > 1: the ranks split the layer's query rows (contiguous ranges of equal
+    # estimated work) and sum their dkv / dsink contributions with one
+    # all-reduce; N = 1 runs the whole layer
+    ranges = config_ranges(cfg, world, rank) if world > 1 else None
     inp = make_inputs(cfg)
     host = {k: v.pin_memory() for k, v in inp.items()}
     d_in = {k: v.to(dev) for k, v in inp.items()}
@@ -295,7 +303,17 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
 
     side = torch.cuda.Stream(dev)
 
+    def step_rows(x):
+        # Events 0-6 at the phase boundaries of shard.layer_rows: compress,
+        # indexer, forward, backward, all-reduce, compressor backward.
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        layer_rows(csa, x, cfg, ranges, kv_full, ws, idx_out, O, L, dq, dkv, dsink, dscore,
+                   idx_given, world=world, mark=lambda i: ev[i].record(stream))
+        return ev
+
     def step(x, doc=None):
+        if ranges is not None:
+            return step_rows(x)
         # Events: 0 step start; 1-2 the compressor on the side stream; 3 end of
         # the indexer; 4 both joined (fwd start); 5 fwd end; 6 bwd end; 7 step
         # end.  The compressor and the indexer are independent (the attention
@@ -328,14 +346,19 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
         return ev
 
     # (start, end) events of compress, indexer_topk, attn_fwd, attn_bwd,
-    # compress_bwd, and of the whole step
-    seg_pairs = ((1, 2), (0, 3), (4, 5), (5, 6), (6, 7))
+    # compress_bwd (and the all-reduce of the row split), and of the whole step
+    if ranges is None:
+        seg_pairs = ((1, 2), (0, 3), (4, 5), (5, 6), (6, 7))
+        last = 7
+    else:
+        seg_pairs = ((0, 1), (1, 2), (2, 3), (3, 4), (5, 6), (4, 5))
+        last = 6
 
     def segments(e):
         return [e[a].elapsed_time(e[b]) for a, b in seg_pairs]
 
     def step_time(e):
-        return e[0].elapsed_time(e[7])
+        return e[0].elapsed_time(e[last])
 
     clk = ClockSampler(local_rank)
     clk.__enter__()          # samples from the warm-up through the end-to-end loop
@@ -343,7 +366,7 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
         flush_l2()
         step(d_in)
     torch.cuda.synchronize()
-    work = algorithmic_work(cfg, idx)
+    work = algorithmic_work(cfg, idx, ranges)
 
     # ---- device-timed region -------------------------------------------------
     if world > 1:
@@ -363,12 +386,14 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
     ms = median(step_ms)
     ms_max = max_over_ranks(ms, world, dev)
     queries = b * sq
-    value = world * queries / (ms_max / 1e3)
+    # N = 1: one layer per GPU; N > 1: the ranks share one layer (strong scaling)
+    value = queries / (ms_max / 1e3)
 
     # ---- variants (skipped with --no-variants) ----------------------------------
     variants = {}
     names = ("compress", "indexer_topk", "attn_fwd", "attn_bwd", "compress_bwd")
-    if variants_on and not args.no_variants and has_indexer and not idx_given:
+    if (variants_on and not args.no_variants and has_indexer and not idx_given
+            and ranges is None):
         # the same layer holding 4 packed documents (window and indexer restricted
         # to each query's document; same timing rules)
         doc = packed_doc_ids(b, sq, cfg.ratio, 4, seed=rank).to(dev)
@@ -384,7 +409,7 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
                                 world, dev)
         variants["docs4"] = {
             "workload": f"{cfg.name} with 4 packed documents (boundaries on multiples of the ratio)",
-            "ms_per_step": round(doc_ms, 4), "value": round(world * queries / (doc_ms / 1e3), 1),
+            "ms_per_step": round(doc_ms, 4), "value": round(queries / (doc_ms / 1e3), 1),
             "unit": "queries/s",
             "kernels_ms": {n: round(median([segments(e)[i] for e in evs_doc]),
                                     4) for i, n in enumerate(names)},
@@ -514,18 +539,24 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
             stream.wait_event(ev_in[sl])
             if i >= 2:
                 stream.wait_event(ev_out[sl])             # results of slot read back
-            kv_full[:, :sq].copy_(x["kv_raw"])
-            csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:])
-            if has_indexer:
-                csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio,
-                                     workspace=ws, out_idx=y["idx"])
-            ix = x["idx"] if idx_given else y["idx"]
-            csa.csa_attn_fwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio, cfg.window,
-                             out=y["O"], lse=y["L"])
-            csa.csa_attn_bwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio, cfg.window,
-                             y["O"], y["L"], x["dO"], dq=y["dq"], dkv=y["dkv"], dsink=y["dsink"])
-            csa.csa_compress_bwd(kv_full[:, :sq], x["score"], cfg.ratio, y["dkv"][:, sq:],
-                                 y["dkv"][:, :sq], dscore=y["dscore"])
+            if ranges is not None:
+                layer_rows(csa, x, cfg, ranges, kv_full, ws, y.get("idx", idx_out), y["O"],
+                           y["L"], y["dq"], y["dkv"], y["dsink"], y["dscore"], idx_given,
+                           world=world)
+            else:
+                kv_full[:, :sq].copy_(x["kv_raw"])
+                csa.csa_compress(kv_full[:, :sq], x["score"], cfg.ratio, out=kv_full[:, sq:])
+                if has_indexer:
+                    csa.csa_indexer_topk(x["q_I"], x["k_I"], x["w"], cfg.topk, cfg.ratio,
+                                         workspace=ws, out_idx=y["idx"])
+                ix = x["idx"] if idx_given else y["idx"]
+                csa.csa_attn_fwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio,
+                                 cfg.window, out=y["O"], lse=y["L"])
+                csa.csa_attn_bwd(x["q"], kv_full, ix, x["sink"], cfg.scale, cfg.ratio,
+                                 cfg.window, y["O"], y["L"], x["dO"], dq=y["dq"], dkv=y["dkv"],
+                                 dsink=y["dsink"])
+                csa.csa_compress_bwd(kv_full[:, :sq], x["score"], cfg.ratio, y["dkv"][:, sq:],
+                                     y["dkv"][:, :sq], dscore=y["dscore"])
             ev_comp[sl].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[sl])
@@ -544,7 +575,7 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
         t_end.record(s_out)
         torch.cuda.synchronize()
         e2e = max_over_ranks(t_start.elapsed_time(t_end) / args.steps, world, dev)
-        e2e_res = {"value": round(world * queries / (e2e / 1e3), 1), "unit": "queries/s",
+        e2e_res = {"value": round(queries / (e2e / 1e3), 1), "unit": "queries/s",
                    "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h,
                    "method": "pinned host buffers; every step copies all inputs in and all "
@@ -557,6 +588,7 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
     traffic = load_traffic()
     names = ("compress", "indexer_topk", "attn_fwd", "attn_bwd", "compress_bwd")
     k_ms = {n: median(s) for n, s in zip(names, seg)}
+    allreduce_ms = median(seg[5]) if ranges is not None else None
     if not has_indexer:
         del k_ms["indexer_topk"]
     per = {
@@ -602,14 +634,17 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "queries/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
         "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic",
         "config": {"workload": workload_string(cfg),
-                   "global_batch": world * b, "seq_len": sq,
-                   "parallelism": "replicas" if world == 1 else f"dp{world} (independent layers)",
+                   "global_batch": b, "seq_len": sq,
+                   "parallelism": "replicas" if world == 1 else
+                   f"{world} ranks split the query rows; one all-reduce of dkv and dsink",
                    "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)"},
         "ms_per_layer": round(ms_max, 4),
+        "rows": ranges,
+        "allreduce_ms": None if allreduce_ms is None else round(allreduce_ms, 4),
         "step_stat": f"median of {args.steps} timed steps",
         "e2e": e2e_res,
         "roofline": roofline,
@@ -670,7 +705,7 @@ def run_reference(args, rank, world):
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "queries/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": workload_string(cfg), "global_batch": cfg.b, "seq_len": cfg.sq,
                    "parallelism": "replicas",

@@ -53,6 +53,13 @@ SIGNATURES = {
     "csa_indexer_teacher": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_f, _c_p] + [_c_int] * 7
                             + [_c_int, _c_p]),
     "csa_indexer_loss": (_c_int, [_c_p] * 9 + [_c_int] * 7 + [_c_int, _c_p]),
+    "csa_indexer_topk_rows": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
+                              + [_c_int, _c_p, _c_sz, _c_int, _c_int, _c_p]),
+    "csa_attn_fwd_rows": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p] + [_c_int] * 8
+                          + [_c_int, _c_int, _c_int, _c_p]),
+    "csa_attn_bwd_rows": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_f, _c_p, _c_p, _c_p, _c_p,
+                                   _c_p, _c_p] + [_c_int] * 8 + [_c_int, _c_int, _c_int, _c_int,
+                                                                 _c_p]),
     "csa_get_device_status": (_c_int, [_c_p, ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     "csa_debug_arm_fault": (_c_int, [_c_int]),
 }
@@ -215,13 +222,16 @@ def csa_indexer_topk(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, topk
                      workspace: Optional[torch.Tensor] = None,
                      out_idx: Optional[torch.Tensor] = None,
                      out_score: Optional[torch.Tensor] = None, return_scores: bool = False,
-                     stream=None, doc_ids: Optional[torch.Tensor] = None):
+                     stream=None, doc_ids: Optional[torch.Tensor] = None,
+                     rows: Optional[Tuple[int, int]] = None):
     """Lightning-indexer scores + exact causal top-k.
 
     q_I [b, sq, H_I, d_I], k_I [b, n_c, d_I] (same dtype), w [b, sq, H_I] fp32,
     doc_ids [b, sq] int32 (optional: packed documents, a block is selectable
     only by queries of its own document).  Returns idx [b, sq, K] int32 (and
     the fp32 scores [b, sq, K] when return_scores or out_score is given).
+    rows=(t_begin, t_end): only those query rows of every batch element
+    (csa_indexer_topk_rows); the other rows of the outputs are not written.
     """
     lib = load_library()
     _need(q_I, "q_I")
@@ -244,11 +254,14 @@ def csa_indexer_topk(q_I: torch.Tensor, k_I: torch.Tensor, w: torch.Tensor, topk
         _need(out_score, "out_score", dtype=torch.float32)
     if doc_ids is not None:
         _need(doc_ids, "doc_ids", dtype=torch.int32)
-    _check("csa_indexer_topk", lib.csa_indexer_topk(
-        q_I.data_ptr(), k_I.data_ptr(), w.data_ptr(), _ptr(doc_ids), out_idx.data_ptr(),
-        _ptr(out_score), b, sq,
-        n_c, H_I, d_I, ratio, topk, _dt(q_I), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+    args = (q_I.data_ptr(), k_I.data_ptr(), w.data_ptr(), _ptr(doc_ids), out_idx.data_ptr(),
+            _ptr(out_score), b, sq, n_c, H_I, d_I, ratio, topk, _dt(q_I), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size())
+    if rows is None:
+        _check("csa_indexer_topk", lib.csa_indexer_topk(*args, _stream(stream)))
+    else:
+        _check("csa_indexer_topk_rows", lib.csa_indexer_topk_rows(*args, int(rows[0]),
+                                                                  int(rows[1]), _stream(stream)))
     if out_score is not None:
         return out_idx, out_score
     return out_idx
@@ -320,11 +333,12 @@ def csa_indexer_topk_fp8(q8: torch.Tensor, q_scale: torch.Tensor, k8: torch.Tens
 def csa_attn_fwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Tensor],
                  sink: Optional[torch.Tensor], scale: float, ratio: int, window: int,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                 stream=None, doc_ids: Optional[torch.Tensor] = None
-                 ) -> Tuple[torch.Tensor, torch.Tensor]:
+                 stream=None, doc_ids: Optional[torch.Tensor] = None,
+                 rows: Optional[Tuple[int, int]] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Sparse MQA forward; idx None = every visible compressed block;
     doc_ids [b, sq] int32 (optional) keeps only window rows of the query's
-    own document."""
+    own document.  rows=(t_begin, t_end): only those query rows
+    (csa_attn_fwd_rows)."""
     lib = load_library()
     _need(q, "q")
     _need(kv_full, "kv_full", dtype=q.dtype)
@@ -344,10 +358,13 @@ def csa_attn_fwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Ten
     _need(lse, "lse", dtype=torch.float32)
     if doc_ids is not None:
         _need(doc_ids, "doc_ids", dtype=torch.int32)
-    _check("csa_attn_fwd", lib.csa_attn_fwd(
-        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), _ptr(doc_ids), float(scale),
-        out.data_ptr(),
-        lse.data_ptr(), b, sq, H, d, n_c, ratio, window, K, _dt(q), _stream(stream)))
+    args = (q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), _ptr(doc_ids), float(scale),
+            out.data_ptr(), lse.data_ptr(), b, sq, H, d, n_c, ratio, window, K, _dt(q))
+    if rows is None:
+        _check("csa_attn_fwd", lib.csa_attn_fwd(*args, _stream(stream)))
+    else:
+        _check("csa_attn_fwd_rows", lib.csa_attn_fwd_rows(*args, int(rows[0]), int(rows[1]),
+                                                          _stream(stream)))
     return out, lse
 
 
@@ -356,9 +373,12 @@ def csa_attn_bwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Ten
                  o: torch.Tensor, lse: torch.Tensor, dO: torch.Tensor,
                  dq: Optional[torch.Tensor] = None, dkv: Optional[torch.Tensor] = None,
                  dsink: Optional[torch.Tensor] = None, stream=None,
-                 doc_ids: Optional[torch.Tensor] = None):
+                 doc_ids: Optional[torch.Tensor] = None,
+                 rows: Optional[Tuple[int, int]] = None, accumulate: bool = False):
     """Sparse MQA backward; returns (dq, dkv, dsink) in fp32.  doc_ids as in
-    csa_attn_fwd."""
+    csa_attn_fwd.  rows=(t_begin, t_end): only those query rows
+    (csa_attn_bwd_rows); with accumulate their dkv / dsink contributions are
+    added to what dkv / dsink hold instead of overwriting them."""
     lib = load_library()
     _need(q, "q")
     _need(kv_full, "kv_full", dtype=q.dtype)
@@ -383,11 +403,16 @@ def csa_attn_bwd(q: torch.Tensor, kv_full: torch.Tensor, idx: Optional[torch.Ten
     _need(dkv, "dkv", dtype=torch.float32)
     if doc_ids is not None:
         _need(doc_ids, "doc_ids", dtype=torch.int32)
-    _check("csa_attn_bwd", lib.csa_attn_bwd(
-        q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), _ptr(doc_ids), float(scale),
-        o.data_ptr(),
-        lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dkv.data_ptr(), _ptr(dsink), b, sq, H, d,
-        n_c, ratio, window, K, _dt(q), _stream(stream)))
+    args = (q.data_ptr(), kv_full.data_ptr(), _ptr(idx), _ptr(sink), _ptr(doc_ids), float(scale),
+            o.data_ptr(), lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dkv.data_ptr(),
+            _ptr(dsink), b, sq, H, d, n_c, ratio, window, K, _dt(q))
+    if rows is None and not accumulate:
+        _check("csa_attn_bwd", lib.csa_attn_bwd(*args, _stream(stream)))
+    else:
+        t0, t1 = (0, sq) if rows is None else rows
+        _check("csa_attn_bwd_rows", lib.csa_attn_bwd_rows(*args, int(t0), int(t1),
+                                                          int(bool(accumulate)),
+                                                          _stream(stream)))
     return dq, dkv, dsink
 
 

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MT>::NT) attn_fwd_mma(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kv,
     const int32_t* __restrict__ idx, const float* __restrict__ sink, float scale,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int sq, int H, int n_c, int ratio,
-    int window, int K, const int32_t* __restrict__ doc) {
+    int window, int K, const int32_t* __restrict__ doc, int tb) {
   using C = FwdCfg<D, MT>;
   constexpr int NS = C::NS, LDQ = C::LDQ, LDS = C::LDS, LDP = C::LDP, NT = C::NT, NW = C::NW;
   constexpr int NQ = NS / 32;      // n8-tiles per warp in the score phase
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MT>::NT) attn_fwd_mma(
   int* rows = reinterpret_cast<int*>(smem + C::OFF_ROWS);
   __shared__ int s_count;
 
-  const int t = blockIdx.x, bi = blockIdx.y, h0 = blockIdx.z * C::ROWS;
+  const int t = tb + (int)blockIdx.x, bi = blockIdx.y, h0 = blockIdx.z * C::ROWS;
   const int tid = threadIdx.x, w = tid / 32, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
   const int n_kv = sq + n_c;
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
     const __nv_bfloat16* __restrict__ o, const float* __restrict__ lse,
     const __nv_bfloat16* __restrict__ dO, float* __restrict__ dq, float* __restrict__ dkv,
     float* __restrict__ dsink, int sq, int H, int n_c, int ratio, int window, int K,
-    const int32_t* __restrict__ doc) {
+    const int32_t* __restrict__ doc, int tb) {
   using C = BwdCfg<D, MT>;
   constexpr int NS = C::NS, LDQ = C::LDQ, LDP = C::LDP, NT = C::NT;
   constexpr int NQ = NS / 32;
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
   int* rows = reinterpret_cast<int*>(smem + C::OFF_ROWS);
   __shared__ int s_count;
 
-  const int t = blockIdx.x, bi = blockIdx.y, h0 = blockIdx.z * C::ROWS;
+  const int t = tb + (int)blockIdx.x, bi = blockIdx.y, h0 = blockIdx.z * C::ROWS;
   const int tid = threadIdx.x, w = tid / 32, lane = tid & 31;
   const int g = lane >> 2, cq = lane & 3;
   const int n_kv = sq + n_c;
@@ -562,15 +562,16 @@ __global__ void __launch_bounds__(BwdCfg<D, MT>::NT) attn_bwd_mma(
 template <int D, int MT>
 static cudaError_t run_fwd(const void* q, const void* kv, const int32_t* idx, const float* sink,
                            float scale, void* o, float* lse, int b, int sq, int H, int n_c,
-                           int ratio, int window, int K, cudaStream_t s, const int32_t* doc) {
+                           int ratio, int window, int K, cudaStream_t s, const int32_t* doc,
+                           int tb, int te) {
   using C = FwdCfg<D, MT>;
   const size_t smem = C::OFF_ROWS + (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   auto k = attn_fwd_mma<D, MT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)sq, (unsigned)b, (unsigned)((H + C::ROWS - 1) / C::ROWS));
+  dim3 grid((unsigned)(te - tb), (unsigned)b, (unsigned)((H + C::ROWS - 1) / C::ROWS));
   k<<<grid, C::NT, smem, s>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
-                              (__nv_bfloat16*)o, lse, sq, H, n_c, ratio, window, K, doc);
+                              (__nv_bfloat16*)o, lse, sq, H, n_c, ratio, window, K, doc, tb);
     count_launches(1);
   return cudaGetLastError();
 }
@@ -579,16 +580,17 @@ template <int D, int MT>
 static cudaError_t run_bwd(const void* q, const void* kv, const int32_t* idx, const float* sink,
                            float scale, const void* o, const float* lse, const void* dO, float* dq,
                            float* dkv, float* dsink, int b, int sq, int H, int n_c, int ratio,
-                           int window, int K, cudaStream_t s, const int32_t* doc) {
+                           int window, int K, cudaStream_t s, const int32_t* doc, int tb,
+                           int te) {
   using C = BwdCfg<D, MT>;
   const size_t smem = C::OFF_ROWS + (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   auto k = attn_bwd_mma<D, MT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)sq, (unsigned)b, (unsigned)((H + C::ROWS - 1) / C::ROWS));
+  dim3 grid((unsigned)(te - tb), (unsigned)b, (unsigned)((H + C::ROWS - 1) / C::ROWS));
   k<<<grid, C::NT, smem, s>>>((const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
                               (const __nv_bfloat16*)o, lse, (const __nv_bfloat16*)dO, dq, dkv,
-                              dsink, sq, H, n_c, ratio, window, K, doc);
+                              dsink, sq, H, n_c, ratio, window, K, doc, tb);
     count_launches(1);
   return cudaGetLastError();
 }
@@ -604,10 +606,11 @@ bool attn_mma_supported(int H, int d, int window, int K) {
 cudaError_t launch_attn_fwd_mma(const void* q, const void* kv, const int32_t* idx,
                                 const float* sink, float scale, void* o, float* lse, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s, const int32_t* doc) {
+                                cudaStream_t s, const int32_t* doc, int tb, int te) {
   const int mt = (H + 15) / 16;
-#define CSA_FWD(DD, MM) \
-  return run_fwd<DD, MM>(q, kv, idx, sink, scale, o, lse, b, sq, H, n_c, ratio, window, K, s, doc)
+#define CSA_FWD(DD, MM)                                                                      \
+  return run_fwd<DD, MM>(q, kv, idx, sink, scale, o, lse, b, sq, H, n_c, ratio, window, K, s, \
+                         doc, tb, te)
   switch (d) {
     case 64:
       if (mt <= 1) CSA_FWD(64, 1);
@@ -631,11 +634,11 @@ cudaError_t launch_attn_bwd_mma(const void* q, const void* kv, const int32_t* id
                                 const float* sink, float scale, const void* o, const float* lse,
                                 const void* dO, float* dq, float* dkv, float* dsink, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s, const int32_t* doc) {
+                                cudaStream_t s, const int32_t* doc, int tb, int te) {
   const int mt = (H + 15) / 16;
 #define CSA_BWD(DD, MM)                                                                       \
   return run_bwd<DD, MM>(q, kv, idx, sink, scale, o, lse, dO, dq, dkv, dsink, b, sq, H, n_c, \
-                         ratio, window, K, s, doc)
+                         ratio, window, K, s, doc, tb, te)
   switch (d) {
     case 64:
       if (mt <= 1) CSA_BWD(64, 1);

@@ -27,9 +27,9 @@ __global__ void __launch_bounds__(128) attn_fwd_simt(const T* __restrict__ q,
                                                      T* __restrict__ o, float* __restrict__ lse,
                                                      int sq, int H, int d, int n_c, int ratio,
                                                      int window, int K,
-                                                     const int32_t* __restrict__ doc) {
+                                                     const int32_t* __restrict__ doc, int tb) {
   extern __shared__ int rows[];
-  const int t = blockIdx.x, bi = blockIdx.y;
+  const int t = tb + (int)blockIdx.x, bi = blockIdx.y;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int n_kv = sq + n_c;
   __shared__ int s_count;
@@ -89,9 +89,9 @@ __global__ void __launch_bounds__(128) attn_bwd_simt(
     const float* __restrict__ sink, float scale, const T* __restrict__ o,
     const float* __restrict__ lse, const T* __restrict__ dO, float* __restrict__ dq,
     float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H, int d, int n_c, int ratio,
-    int window, int K, const int32_t* __restrict__ doc) {
+    int window, int K, const int32_t* __restrict__ doc, int tb) {
   extern __shared__ int rows[];
-  const int t = blockIdx.x, bi = blockIdx.y;
+  const int t = tb + (int)blockIdx.x, bi = blockIdx.y;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int n_kv = sq + n_c;
   __shared__ int s_count;
@@ -158,18 +158,19 @@ __global__ void __launch_bounds__(128) attn_bwd_simt(
 cudaError_t launch_attn_fwd_simt(const void* q, const void* kv, const int32_t* idx,
                                  const float* sink, float scale, void* o, float* lse, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s, const int32_t* doc) {
-  dim3 grid((unsigned)sq, (unsigned)b);
+                                 bool bf16, cudaStream_t s, const int32_t* doc, int tb, int te) {
+  dim3 grid((unsigned)(te - tb), (unsigned)b);
   const size_t smem = (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   if (bf16) {
     attn_fwd_simt<__nv_bfloat16><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale, (__nv_bfloat16*)o,
-        lse, sq, H, d, n_c, ratio, window, K, doc);
+        lse, sq, H, d, n_c, ratio, window, K, doc, tb);
     count_launches(1);
   } else {
     attn_fwd_simt<float><<<grid, 32 * kSimtWarps, smem, s>>>((const float*)q, (const float*)kv,
                                                              idx, sink, scale, (float*)o, lse, sq,
-                                                             H, d, n_c, ratio, window, K, doc);
+                                                             H, d, n_c, ratio, window, K, doc,
+                                                             tb);
     count_launches(1);
   }
   return cudaGetLastError();
@@ -179,19 +180,19 @@ cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* i
                                  const float* sink, float scale, const void* o, const float* lse,
                                  const void* dO, float* dq, float* dkv, float* dsink, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s, const int32_t* doc) {
-  dim3 grid((unsigned)sq, (unsigned)b);
+                                 bool bf16, cudaStream_t s, const int32_t* doc, int tb, int te) {
+  dim3 grid((unsigned)(te - tb), (unsigned)b);
   const size_t smem = (size_t)(window + (idx ? K : n_c) + 32) * sizeof(int);
   if (bf16) {
     attn_bwd_simt<__nv_bfloat16><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)kv, idx, sink, scale,
         (const __nv_bfloat16*)o, lse, (const __nv_bfloat16*)dO, dq, dkv, dsink, sq, H, d, n_c,
-        ratio, window, K, doc);
+        ratio, window, K, doc, tb);
     count_launches(1);
   } else {
     attn_bwd_simt<float><<<grid, 32 * kSimtWarps, smem, s>>>(
         (const float*)q, (const float*)kv, idx, sink, scale, (const float*)o, lse,
-        (const float*)dO, dq, dkv, dsink, sq, H, d, n_c, ratio, window, K, doc);
+        (const float*)dO, dq, dkv, dsink, sq, H, d, n_c, ratio, window, K, doc, tb);
     count_launches(1);
   }
   return cudaGetLastError();

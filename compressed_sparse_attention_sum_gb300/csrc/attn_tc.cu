@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __nv_bfloat16* __restrict__ kv,
     const int32_t* __restrict__ idx, const float* __restrict__ sink, float scale,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int sq, int H, int n_c, int ratio,
-    int window, int K, int* __restrict__ status, const int32_t* __restrict__ doc) {
+    int window, int K, int* __restrict__ status, const int32_t* __restrict__ doc, int tb, int te) {
   constexpr int NW = (QB + 3) / 4;               // u64 count words per block id
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -87,8 +87,8 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bi, xb;
-  heavy_first_block((sq + QB - 1) / QB, &bi, &xb);
-  const int t0 = xb * QB;
+  heavy_first_block((te - tb + QB - 1) / QB, &bi, &xb);
+  const int t0 = tb + xb * QB;       // rows t0 .. t0+QB-1 below te are this block's queries
   const int n_kv = sq + n_c;
   const __nv_bfloat16* kv_b = kv + (long long)bi * n_kv * kD;
 
@@ -117,8 +117,9 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
   }
 
   // ---- union of the block's selected compressed blocks ----------------------
-  const int t_last = min(t0 + QB, sq) - 1;
-  const int nu = build_union<QB, kThreads>(idx, bi, sq, K, t0, ratio, n_c, cnt, ulist, wsum, scal);
+  const int t_last = min(t0 + QB, te) - 1;
+  const int nu = build_union<QB, kThreads>(idx, bi, sq, K, t0, te, ratio, n_c, cnt, ulist, wsum,
+                                           scal);
   const int win0 = max(0, t0 - window + 1);
   const int nwin = t_last - win0 + 1;
   const int S_total = nwin + nu;
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
   const int r = qd * 32 + lane;              // row = TMEM lane
   const int q = r / H, h = r % H;
   const int t = t0 + q;
-  const bool row_ok = t < sq;
+  const bool row_ok = t < te;
   const float sc2 = scale * kLog2e;
   float m_run = (row_ok && sink != nullptr) ? sink[h] * kLog2e : -INFINITY;
   // the sink's unit mass is carried by the partial sum of column half 0
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
       const int s = sbase + c;
       const int tq = t0 + qq;
       float bv = -INFINITY;
-      if (tq < sq) {
+      if (tq < te) {
         if (s < nwin) {
           const int raw = win0 + s;
           if (raw <= tq && raw > tq - window &&
@@ -382,7 +383,7 @@ bool attn_tc_supported(int H, int d, int n_c, int K) {
 cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx,
                                const float* sink, float scale, void* o, float* lse, int b, int sq,
                                int H, int n_c, int ratio, int window, int K, int* status,
-                               cudaStream_t s, const int32_t* doc) {
+                               cudaStream_t s, const int32_t* doc, int tb, int te) {
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   CUtensorMap tq;
@@ -396,14 +397,14 @@ cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx
     return cudaErrorInvalidValue;
   const int QB = 128 / H;
   const size_t smem = attn_tc_smem(QB, n_c);
-  dim3 grid((unsigned)(((sq + QB - 1) / QB) * b));   // heaviest blocks first
+  dim3 grid((unsigned)(((te - tb + QB - 1) / QB) * b));   // heaviest blocks first
 #define CSA_TC_FWD(QQ)                                                                          \
   {                                                                                             \
     auto k = atc::attn_fwd_tc_kernel<QQ>;                                                       \
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);           \
     k<<<grid, atc::kThreads, smem, s>>>(tq, (const __nv_bfloat16*)kv, idx, sink, scale,       \
                                         (__nv_bfloat16*)o, lse, sq, H, n_c, ratio, window, K, \
-                                        status, doc);                                           \
+                                        status, doc, tb, te);                                   \
     count_launches(1);                                                                          \
   }
   if (QB == 8) CSA_TC_FWD(8)

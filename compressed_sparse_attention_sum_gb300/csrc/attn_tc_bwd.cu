@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     const float* __restrict__ sink, float scale, const __nv_bfloat16* __restrict__ o,
     const float* __restrict__ lse, float* __restrict__ dq, float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H,
     int n_c, int ratio, int window, int K, int* __restrict__ status,
-    const int32_t* __restrict__ doc) {
+    const int32_t* __restrict__ doc, int tb, int te) {
   constexpr int NW = (QB + 3) / 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -119,8 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int bi, xb;
-  heavy_first_block((sq + QB - 1) / QB, &bi, &xb);
-  const int t0 = xb * QB;
+  heavy_first_block((te - tb + QB - 1) / QB, &bi, &xb);
+  const int t0 = tb + xb * QB;       // rows t0 .. t0+QB-1 below te are this block's queries
   const int n_kv = sq + n_c;
   const __nv_bfloat16* kv_b = kv + (long long)bi * n_kv * kD;
   float* dkv_b = dkv + (long long)bi * n_kv * kD;
@@ -151,8 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   }
 
   // ---- union of the block's selected compressed blocks ----------------------
-  const int t_last = min(t0 + QB, sq) - 1;
-  const int nu = build_union<QB, kThreads>(idx, bi, sq, K, t0, ratio, n_c, cnt, ulist, wsum, scal);
+  const int t_last = min(t0 + QB, te) - 1;
+  const int nu = build_union<QB, kThreads>(idx, bi, sq, K, t0, te, ratio, n_c, cnt, ulist, wsum,
+                                           scal);
   const int win0 = max(0, t0 - window + 1);
   const int nwin = t_last - win0 + 1;
   const int S_total = nwin + nu;
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       const int s = sbase + c;
       const int tq = t0 + qq;
       float bv = -INFINITY;
-      if (tq < sq) {
+      if (tq < te) {
         if (s < nwin) {
           const int raw = win0 + s;
           if (raw <= tq && raw > tq - window &&
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   const int r = qd * 32 + lane;                    // TMEM lane: row (S, dP, dQ) or slot (dKV)
   const int q = r / H, h = r % H;
   const int t = t0 + q;
-  const bool row_ok = t < sq;
+  const bool row_ok = t < te;
   const float sc2 = scale * kLog2e;
   const float lse2 = row_ok ? lse[(long long)(bi * sq + t0) * H + r] * kLog2e : INFINITY;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
@@ -556,13 +557,13 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
                                const void* dO,
                                float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
                                int ratio, int window, int K, int* status, cudaStream_t s,
-                               const int32_t* doc) {
+                               const int32_t* doc, int tb, int te) {
   CUtensorMap tq, tg;
   const long long rows = (long long)b * sq * H;
   if (!make_rows_map(&tq, q, rows) || !make_rows_map(&tg, dO, rows)) return cudaErrorInvalidValue;
   const int QB = 128 / H;
   const size_t smem = attn_tc_bwd_smem(QB, n_c);
-  dim3 grid((unsigned)(((sq + QB - 1) / QB) * b));   // heaviest blocks first
+  dim3 grid((unsigned)(((te - tb + QB - 1) / QB) * b));   // heaviest blocks first
 #define CSA_TC_BWD(QQ)                                                                        \
   {                                                                                           \
     auto k = atb::attn_bwd_tc_kernel<QQ>;                                                     \
@@ -570,7 +571,7 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
     k<<<grid, atb::kThreads, smem, s>>>(tq, tg, (const __nv_bfloat16*)kv,                   \
                                         (const __nv_bfloat16*)dO, idx, sink, scale,           \
                                         (const __nv_bfloat16*)o, lse, dq, dkv, dsink, sq, H,  \
-                                        n_c, ratio, window, K, status, doc);                  \
+                                        n_c, ratio, window, K, status, doc, tb, te);          \
     count_launches(1);                                                                        \
   }
   if (QB == 8) CSA_TC_BWD(8)

@@ -40,29 +40,29 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
                                const void* dO,
                                float* dq, float* dkv, float* dsink, int b, int sq, int H, int n_c,
                                int ratio, int window, int K, int* status, cudaStream_t s,
-                               const int32_t* doc);
+                               const int32_t* doc, int tb, int te);
 cudaError_t launch_attn_fwd_tc(const void* q, const void* kv, const int32_t* idx,
                                const float* sink, float scale, void* o, float* lse, int b, int sq,
                                int H, int n_c, int ratio, int window, int K, int* status,
-                               cudaStream_t s, const int32_t* doc);
+                               cudaStream_t s, const int32_t* doc, int tb, int te);
 cudaError_t launch_attn_fwd_mma(const void* q, const void* kv, const int32_t* idx,
                                 const float* sink, float scale, void* o, float* lse, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s, const int32_t* doc);
+                                cudaStream_t s, const int32_t* doc, int tb, int te);
 cudaError_t launch_attn_bwd_mma(const void* q, const void* kv, const int32_t* idx,
                                 const float* sink, float scale, const void* o, const float* lse,
                                 const void* dO, float* dq, float* dkv, float* dsink, int b, int sq,
                                 int H, int d, int n_c, int ratio, int window, int K,
-                                cudaStream_t s, const int32_t* doc);
+                                cudaStream_t s, const int32_t* doc, int tb, int te);
 cudaError_t launch_attn_fwd_simt(const void* q, const void* kv, const int32_t* idx,
                                  const float* sink, float scale, void* o, float* lse, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s, const int32_t* doc);
+                                 bool bf16, cudaStream_t s, const int32_t* doc, int tb, int te);
 cudaError_t launch_attn_bwd_simt(const void* q, const void* kv, const int32_t* idx,
                                  const float* sink, float scale, const void* o, const float* lse,
                                  const void* dO, float* dq, float* dkv, float* dsink, int b,
                                  int sq, int H, int d, int n_c, int ratio, int window, int K,
-                                 bool bf16, cudaStream_t s, const int32_t* doc);
+                                 bool bf16, cudaStream_t s, const int32_t* doc, int tb, int te);
 bool indexer_teacher_mma_ok(int H, int d);
 bool indexer_loss_mma_ok(int H_I, int d_I);
 size_t indexer_teacher_smem(bool mma, int H, int d, int K);
@@ -133,6 +133,11 @@ namespace {
 csa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
 bool valid_dtype(csa_dtype_t dt) { return dt == CSA_FP32 || dt == CSA_BF16; }
+
+// The query rows [tb, te) of every batch element (0 <= tb < te <= sq).
+csa_status_t check_rows(int sq, int t_begin, int t_end) {
+  return (t_begin < 0 || t_end > sq || t_begin >= t_end) ? CSA_ERR_INVALID_ARG : CSA_OK;
+}
 
 // Shared validation of the attention calls.
 csa_status_t check_attn(const void* q, const void* kv_full, const int32_t* idx, float scale,
@@ -296,11 +301,11 @@ size_t csa_indexer_topk_workspace_size(int b, int sq, int n_c, int H_I, int d_I,
   return ws;
 }
 
-csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float* w,
-                              const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
-                              int b, int sq, int n_c, int H_I, int d_I, int ratio, int topk,
-                              csa_dtype_t dt, void* workspace, size_t workspace_bytes,
-                              csa_stream_t stream) {
+csa_status_t csa_indexer_topk_rows(const void* q_idx, const void* k_idx, const float* w,
+                                   const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
+                                   int b, int sq, int n_c, int H_I, int d_I, int ratio, int topk,
+                                   csa_dtype_t dt, void* workspace, size_t workspace_bytes,
+                                   int t_begin, int t_end, csa_stream_t stream) {
   if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
   if (q_idx == nullptr || k_idx == nullptr || w == nullptr || topk_idx == nullptr ||
       workspace == nullptr)
@@ -310,6 +315,7 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
     return CSA_ERR_INVALID_ARG;
   const csa_status_t st = csa::check_indexer_shape(b, sq, n_c, H_I, d_I, ratio, topk, 8);
   if (st != CSA_OK) return st;
+  if (check_rows(sq, t_begin, t_end) != CSA_OK) return CSA_ERR_INVALID_ARG;
   if (workspace_bytes < csa::indexer_min_chunk_bytes(b, n_c)) return CSA_ERR_WORKSPACE;
   const bool use_tc = dt == CSA_BF16 && !csa::indexer_cuda_cores_forced() &&
                       csa::indexer_tc_supported(H_I, d_I);
@@ -319,12 +325,21 @@ csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float*
       csa::launch_doc_boundary_check(doc_ids, b, sq, ratio, status, s) != cudaSuccess)
     return CSA_ERR_CUDA;
   return csa::indexer_chunks(b, sq, n_c, ratio, topk, doc_ids, topk_idx, topk_score, workspace,
-                             workspace_bytes, s, 0, sq, [&](float* ws, int t0, int nt) {
+                             workspace_bytes, s, t_begin, t_end, [&](float* ws, int t0, int nt) {
     return use_tc ? csa::launch_indexer_scores_tc(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
                                                   d_I, ratio, status, s)
                   : csa::launch_indexer_scores_simt(q_idx, k_idx, w, ws, t0, nt, b, sq, n_c, H_I,
                                                     d_I, ratio, dt == CSA_BF16, s);
   });
+}
+
+csa_status_t csa_indexer_topk(const void* q_idx, const void* k_idx, const float* w,
+                              const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
+                              int b, int sq, int n_c, int H_I, int d_I, int ratio, int topk,
+                              csa_dtype_t dt, void* workspace, size_t workspace_bytes,
+                              csa_stream_t stream) {
+  return csa_indexer_topk_rows(q_idx, k_idx, w, doc_ids, topk_idx, topk_score, b, sq, n_c, H_I,
+                               d_I, ratio, topk, dt, workspace, workspace_bytes, 0, sq, stream);
 }
 
 csa_status_t csa_quantize_e4m3(const void* x, long long rows, int d, csa_dtype_t dt,
@@ -369,38 +384,49 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
   });
 }
 
-csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx,
-                          const float* sink, const int32_t* doc_ids, float scale, void* o,
-                          float* lse, int b, int sq, int H, int d, int n_c, int ratio, int window,
-                          int K, csa_dtype_t dt, csa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// CSA_ATTN_WARP_MMA=1 selects the warp-level mma.sync kernels for bf16 even
+// where the tcgen05 kernels apply (same results up to rounding order).
+bool warp_mma_forced() {
+  const char* wm = getenv("CSA_ATTN_WARP_MMA");
+  return wm != nullptr && wm[0] == '1';
+}
+
+csa_status_t attn_fwd_rows(const void* q, const void* kv_full, const int32_t* idx,
+                           const float* sink, const int32_t* doc_ids, float scale, void* o,
+                           float* lse, int b, int sq, int H, int d, int n_c, int ratio, int window,
+                           int K, csa_dtype_t dt, int tb, int te, csa_stream_t stream) {
   csa_status_t st = check_attn(q, kv_full, idx, scale, b, sq, H, d, n_c, ratio, window, K, dt);
   if (st != CSA_OK) return st;
+  if (check_rows(sq, tb, te) != CSA_OK) return CSA_ERR_INVALID_ARG;
   if (o == nullptr || lse == nullptr || !aligned16(o) || !aligned16(lse) || !aligned16(sink) ||
       !aligned16(doc_ids))
     return CSA_ERR_INVALID_ARG;
   const int Kl = idx ? K : n_c;
   cudaStream_t s = (cudaStream_t)stream;
-  // CSA_ATTN_WARP_MMA=1 selects the warp-level mma.sync kernels for bf16 even
-  // where the tcgen05 kernels apply (same results up to rounding order).
-  const char* wm = getenv("CSA_ATTN_WARP_MMA");
-  const bool warp_mma = wm && wm[0] == '1';
-  if (dt == CSA_BF16 && !warp_mma && csa::attn_tc_supported(H, d, n_c, Kl))
+  if (dt == CSA_BF16 && !warp_mma_forced() && csa::attn_tc_supported(H, d, n_c, Kl))
     return from_cuda(csa::launch_attn_fwd_tc(q, kv_full, idx, sink, scale, o, lse, b, sq, H, n_c,
-                                             ratio, window, Kl, device_status_ptr(), s, doc_ids));
+                                             ratio, window, Kl, device_status_ptr(), s, doc_ids,
+                                             tb, te));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
     return from_cuda(csa::launch_attn_fwd_mma(q, kv_full, idx, sink, scale, o, lse, b, sq, H, d,
-                                              n_c, ratio, window, Kl, s, doc_ids));
+                                              n_c, ratio, window, Kl, s, doc_ids, tb, te));
   return from_cuda(csa::launch_attn_fwd_simt(q, kv_full, idx, sink, scale, o, lse, b, sq, H, d,
-                                             n_c, ratio, window, Kl, dt == CSA_BF16, s, doc_ids));
+                                             n_c, ratio, window, Kl, dt == CSA_BF16, s, doc_ids,
+                                             tb, te));
 }
 
-csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx,
-                          const float* sink, const int32_t* doc_ids, float scale, const void* o,
-                          const float* lse, const void* dO, float* dq, float* dkv, float* dsink,
-                          int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
-                          csa_dtype_t dt, csa_stream_t stream) {
+csa_status_t attn_bwd_rows(const void* q, const void* kv_full, const int32_t* idx,
+                           const float* sink, const int32_t* doc_ids, float scale, const void* o,
+                           const float* lse, const void* dO, float* dq, float* dkv, float* dsink,
+                           int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
+                           csa_dtype_t dt, int tb, int te, bool accumulate, csa_stream_t stream) {
   csa_status_t st = check_attn(q, kv_full, idx, scale, b, sq, H, d, n_c, ratio, window, K, dt);
   if (st != CSA_OK) return st;
+  if (check_rows(sq, tb, te) != CSA_OK) return CSA_ERR_INVALID_ARG;
   if (o == nullptr || lse == nullptr || dO == nullptr || dq == nullptr || dkv == nullptr)
     return CSA_ERR_INVALID_ARG;
   if (sink != nullptr && dsink == nullptr) return CSA_ERR_INVALID_ARG;
@@ -410,22 +436,62 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
   const int Kl = idx ? K : n_c;
   cudaStream_t s = (cudaStream_t)stream;
   const int n_kv = sq + n_c;
-  cudaError_t e = csa::launch_zero_f32_pair(dkv, (size_t)b * n_kv * d, dsink,
-                                            dsink != nullptr ? (size_t)H : 0, s);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-  const char* wm = getenv("CSA_ATTN_WARP_MMA");
-  const bool warp_mma = wm && wm[0] == '1';
-  if (dt == CSA_BF16 && !warp_mma && csa::attn_tc_bwd_supported(H, d, n_c, Kl))
+  if (!accumulate) {
+    cudaError_t e = csa::launch_zero_f32_pair(dkv, (size_t)b * n_kv * d, dsink,
+                                              dsink != nullptr ? (size_t)H : 0, s);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  if (dt == CSA_BF16 && !warp_mma_forced() && csa::attn_tc_bwd_supported(H, d, n_c, Kl))
     return from_cuda(csa::launch_attn_bwd_tc(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                              dsink, b, sq, H, n_c, ratio, window, Kl,
-                                             device_status_ptr(), s, doc_ids));
+                                             device_status_ptr(), s, doc_ids, tb, te));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
     return from_cuda(csa::launch_attn_bwd_mma(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                               dsink, b, sq, H, d, n_c, ratio, window, Kl, s,
-                                              doc_ids));
+                                              doc_ids, tb, te));
   return from_cuda(csa::launch_attn_bwd_simt(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                              dsink, b, sq, H, d, n_c, ratio, window, Kl,
-                                             dt == CSA_BF16, s, doc_ids));
+                                             dt == CSA_BF16, s, doc_ids, tb, te));
+}
+
+}  // namespace
+
+extern "C" {
+
+csa_status_t csa_attn_fwd(const void* q, const void* kv_full, const int32_t* idx,
+                          const float* sink, const int32_t* doc_ids, float scale, void* o,
+                          float* lse, int b, int sq, int H, int d, int n_c, int ratio, int window,
+                          int K, csa_dtype_t dt, csa_stream_t stream) {
+  return attn_fwd_rows(q, kv_full, idx, sink, doc_ids, scale, o, lse, b, sq, H, d, n_c, ratio,
+                       window, K, dt, 0, sq, stream);
+}
+
+csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx,
+                          const float* sink, const int32_t* doc_ids, float scale, const void* o,
+                          const float* lse, const void* dO, float* dq, float* dkv, float* dsink,
+                          int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
+                          csa_dtype_t dt, csa_stream_t stream) {
+  return attn_bwd_rows(q, kv_full, idx, sink, doc_ids, scale, o, lse, dO, dq, dkv, dsink, b, sq,
+                       H, d, n_c, ratio, window, K, dt, 0, sq, false, stream);
+}
+
+csa_status_t csa_attn_fwd_rows(const void* q, const void* kv_full, const int32_t* idx,
+                               const float* sink, const int32_t* doc_ids, float scale, void* o,
+                               float* lse, int b, int sq, int H, int d, int n_c, int ratio,
+                               int window, int K, csa_dtype_t dt, int t_begin, int t_end,
+                               csa_stream_t stream) {
+  return attn_fwd_rows(q, kv_full, idx, sink, doc_ids, scale, o, lse, b, sq, H, d, n_c, ratio,
+                       window, K, dt, t_begin, t_end, stream);
+}
+
+csa_status_t csa_attn_bwd_rows(const void* q, const void* kv_full, const int32_t* idx,
+                               const float* sink, const int32_t* doc_ids, float scale,
+                               const void* o, const float* lse, const void* dO, float* dq,
+                               float* dkv, float* dsink, int b, int sq, int H, int d, int n_c,
+                               int ratio, int window, int K, csa_dtype_t dt, int t_begin,
+                               int t_end, int accumulate, csa_stream_t stream) {
+  return attn_bwd_rows(q, kv_full, idx, sink, doc_ids, scale, o, lse, dO, dq, dkv, dsink, b, sq,
+                       H, d, n_c, ratio, window, K, dt, t_begin, t_end, accumulate != 0, stream);
 }
 
 csa_status_t csa_indexer_teacher(const void* q, const void* kv_full, const int32_t* idx,

@@ -13,8 +13,10 @@
  * Further calls: packed documents (the doc_ids argument of the indexer and
  * the attention), the indexer's training path (csa_indexer_teacher,
  * csa_indexer_loss), overlapping compression (csa_compress_overlap and its
- * backward), an FP8 indexer (csa_quantize_e4m3, csa_indexer_topk_fp8) and an
- * indexer that needs no caller workspace (csa_indexer_topk_noalloc).
+ * backward), an FP8 indexer (csa_quantize_e4m3, csa_indexer_topk_fp8), an
+ * indexer that needs no caller workspace (csa_indexer_topk_noalloc) and
+ * row-range forms of the indexer and the attention for a layer split by
+ * query rows across GPUs (csa_*_rows).
  *
  * Sources (page title, section):
  *   "Add unfused SBHD compressed sparse attention" (Megatron-LM PR #6400):
@@ -385,6 +387,47 @@ csa_status_t csa_attn_bwd(const void* q, const void* kv_full, const int32_t* idx
                           const void* dO, float* dq, float* dkv, float* dsink,
                           int b, int sq, int H, int d, int n_c, int ratio, int window, int K,
                           csa_dtype_t dt, csa_stream_t stream);
+
+/*
+ * Row-range calls: one layer split by query rows across GPUs.
+ *
+ * The layer partitions by query rows: every query's indexer row, top-k and
+ * attention read only shared inputs (kv_full, k_idx, sink), so a GPU that
+ * holds those can process any subset of the query rows, and the backward's
+ * only cross-row result is the scatter into dkv and dsink, which sums.  The
+ * pages keep the sink per head and reject splitting heads across ranks
+ * ("Add unfused SBHD compressed sparse attention", attention-sink parameter
+ * and the review of its tensor-parallel guard), which leaves the query rows
+ * as the axis to split.  These calls take the same arguments as
+ * csa_indexer_topk / csa_attn_fwd / csa_attn_bwd, with the full-size arrays
+ * (positions stay absolute), plus the query rows [t_begin, t_end) of every
+ * batch element to process (0 <= t_begin < t_end <= sq); other rows of the
+ * outputs are not touched.
+ *
+ * csa_attn_bwd_rows: dq rows in the range are written; the range's
+ * contributions to dkv and dsink are added to what they hold when
+ * accumulate != 0, else dkv and dsink are zeroed first.  The layer's dkv and
+ * dsink are the sum of the contributions of disjoint ranges that cover all
+ * rows (on one GPU: calls with accumulate = 1 after the first; across GPUs:
+ * one sum-reduction of [dkv, dsink]).
+ * Errors: as the full calls, plus INVALID_ARG for a range outside [0, sq).
+ */
+csa_status_t csa_indexer_topk_rows(const void* q_idx, const void* k_idx, const float* w,
+                                   const int32_t* doc_ids, int32_t* topk_idx, float* topk_score,
+                                   int b, int sq, int n_c, int H_I, int d_I, int ratio, int topk,
+                                   csa_dtype_t dt, void* workspace, size_t workspace_bytes,
+                                   int t_begin, int t_end, csa_stream_t stream);
+csa_status_t csa_attn_fwd_rows(const void* q, const void* kv_full, const int32_t* idx,
+                               const float* sink, const int32_t* doc_ids, float scale, void* o,
+                               float* lse, int b, int sq, int H, int d, int n_c, int ratio,
+                               int window, int K, csa_dtype_t dt, int t_begin, int t_end,
+                               csa_stream_t stream);
+csa_status_t csa_attn_bwd_rows(const void* q, const void* kv_full, const int32_t* idx,
+                               const float* sink, const int32_t* doc_ids, float scale,
+                               const void* o, const float* lse, const void* dO, float* dq,
+                               float* dkv, float* dsink, int b, int sq, int H, int d, int n_c,
+                               int ratio, int window, int K, csa_dtype_t dt, int t_begin,
+                               int t_end, int accumulate, csa_stream_t stream);
 
 /*
  * csa_indexer_teacher - distillation target of the indexer.

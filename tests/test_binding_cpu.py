@@ -32,6 +32,16 @@ CALLS = {
     "csa_attn_bwd": lambda: csa.csa_attn_bwd(_t(1, 8, 2, 16), _t(1, 10, 16), _t(1, 8, 2, dtype=i32),
                                              None, 0.25, 4, 4, _t(1, 8, 2, 16),
                                              _t(1, 8, 2, dtype=f32), _t(1, 8, 2, 16)),
+    "csa_indexer_topk_rows": lambda: csa.csa_indexer_topk(_t(1, 8, 2, 16), _t(1, 2, 16),
+                                                          _t(1, 8, 2, dtype=f32), 2, 4,
+                                                          rows=(0, 4)),
+    "csa_attn_fwd_rows": lambda: csa.csa_attn_fwd(_t(1, 8, 2, 16), _t(1, 10, 16),
+                                                  _t(1, 8, 2, dtype=i32), None, 0.25, 4, 4,
+                                                  rows=(0, 4)),
+    "csa_attn_bwd_rows": lambda: csa.csa_attn_bwd(_t(1, 8, 2, 16), _t(1, 10, 16),
+                                                  _t(1, 8, 2, dtype=i32), None, 0.25, 4, 4,
+                                                  _t(1, 8, 2, 16), _t(1, 8, 2, dtype=f32),
+                                                  _t(1, 8, 2, 16), rows=(4, 8), accumulate=True),
     "csa_indexer_teacher": lambda: csa.csa_indexer_teacher(_t(1, 8, 2, 16), _t(1, 10, 16),
                                                            _t(1, 8, 2, dtype=i32),
                                                            _t(1, 8, 2, dtype=f32), 0.25, 4),
