@@ -48,6 +48,14 @@ the design notes of the repository):
     compressor review names);
   * FP8 indexer: per-row e4m3 codes with scale absmax / 448 (the pages list
     indexer quantization only as not yet included).
+  * normalization of the pooled rows: RMS normalization over the d channels
+    with a per-channel weight, on the pooled row after its one cast, result
+    cast once more (the compressor review shows kv = self.norm(kv) after the
+    cast; the norm's type is not shown);
+  * rotary embedding of the pooled rows: interleaved channel pairs
+    (2i, 2i+1) of the last rope_dim channels, angle pos * base^(-2i/rope_dim),
+    entry j at the position of the last token it pools, (j+1)*ratio - 1
+    (the pages give only the base, 40000, "for compressed KV positions").
 
 All functions take and return numpy arrays; floating results are float64.
 """
@@ -63,6 +71,7 @@ __all__ = [
     "selected_entries", "indexer_teacher_row", "indexer_teacher",
     "indexer_student_row", "indexer_kl_row", "indexer_loss",
     "round_e4m3", "quantize_rows_e4m3", "indexer_scores_fp8",
+    "compressed_position", "rope_angles", "kv_norm_rope", "kv_norm_rope_bwd",
 ]
 
 
@@ -551,3 +560,85 @@ def indexer_scores_fp8(q8, q_scale, k8, k_scale, w, ratio: int, doc_ids=None):
             if doc_ids is not None:
                 out[bi, t, ~indexer_selectable(t, n_c, ratio, doc_ids[bi])] = -np.inf
     return out
+
+
+# ---------------------------------------------------------------------------
+# Normalization and rotary embedding of the pooled rows
+# ---------------------------------------------------------------------------
+#
+# "Add unfused SBHD compressed sparse attention" (compressor review): the
+# pooled row is cast once to the storage dtype and then normalized,
+# kv = self.norm(kv); its config fields give the rotary base of compressed KV
+# positions, csa_compress_rotary_base = 40000.  "[DeepSeek-v4] Part 1": the
+# KV norm is created over v_head_dim channels (one weight per channel), and
+# the MLA rotary kernels keep the interleaved channel layout.  Neither the
+# norm's type nor the rotary channels nor the compressed position are given;
+# the readings are stated in the module header.
+
+def compressed_position(j, ratio: int):
+    """Position of compressed entry j: its last pooled token, (j+1)*ratio - 1
+    (the token at which the entry becomes visible)."""
+    return (np.asarray(j, np.int64) + 1) * ratio - 1
+
+
+def rope_angles(pos, rope_dim: int, base: float):
+    """Angles [len(pos), rope_dim/2]: pos * base^(-2i/rope_dim)."""
+    i = np.arange(rope_dim // 2, dtype=np.float64)
+    theta = np.power(float(base), -2.0 * i / rope_dim)
+    return np.asarray(pos, np.float64)[:, None] * theta[None, :]
+
+
+def _rotate(y, ang, sign: float):
+    """Rotate the interleaved pairs (2i, 2i+1) of y [..., 2m] by sign*ang [..., m]."""
+    c, s = np.cos(ang), sign * np.sin(ang)
+    a, b = y[..., 0::2], y[..., 1::2]
+    out = np.empty_like(y)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = a * s + b * c
+    return out
+
+
+def kv_norm_rope(kv_c, weight, eps: float, rope_dim: int, base: float, ratio: int,
+                 out_dtype: str = "fp64"):
+    """RMS-normalize each pooled row over its d channels and rotate its last
+    rope_dim channels.
+
+    kv_c [b, n_c, d] (the pooled rows as stored), weight [d]:
+      y = kv_c / sqrt(mean_c(kv_c^2) + eps) * weight
+      y[..., d-rope_dim:] rotated pairwise by pos_j * base^(-2i/rope_dim),
+      pos_j = (j+1)*ratio - 1,
+    rounded once to out_dtype.
+    """
+    x = np.asarray(kv_c, np.float64)
+    b, n_c, d = x.shape
+    rms = np.sqrt((x * x).mean(axis=2, keepdims=True) + eps)
+    y = x / rms * np.asarray(weight, np.float64)
+    if rope_dim:
+        ang = rope_angles(compressed_position(np.arange(n_c), ratio), rope_dim, base)
+        y[..., d - rope_dim:] = _rotate(y[..., d - rope_dim:], ang[None], 1.0)
+    return round_to_storage(y, out_dtype)
+
+
+def kv_norm_rope_bwd(kv_c, weight, eps: float, rope_dim: int, base: float, ratio: int, g):
+    """Gradients of kv_norm_rope (unrounded) given g = dL/d(output) [b, n_c, d]:
+    returns (dL/dkv_c [b, n_c, d], dL/dweight [d]).
+
+    The rotation is orthogonal, so its gradient rotates g back (angle
+    negated); with xh = x / rms and dy the unrotated gradient:
+      dweight = sum over rows of dy * xh,
+      dx = (dy*weight - xh * mean_c(dy*weight*xh)) / rms.
+    """
+    x = np.asarray(kv_c, np.float64)
+    g = np.asarray(g, np.float64)
+    w = np.asarray(weight, np.float64)
+    b, n_c, d = x.shape
+    dy = g.copy()
+    if rope_dim:
+        ang = rope_angles(compressed_position(np.arange(n_c), ratio), rope_dim, base)
+        dy[..., d - rope_dim:] = _rotate(g[..., d - rope_dim:], ang[None], -1.0)
+    rms = np.sqrt((x * x).mean(axis=2, keepdims=True) + eps)
+    xh = x / rms
+    dweight = (dy * xh).sum(axis=(0, 1))
+    dxh = dy * w
+    dx = (dxh - xh * (dxh * xh).mean(axis=2, keepdims=True)) / rms
+    return dx, dweight

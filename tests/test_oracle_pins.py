@@ -743,3 +743,118 @@ def test_indexer_scores_fp8_reduce_to_plain_scores():
     sq_s, sk_s = rng.uniform(0.5, 2, (b, sq, H)), rng.uniform(0.5, 2, (b, sq // r))
     ref = orc.indexer_scores(q * sq_s[..., None], k * sk_s[..., None], w, r)
     np.testing.assert_allclose(orc.indexer_scores_fp8(q, sq_s, k, sk_s, w, r), ref, atol=1e-9)
+
+
+# ---------------------------------------------------------------------------
+# normalization and rotary embedding of the pooled rows
+# ---------------------------------------------------------------------------
+
+def test_kv_norm_unit_weight_has_the_closed_form_rms():
+    """Weight 1, no rotation: each row is x / sqrt(mean(x^2) + eps), so its
+    mean square is ms / (ms + eps) and x is recovered by the RMS factor."""
+    rng = np.random.default_rng(40)
+    x = rng.normal(size=(2, 5, 24)) * rng.uniform(0.1, 10, size=(2, 5, 1))
+    eps = 1e-3
+    y = orc.kv_norm_rope(x, np.ones(24), eps, 0, 40000.0, 4)
+    ms = (x ** 2).sum(axis=2) / 24
+    assert np.allclose((y ** 2).sum(axis=2) / 24, ms / (ms + eps), rtol=1e-12)
+    assert np.allclose(y * np.sqrt(ms + eps)[..., None], x, rtol=1e-12)
+
+
+def test_kv_norm_weight_scales_each_channel():
+    rng = np.random.default_rng(41)
+    x = rng.normal(size=(1, 3, 16))
+    w = rng.normal(size=16)
+    y1 = orc.kv_norm_rope(x, np.ones(16), 1e-6, 0, 40000.0, 4)
+    yw = orc.kv_norm_rope(x, w, 1e-6, 0, 40000.0, 4)
+    assert np.allclose(yw, y1 * w, rtol=1e-12, atol=0)
+
+
+def test_rope_is_complex_multiplication_of_interleaved_pairs():
+    """The rotary part equals (y[2i] + i y[2i+1]) * exp(i pos theta_i) with
+    pos = (j+1)*ratio - 1 and theta_i = 40000^(-i/(rope_dim/2)), evaluated
+    with numpy complex arithmetic; the other channels are untouched."""
+    rng = np.random.default_rng(42)
+    d, rd, ratio, n_c = 32, 12, 4, 7
+    x = rng.normal(size=(2, n_c, d))
+    w = rng.normal(size=d)
+    plain = orc.kv_norm_rope(x, w, 1e-6, 0, 40000.0, ratio)
+    got = orc.kv_norm_rope(x, w, 1e-6, rd, 40000.0, ratio)
+    assert np.array_equal(got[..., :d - rd], plain[..., :d - rd])
+    z = plain[..., d - rd::2] + 1j * plain[..., d - rd + 1::2]
+    pos = np.array([(j + 1) * ratio - 1 for j in range(n_c)], np.float64)
+    freq = 1.0 / 40000.0 ** (np.arange(rd // 2) / (rd // 2))
+    zr = z * np.exp(1j * pos[:, None] * freq[None, :])
+    assert np.allclose(got[..., d - rd::2], zr.real, atol=1e-12)
+    assert np.allclose(got[..., d - rd + 1::2], zr.imag, atol=1e-12)
+
+
+def test_rope_depends_only_on_relative_position():
+    """Rows with identical content: the rotary parts' inner products depend
+    only on the distance between the rows, and each pair keeps its norm."""
+    rng = np.random.default_rng(43)
+    d, rd, ratio, n_c = 16, 16, 4, 9
+    u = rng.normal(size=d)
+    x = np.broadcast_to(u, (1, n_c, d)).copy()
+    y = orc.kv_norm_rope(x, np.ones(d), 0.0, rd, 40000.0, ratio)[0]
+    dots = y @ y.T
+    for k in range(1, 5):
+        diag = np.diagonal(dots, offset=k)
+        assert np.allclose(diag, diag[0], rtol=1e-10)
+    pair = y[:, 0::2] ** 2 + y[:, 1::2] ** 2
+    assert np.allclose(pair, pair[0], rtol=1e-12)
+
+
+def test_rope_at_position_zero_is_identity():
+    """ratio 1: entry 0 sits at position 0, where every angle is 0."""
+    rng = np.random.default_rng(44)
+    x = rng.normal(size=(1, 3, 16))
+    w = rng.normal(size=16)
+    a = orc.kv_norm_rope(x, w, 1e-6, 16, 40000.0, 1)
+    b = orc.kv_norm_rope(x, w, 1e-6, 0, 40000.0, 1)
+    assert np.array_equal(a[:, 0], b[:, 0]) and not np.allclose(a[:, 1], b[:, 1])
+
+
+def test_kv_norm_rope_bwd_matches_torch_autograd():
+    """Gradients against float64 autograd of torch's own RMS norm and a
+    complex-number rotation (torch.view_as_complex / torch.polar)."""
+    rng = np.random.default_rng(45)
+    b, n_c, d, rd, ratio, eps = 2, 6, 32, 16, 4, 1e-5
+    x = rng.normal(size=(b, n_c, d))
+    w = rng.normal(size=d)
+    g = rng.normal(size=(b, n_c, d))
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    y = torch.nn.functional.rms_norm(xt, (d,), weight=wt, eps=eps)
+    pos = torch.tensor([(j + 1) * ratio - 1 for j in range(n_c)], dtype=torch.float64)
+    freq = 40000.0 ** (-torch.arange(rd // 2, dtype=torch.float64) / (rd // 2))
+    rot = torch.polar(torch.ones(n_c, rd // 2, dtype=torch.float64), pos[:, None] * freq[None])
+    zc = torch.view_as_complex(y[..., d - rd:].reshape(b, n_c, rd // 2, 2).contiguous()) * rot
+    out = torch.cat([y[..., :d - rd], torch.view_as_real(zc).reshape(b, n_c, rd)], dim=-1)
+    out.backward(torch.tensor(g))
+    assert np.allclose(orc.kv_norm_rope(x, w, eps, rd, 40000.0, ratio), out.detach().numpy(),
+                       atol=1e-12)
+    dx, dw = orc.kv_norm_rope_bwd(x, w, eps, rd, 40000.0, ratio, g)
+    assert np.allclose(dx, xt.grad.numpy(), atol=1e-10)
+    assert np.allclose(dw, wt.grad.numpy(), atol=1e-10)
+
+
+def test_kv_norm_rope_bwd_finite_differences():
+    rng = np.random.default_rng(46)
+    b, n_c, d, rd, ratio, eps = 1, 3, 8, 4, 2, 1e-4
+    x = rng.normal(size=(b, n_c, d))
+    w = rng.normal(size=d)
+    g = rng.normal(size=(b, n_c, d))
+    dx, dw = orc.kv_norm_rope_bwd(x, w, eps, rd, 40000.0, ratio, g)
+    f = lambda xx, ww: float((orc.kv_norm_rope(xx, ww, eps, rd, 40000.0, ratio) * g).sum())
+    h = 1e-6
+    for idx in [(0, 0, 0), (0, 1, 5), (0, 2, 7), (0, 2, 3)]:
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        assert abs((f(xp, w) - f(xm, w)) / (2 * h) - dx[idx]) < 1e-7
+    for c in (0, 6):
+        wp, wm = w.copy(), w.copy()
+        wp[c] += h
+        wm[c] -= h
+        assert abs((f(x, wp) - f(x, wm)) / (2 * h) - dw[c]) < 1e-7
