@@ -38,6 +38,11 @@ SIGNATURES = {
                              + [_c_p]),
     "csa_compress_overlap_bwd": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_ll, _c_p, _c_ll,
                                           _c_p] + [_c_int] * 6 + [_c_p]),
+    "csa_compress_norm_rope": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_f, _c_int, _c_f,
+                                        _c_p, _c_ll] + [_c_int] * 5 + [_c_p]),
+    "csa_compress_norm_rope_bwd": (_c_int, [_c_p, _c_ll, _c_p, _c_int, _c_p, _c_f, _c_int, _c_f,
+                                            _c_p, _c_ll, _c_p, _c_ll, _c_p, _c_p]
+                                   + [_c_int] * 5 + [_c_p]),
     "csa_indexer_topk_workspace_size": (_c_sz, [_c_int] * 6 + [_c_int]),
     "csa_indexer_topk_min_workspace": (_c_sz, [_c_int, _c_int]),
     "csa_indexer_topk": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p] + [_c_int] * 7
@@ -209,6 +214,47 @@ def csa_compress_overlap_bwd(kv: torch.Tensor, score: torch.Tensor, ratio: int, 
         dout.stride(0), dkv.data_ptr(), dkv.stride(0), dscore.data_ptr(), b, sq, d, ratio, coff,
         _dt(kv), _stream(stream)))
     return dscore
+
+
+def csa_compress_norm_rope(kv: torch.Tensor, score: torch.Tensor, ratio: int,
+                           norm_weight: torch.Tensor, eps: float, rope_dim: int,
+                           rope_base: float = 40000.0, out: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """csa_compress, then the RMS normalization (norm_weight [d] fp32, eps) and
+    the rotary embedding (last rope_dim channels, interleaved pairs, entry j
+    at position (j+1)*ratio - 1) of each pooled row; arguments otherwise as
+    csa_compress."""
+    lib = load_library()
+    out = _compress_out(kv, score, ratio, out)
+    _need(norm_weight, "norm_weight", dtype=torch.float32)
+    b, sq, d = kv.shape
+    _check("csa_compress_norm_rope", lib.csa_compress_norm_rope(
+        kv.data_ptr(), kv.stride(0), score.data_ptr(), score.shape[2], norm_weight.data_ptr(),
+        float(eps), int(rope_dim), float(rope_base), out.data_ptr(), out.stride(0), b, sq, d,
+        ratio, _dt(kv), _stream(stream)))
+    return out
+
+
+def csa_compress_norm_rope_bwd(kv: torch.Tensor, score: torch.Tensor, ratio: int,
+                               norm_weight: torch.Tensor, eps: float, rope_dim: int,
+                               rope_base: float, dout: torch.Tensor, dkv: torch.Tensor,
+                               dscore: Optional[torch.Tensor] = None,
+                               dnorm_weight: Optional[torch.Tensor] = None, stream=None):
+    """Gradient of csa_compress_norm_rope: adds the pooling's share into dkv
+    (in place) and returns (dscore, dnorm_weight)."""
+    lib = load_library()
+    dscore = _compress_bwd_args(kv, score, dout, dkv, dscore)
+    _need(norm_weight, "norm_weight", dtype=torch.float32)
+    b, sq, d = kv.shape
+    if dnorm_weight is None:
+        dnorm_weight = torch.empty(d, dtype=torch.float32, device=kv.device)
+    _need(dnorm_weight, "dnorm_weight", dtype=torch.float32)
+    _check("csa_compress_norm_rope_bwd", lib.csa_compress_norm_rope_bwd(
+        kv.data_ptr(), kv.stride(0), score.data_ptr(), score.shape[2], norm_weight.data_ptr(),
+        float(eps), int(rope_dim), float(rope_base), dout.data_ptr(), dout.stride(0),
+        dkv.data_ptr(), dkv.stride(0), dscore.data_ptr(), dnorm_weight.data_ptr(), b, sq, d,
+        ratio, _dt(kv), _stream(stream)))
+    return dscore, dnorm_weight
 
 
 def csa_indexer_topk_workspace_size(b: int, sq: int, n_c: int, H_I: int, d_I: int, topk: int,

@@ -8,73 +8,15 @@
 // HBM-bound: each kv and score element is read once and each pooled element
 // written once.  One thread owns 8 consecutive channels of one block.  For
 // ratio 4 (the CSA ratio) the thread loads the whole block before any
-// arithmetic, so one memory latency covers it; other ratios walk the tokens
-// with an online (running max) softmax, reading the scores in one pass.
+// arithmetic, so one memory latency covers it; other small ratios walk the
+// tokens with an online (running max) softmax, reading the scores in one
+// pass; ratios of 16 and more (HCA: 128) split each block's tokens over the
+// threads of a CTA and merge the partial softmax statistics.
+#include "compress_pool.cuh"
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 
 namespace csa {
-
-// 8 channels of token t of a block: kv row and the pooling score (the score is
-// broadcast over the channels when one score drives the whole row)
-template <typename T>
-__device__ __forceinline__ void load_token(const T* kvp, const T* scp, int t, int d,
-                                           int score_width, int c0, float* v, float* s) {
-  load8(kvp + (long long)t * d, v);
-  if (score_width == 1) {
-    const float s1 = to_f(scp[t]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i] = s1;
-  } else {
-    load8(scp + (long long)t * score_width + c0, s);
-  }
-}
-
-// Per-channel softmax statistics of a block (running max m, sum l) and the
-// pooled value sum_t w_t kv_t.  R > 0: compile-time ratio, the block is held
-// in registers (v, s filled by the caller); R == 0: runtime ratio, online.
-template <typename T, int R>
-__device__ __forceinline__ void pool_block(const T* kvp, const T* scp, int ratio, int d,
-                                           int score_width, int c0, float (*v)[8],
-                                           float (*s)[8], float* m, float* l, float* pooled) {
-  if constexpr (R > 0) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float mx = s[0][i];
-#pragma unroll
-      for (int t = 1; t < R; ++t) mx = fmaxf(mx, s[t][i]);
-      float sum = 0.f, acc = 0.f;
-#pragma unroll
-      for (int t = 0; t < R; ++t) {
-        const float e = expf(s[t][i] - mx);
-        sum += e;
-        acc = fmaf(e, v[t][i], acc);
-      }
-      m[i] = mx;
-      l[i] = sum;
-      pooled[i] = acc / sum;
-    }
-  } else {
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; l[i] = 0.f; acc[i] = 0.f; }
-    for (int t = 0; t < ratio; ++t) {
-      float vt[8], st[8];
-      load_token(kvp, scp, t, d, score_width, c0, vt, st);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float mn = fmaxf(m[i], st[i]);
-        const float alpha = expf(m[i] - mn);  // 0 on the first token (m = -inf)
-        const float e = expf(st[i] - mn);
-        l[i] = l[i] * alpha + e;
-        acc[i] = acc[i] * alpha + e * vt[i];
-        m[i] = mn;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) pooled[i] = acc[i] / l[i];
-  }
-}
 
 template <typename T, int R>
 __global__ void __launch_bounds__(64) compress_kernel(const T* __restrict__ kv, long long kv_bs,
@@ -261,13 +203,167 @@ __global__ void __launch_bounds__(64) compress_overlap_bwd_kernel(
   }
 }
 
+// Large ratios (the HCA ratio 128): one CTA per block, whose threads split
+// the block's tokens into TS ranges as well as its channels (8 per thread).
+// Each thread forms the online softmax of its tokens; the partial (max, sum,
+// weighted sum) triples are merged in shared memory.  A thread per (block,
+// 8 channels) walking all `ratio` tokens, as above, would leave a few
+// thousand threads each waiting on `ratio` dependent loads in turn.
+constexpr int kSplitThreads = 256;
+constexpr int kSplitMinRatio = 16;
+
+template <typename T>
+__device__ __forceinline__ void split_partial(const T* kvp, const T* scp, int d, int score_width,
+                                              int c0, int t_lo, int t_hi, float* m, float* l,
+                                              float* acc) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; l[i] = 0.f; acc[i] = 0.f; }
+  for (int t = t_lo; t < t_hi; ++t) {
+    float vt[8], st[8];
+    load_token(kvp, scp, t, d, score_width, c0, vt, st);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float mn = fmaxf(m[i], st[i]);
+      const float alpha = expf(m[i] - mn);    // 0 on the first token (m = -inf)
+      const float e = expf(st[i] - mn);
+      l[i] = l[i] * alpha + e;
+      acc[i] = acc[i] * alpha + e * vt[i];
+      m[i] = mn;
+    }
+  }
+}
+
+// The block's statistics per channel: the TS partials of this CTA merged by
+// the threads of token range 0 into (M, L, pooled), left in shared memory
+// (sm[0..3*groups*8)) for every thread.  kvp points at channel 0 of the
+// block's first token.
+template <typename T>
+__device__ __forceinline__ void split_stats(const T* kvp, const T* scp, int d, int score_width,
+                                            int ratio, float* sm, int groups, int TS, int cg,
+                                            int ts) {
+  const int per = (ratio + TS - 1) / TS;
+  float m[8], l[8], acc[8];
+  const int t_lo = min(ratio, ts * per), t_hi = min(ratio, t_lo + per);
+  if (ts < TS) {
+    split_partial(kvp + cg * 8, scp, d, score_width, cg * 8, t_lo, t_hi, m, l, acc);
+    float* pm = sm + ((size_t)ts * groups + cg) * 24;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { pm[i] = m[i]; pm[8 + i] = l[i]; pm[16 + i] = acc[i]; }
+  }
+  __syncthreads();
+  float M[8], L[8], A[8];
+  if (ts == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { M[i] = -INFINITY; L[i] = 0.f; A[i] = 0.f; }
+    for (int k = 0; k < TS; ++k) {
+      const float* pm = sm + ((size_t)k * groups + cg) * 24;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) M[i] = fmaxf(M[i], pm[i]);
+    }
+    for (int k = 0; k < TS; ++k) {
+      const float* pm = sm + ((size_t)k * groups + cg) * 24;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float f = expf(pm[i] - M[i]);   // 0 for an empty range (m = -inf)
+        L[i] = fmaf(pm[8 + i], f, L[i]);
+        A[i] = fmaf(pm[16 + i], f, A[i]);
+      }
+    }
+  }
+  __syncthreads();              // every partial has been read
+  if (ts == 0) {
+    float* st = sm + (size_t)cg * 24;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { st[i] = M[i]; st[8 + i] = L[i]; st[16 + i] = A[i] / L[i]; }
+  }
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads) compress_split_kernel(
+    const T* __restrict__ kv, long long kv_bs, const T* __restrict__ score, int score_width,
+    T* __restrict__ out, long long out_bs, int sq, int d, int ratio) {
+  extern __shared__ float sm_split[];
+  const int groups = d / 8, TS = kSplitThreads / groups;
+  const int j = blockIdx.x, bi = blockIdx.y;
+  const int cg = threadIdx.x % groups, ts = threadIdx.x / groups;
+  const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d;
+  const T* scp = score + ((long long)bi * sq + (long long)j * ratio) * score_width;
+  split_stats(kvp, scp, d, score_width, ratio, sm_split, groups, TS, cg, ts);
+  if (ts == 0) store8(out + bi * out_bs + (long long)j * d + cg * 8, sm_split + cg * 24 + 16);
+}
+
+// Its backward: the block's statistics as above, then every thread adds
+// w_t g to its tokens' dkv rows and writes their score gradients (the CTA
+// past the last block writes the zero score gradient of the tail tokens).
+template <typename T>
+__global__ void __launch_bounds__(kSplitThreads) compress_bwd_split_kernel(
+    const T* __restrict__ kv, long long kv_bs, const T* __restrict__ score, int score_width,
+    const float* __restrict__ g, long long g_bs, float* __restrict__ dkv, long long dkv_bs,
+    float* __restrict__ dscore, int sq, int d, int ratio, int n_c) {
+  extern __shared__ float sm_split[];
+  const int groups = d / 8, TS = kSplitThreads / groups;
+  const int j = blockIdx.x, bi = blockIdx.y;
+  const int cg = threadIdx.x % groups, ts = threadIdx.x / groups;
+  if (j >= n_c) {             // tail tokens: zero score gradient (per-channel scores)
+    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int t = n_c * ratio + ts; ts < TS && t < sq; t += TS)
+      store8(dscore + ((long long)bi * sq + t) * score_width + cg * 8, z);
+    return;
+  }
+  const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d;
+  const T* scp = score + ((long long)bi * sq + (long long)j * ratio) * score_width;
+  split_stats(kvp, scp, d, score_width, ratio, sm_split, groups, TS, cg, ts);
+  if (ts >= TS) return;
+  const int c0 = cg * 8;
+  float M[8], L[8], P[8], gv[8];
+  const float* st = sm_split + cg * 24;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { M[i] = st[i]; L[i] = st[8 + i]; P[i] = st[16 + i]; }
+  load8(g + bi * g_bs + (long long)j * d + c0, gv);
+  const int per = (ratio + TS - 1) / TS;
+  const int t_lo = min(ratio, ts * per), t_hi = min(ratio, t_lo + per);
+  float* dkp = dkv + bi * dkv_bs + (long long)j * ratio * d + c0;
+  for (int t = t_lo; t < t_hi; ++t) {
+    float vt[8], sv[8], dt[8];
+    load_token(kvp + c0, scp, t, d, score_width, c0, vt, sv);
+    load8(dkp + (long long)t * d, dt);
+    float ds[8], dsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w = expf(sv[i] - M[i]) / L[i];
+      dt[i] = fmaf(w, gv[i], dt[i]);
+      ds[i] = w * gv[i] * (vt[i] - P[i]);
+      dsum += ds[i];
+    }
+    store8(dkp + (long long)t * d, dt);
+    const long long tok = (long long)j * ratio + t;
+    if (score_width == 1)
+      atomicAdd(dscore + (long long)bi * sq + tok, dsum);
+    else
+      store8(dscore + ((long long)bi * sq + tok) * score_width + c0, ds);
+  }
+}
+
 namespace {
 constexpr int kCompressThreads = 64;
+
+size_t split_smem(int d) {
+  const int groups = d / 8;
+  return (size_t)(kSplitThreads / groups) * groups * 24 * sizeof(float);
+}
 
 template <typename T, int R>
 void compress_fwd_t(const void* kv, long long kv_bs, const void* score, int score_width,
                     void* out, long long out_bs, int b, int sq, int d, int ratio, cudaStream_t s) {
   const int n_c = sq / ratio;
+  if (R == 0 && ratio >= kSplitMinRatio) {
+    compress_split_kernel<T><<<dim3((unsigned)n_c, (unsigned)b), kSplitThreads, split_smem(d),
+                               s>>>((const T*)kv, kv_bs, (const T*)score, score_width, (T*)out,
+                                    out_bs, sq, d, ratio);
+    count_launches(1);
+    return;
+  }
   const long long work = (long long)n_c * (d / 8);
   dim3 grid((unsigned)((work + kCompressThreads - 1) / kCompressThreads), (unsigned)b);
   compress_kernel<T, R><<<grid, kCompressThreads, 0, s>>>((const T*)kv, kv_bs, (const T*)score,
@@ -282,6 +378,14 @@ void compress_bwd_t(const void* kv, long long kv_bs, const void* score, int scor
                     int b, int sq, int d, int ratio, cudaStream_t s) {
   const int n_c = sq / ratio;
   const int tail = score_width == 1 ? 0 : sq - n_c * ratio;
+  if (R == 0 && ratio >= kSplitMinRatio) {
+    const unsigned nx = (unsigned)(n_c + (tail > 0 ? 1 : 0));
+    compress_bwd_split_kernel<T><<<dim3(nx, (unsigned)b), kSplitThreads, split_smem(d), s>>>(
+        (const T*)kv, kv_bs, (const T*)score, score_width, g, g_bs, dkv, dkv_bs, dscore, sq, d,
+        ratio, n_c);
+    count_launches(1);
+    return;
+  }
   const long long work = (long long)(n_c + tail) * (d / 8);
   if (work == 0) return;
   dim3 grid((unsigned)((work + kCompressThreads - 1) / kCompressThreads), (unsigned)b);

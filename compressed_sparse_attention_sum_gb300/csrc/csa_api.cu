@@ -285,6 +285,77 @@ csa_status_t csa_compress_overlap_bwd(const void* kv, long long kv_batch_stride,
                                                     dt == CSA_BF16, (cudaStream_t)stream));
 }
 
+// Arguments of the normalization and rotary embedding of the pooled rows.
+static csa_status_t check_norm_rope(const float* weight, float eps, int rope_dim, float base,
+                                    int d) {
+  if (weight == nullptr || !aligned16(weight)) return CSA_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || eps > 1e30f) return CSA_ERR_INVALID_ARG;
+  if (rope_dim < 0 || rope_dim > d || rope_dim % 2 != 0) return CSA_ERR_INVALID_ARG;
+  if (rope_dim > 0 && !(base > 0.f && base < 1e30f)) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+csa_status_t csa_compress_norm_rope(const void* kv, long long kv_batch_stride, const void* score,
+                                    int score_width, const float* norm_weight, float eps,
+                                    int rope_dim, float rope_base, void* out,
+                                    long long out_batch_stride, int b, int sq, int d, int ratio,
+                                    csa_dtype_t dt, csa_stream_t stream) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (kv == nullptr || score == nullptr || out == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(kv) || !aligned16(score) || !aligned16(out)) return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || d < 8 || d % 8 != 0 || ratio < 1 || sq < ratio)
+    return CSA_ERR_INVALID_ARG;
+  if (score_width != 1 && score_width != d) return CSA_ERR_INVALID_ARG;
+  if (check_norm_rope(norm_weight, eps, rope_dim, rope_base, d) != CSA_OK)
+    return CSA_ERR_INVALID_ARG;
+  const int n_c = sq / ratio;
+  if (kv_batch_stride < (long long)sq * d || out_batch_stride < (long long)n_c * d)
+    return CSA_ERR_INVALID_ARG;
+  const int esz = dt == CSA_BF16 ? 2 : 4;
+  if ((kv_batch_stride * esz) % 16 != 0 || (out_batch_stride * esz) % 16 != 0)
+    return CSA_ERR_INVALID_ARG;
+  if (d > kMaxD) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(csa::launch_compress_norm_rope(kv, kv_batch_stride, score, score_width,
+                                                  norm_weight, eps, rope_dim, rope_base, out,
+                                                  out_batch_stride, b, sq, d, ratio,
+                                                  dt == CSA_BF16, (cudaStream_t)stream));
+}
+
+csa_status_t csa_compress_norm_rope_bwd(const void* kv, long long kv_batch_stride,
+                                        const void* score, int score_width,
+                                        const float* norm_weight, float eps, int rope_dim,
+                                        float rope_base, const float* dout,
+                                        long long dout_batch_stride, float* dkv,
+                                        long long dkv_batch_stride, float* dscore,
+                                        float* dnorm_weight, int b, int sq, int d, int ratio,
+                                        csa_dtype_t dt, csa_stream_t stream) {
+  if (!valid_dtype(dt)) return CSA_ERR_INVALID_ARG;
+  if (kv == nullptr || score == nullptr || dout == nullptr || dkv == nullptr ||
+      dscore == nullptr || dnorm_weight == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned16(kv) || !aligned16(score) || !aligned16(dout) || !aligned16(dkv) ||
+      !aligned16(dscore) || !aligned16(dnorm_weight))
+    return CSA_ERR_INVALID_ARG;
+  if (b < 1 || sq < 1 || d < 8 || d % 8 != 0 || ratio < 1 || sq < ratio)
+    return CSA_ERR_INVALID_ARG;
+  if (score_width != 1 && score_width != d) return CSA_ERR_INVALID_ARG;
+  if (check_norm_rope(norm_weight, eps, rope_dim, rope_base, d) != CSA_OK)
+    return CSA_ERR_INVALID_ARG;
+  const int n_c = sq / ratio;
+  if (kv_batch_stride < (long long)sq * d || dkv_batch_stride < (long long)sq * d ||
+      dout_batch_stride < (long long)n_c * d)
+    return CSA_ERR_INVALID_ARG;
+  const int esz = dt == CSA_BF16 ? 2 : 4;
+  if ((kv_batch_stride * esz) % 16 != 0 || (dout_batch_stride * 4) % 16 != 0 ||
+      (dkv_batch_stride * 4) % 16 != 0)
+    return CSA_ERR_INVALID_ARG;
+  if (d > kMaxD) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(csa::launch_compress_norm_rope_bwd(
+      kv, kv_batch_stride, score, score_width, norm_weight, eps, rope_dim, rope_base, dout,
+      dout_batch_stride, dkv, dkv_batch_stride, dscore, dnorm_weight, b, sq, d, ratio,
+      dt == CSA_BF16, (cudaStream_t)stream));
+}
+
 size_t csa_indexer_topk_min_workspace(int b, int n_c) {
   if (b < 1 || n_c < 1) return 0;
   return csa::indexer_min_chunk_bytes(b, n_c);

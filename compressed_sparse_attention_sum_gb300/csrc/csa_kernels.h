@@ -39,6 +39,19 @@ cudaError_t launch_compress_overlap_bwd(const void* kv, long long kv_bs, const v
                                         int sq, int d, int ratio, int coff, bool bf16,
                                         cudaStream_t s);
 
+// Compressor followed by the RMS normalization and the rotary embedding of
+// each pooled row, and the gradient of the three (dweight [d] zeroed here).
+cudaError_t launch_compress_norm_rope(const void* kv, long long kv_bs, const void* score,
+                                      int score_width, const float* weight, float eps,
+                                      int rope_dim, float base, void* out, long long out_bs,
+                                      int b, int sq, int d, int ratio, bool bf16, cudaStream_t s);
+cudaError_t launch_compress_norm_rope_bwd(const void* kv, long long kv_bs, const void* score,
+                                          int score_width, const float* weight, float eps,
+                                          int rope_dim, float base, const float* g,
+                                          long long g_bs, float* dkv, long long dkv_bs,
+                                          float* dscore, float* dweight, int b, int sq, int d,
+                                          int ratio, bool bf16, cudaStream_t s);
+
 cudaError_t launch_zero_f32(float* p, size_t n, cudaStream_t s);
 // Two buffers in one launch (b may be null with nb = 0).
 cudaError_t launch_zero_f32_pair(float* a, size_t na, float* b, size_t nb, cudaStream_t s);

@@ -10,8 +10,10 @@
  *                     rows + per-head sink; returns O and LSE
  *   csa_attn_bwd      dQ, dKV, dSink, accumulated in fp32
  *
- * Further calls: packed documents (the doc_ids argument of the indexer and
- * the attention), the indexer's training path (csa_indexer_teacher,
+ * Further calls: the normalization and rotary embedding of the pooled rows
+ * (csa_compress_norm_rope and its backward), packed documents (the doc_ids
+ * argument of the indexer and the attention), the indexer's training path
+ * (csa_indexer_teacher,
  * csa_indexer_loss), overlapping compression (csa_compress_overlap and its
  * backward), an FP8 indexer (csa_quantize_e4m3, csa_indexer_topk_fp8), an
  * indexer that needs no caller workspace (csa_indexer_topk_noalloc) and
@@ -182,6 +184,63 @@ csa_status_t csa_compress_overlap_bwd(const void* kv, long long kv_batch_stride,
                                       float* dkv, long long dkv_batch_stride, float* dscore,
                                       int b, int sq, int d, int ratio, int coff,
                                       csa_dtype_t dt, csa_stream_t stream);
+
+/*
+ * csa_compress_norm_rope - csa_compress followed by the normalization and the
+ * rotary embedding of each pooled row.
+ *
+ * "Add unfused SBHD compressed sparse attention", compressor review: the
+ * pooled row is cast once to dt and then normalized (kv = self.norm(kv));
+ * its config fields give the rotary base of compressed KV positions
+ * (csa_compress_rotary_base = 40000).  The norm's type, the rotary channels
+ * and the compressed positions are not given; this call's readings: with x
+ * the pooled row after its cast to dt,
+ *   y = x / sqrt(mean_c(x^2) + eps) * norm_weight          (fp32)
+ *   y[2i'], y[2i'+1] of the last rope_dim channels (i' = the pair's index in
+ *   the rotary part, channel pairs interleaved) turned by the angle
+ *   pos_j * rope_base^(-2 i' / rope_dim), pos_j = (j+1)*ratio - 1 (the
+ *   position of the entry's last pooled token),
+ *   out[b, j, :] = y cast once to dt.
+ * The angles are formed in double precision.  rope_dim = 0: no rotation.
+ *
+ *   kv, score, out, strides, sizes, dt   as csa_compress
+ *   norm_weight  in  [d] fp32, 16-byte aligned
+ *   eps          >= 0 (finite)
+ *   rope_dim     even, 0 <= rope_dim <= d;  rope_base > 0 when rope_dim > 0
+ * Errors: as csa_compress, plus INVALID_ARG for a null or misaligned weight,
+ * a negative or non-finite eps, an odd or out-of-range rope_dim, a
+ * non-positive rope_base.
+ */
+csa_status_t csa_compress_norm_rope(const void* kv, long long kv_batch_stride,
+                                    const void* score, int score_width,
+                                    const float* norm_weight, float eps, int rope_dim,
+                                    float rope_base, void* out, long long out_batch_stride,
+                                    int b, int sq, int d, int ratio, csa_dtype_t dt,
+                                    csa_stream_t stream);
+
+/*
+ * csa_compress_norm_rope_bwd - gradient of csa_compress_norm_rope.
+ *
+ * dout [b, n_c, d] fp32 (batch stride dout_batch_stride) is the gradient of
+ * the output rows.  With x the cast pooled row, xh = x / rms and dy = dout
+ * turned back by the rotation's angle:
+ *   dnorm_weight[c] = sum over all rows of dy[c] * xh[c]  (zeroed by the call)
+ *   dx = (dy * norm_weight - xh * mean_c(dy * norm_weight * xh)) / rms
+ * and dx passes the cast unchanged into the pooling's gradient, as in
+ * csa_compress_bwd: dkv += w_t dx (accumulated), dscore written.
+ *   other arguments as csa_compress_bwd and csa_compress_norm_rope
+ * Errors: as csa_compress_bwd, plus those of csa_compress_norm_rope and
+ * INVALID_ARG for a null dnorm_weight.  dnorm_weight is summed with fp32
+ * atomics (reproducible to rounding only).
+ */
+csa_status_t csa_compress_norm_rope_bwd(const void* kv, long long kv_batch_stride,
+                                        const void* score, int score_width,
+                                        const float* norm_weight, float eps, int rope_dim,
+                                        float rope_base, const float* dout,
+                                        long long dout_batch_stride, float* dkv,
+                                        long long dkv_batch_stride, float* dscore,
+                                        float* dnorm_weight, int b, int sq, int d, int ratio,
+                                        csa_dtype_t dt, csa_stream_t stream);
 
 /*
  * Bytes of indexer workspace that csa_indexer_topk uses by default: the

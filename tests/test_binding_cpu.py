@@ -21,6 +21,11 @@ CALLS = {
     "csa_compress_overlap": lambda: csa.csa_compress_overlap(_t(1, 8, 8), _t(1, 8, 8), 4, 2),
     "csa_compress_overlap_bwd": lambda: csa.csa_compress_overlap_bwd(
         _t(1, 8, 8), _t(1, 8, 8), 4, 2, _t(1, 2, 8, dtype=f32), _t(1, 8, 8, dtype=f32)),
+    "csa_compress_norm_rope": lambda: csa.csa_compress_norm_rope(
+        _t(1, 8, 8), _t(1, 8, 8), 4, _t(8, dtype=f32), 1e-6, 4),
+    "csa_compress_norm_rope_bwd": lambda: csa.csa_compress_norm_rope_bwd(
+        _t(1, 8, 8), _t(1, 8, 8), 4, _t(8, dtype=f32), 1e-6, 4, 40000.0,
+        _t(1, 2, 8, dtype=f32), _t(1, 8, 8, dtype=f32)),
     "csa_indexer_topk": lambda: csa.csa_indexer_topk(_t(1, 8, 2, 16), _t(1, 2, 16),
                                                      _t(1, 8, 2, dtype=f32), 2, 4),
     "csa_quantize_e4m3": lambda: csa.csa_quantize_e4m3(_t(4, 16)),

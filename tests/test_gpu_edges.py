@@ -209,8 +209,13 @@ def test_tc_forward_dense_mode_and_large_logits(H):
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("score_width", [1, "d"])
-def test_compress_fwd_bwd_ragged_and_scalar_score(dtype, score_width):
-    b, sq, d, ratio = 2, 43, 24, 5          # 3 tokens past the last block
+@pytest.mark.parametrize("b,sq,d,ratio", [
+    (2, 43, 24, 5),        # one thread per block and 8 channels; 3 tokens past the last block
+    (2, 200, 24, 37),      # token-split kernel: odd ratio, 3 channel groups, 15-token tail
+    (1, 300, 512, 128),    # token-split kernel at the HCA ratio, d = 512, 44-token tail
+    (1, 1091, 64, 17),     # token-split kernel, ratio just above its threshold
+])
+def test_compress_fwd_bwd_ragged_and_scalar_score(dtype, score_width, b, sq, d, ratio):
     g = torch.Generator().manual_seed(11)
     sw = d if score_width == "d" else 1
     kv = torch.randn(b, sq, d, generator=g).to(_dt(dtype))
@@ -225,4 +230,5 @@ def test_compress_fwd_bwd_ragged_and_scalar_score(dtype, score_width):
     ref_dkv, ref_ds = orc.compress_bwd(f64(kv), f64(score), ratio, f64(dout))
     assert maxabs(f64(dkv), ref_dkv) <= tol
     assert maxabs(f64(dscore), ref_ds) <= tol
-    assert torch.all(dkv[:, 40:] == 0) and torch.all(dscore[:, 40:] == 0)
+    n_tok = sq // ratio * ratio
+    assert torch.all(dkv[:, n_tok:] == 0) and torch.all(dscore[:, n_tok:] == 0)
