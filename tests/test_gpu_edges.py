@@ -85,6 +85,38 @@ def test_ragged_shapes(dtype, shape):
     _run_both(q, kv, idx, snk, dO, shape["ratio"], shape["window"], dtype)
 
 
+# ---------------------------------------------------------------------------
+# the production-width tensor-core forward (bf16, d = 512, H = 64)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", [
+    dict(b=2, sq=300, ratio=4, window=40, K=30, sink=True),     # repeats, -1, out of range
+    dict(b=1, sq=261, ratio=3, window=1, K=200, sink=False),    # window 1, no sink, K > n_c
+    dict(b=1, sq=700, ratio=4, window=128, K=175, sink=True),   # several slot tiles
+    dict(b=1, sq=9, ratio=4, window=3, K=2, sink=True),         # n_c = 2, ragged tail
+])
+def test_tc512_forward_edges(case):
+    """The transposed tcgen05 forward at the production width against the
+    oracle (the backward runs on the warp-MMA kernel at this width)."""
+    c = dict(case)
+    sink = c.pop("sink")
+    q, kv, idx, snk, dO = _rand_attn(12, H=64, d=512, dtype="bf16", sink=sink, **c)
+    _run_both(q, kv, idx, snk, dO, c["ratio"], c["window"], "bf16")
+
+
+def test_tc512_forward_large_logits_and_dense_mode():
+    """The running maximum grows by far more than 2^8 between slot tiles, so
+    O and the sums are rescaled: the window rows (the first tiles) are small
+    and the compressed rows (later tiles, dense list) large in logit, while
+    every row stays of unit size so that |O| <= 4 (the bf16 output's rounding
+    stays inside the bound)."""
+    b, sq, ratio, W = 1, 1100, 4, 256
+    q, kv, _, snk, dO = _rand_attn(13, b, sq, 64, 512, ratio, W, 1, "bf16")
+    kv[:, :sq] = (kv[:, :sq].float() * 0.05).to(torch.bfloat16)
+    q = (q.float() * 4).to(torch.bfloat16)
+    _run_both(q, kv, None, snk, dO, ratio, W, "bf16")
+
+
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 def test_dense_mode_matches_all_visible_list(dtype):
     b, sq, H, d, ratio, W = 2, 300, 8, 128, 16, 24
