@@ -266,6 +266,9 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
     dev = torch.device("cuda", local_rank)
     from compressed_sparse_attention_sum_gb300.shard import config_ranges, layer_rows
     cfg = CONFIGS[workload or args.workload]
+    if getattr(args, "seq_len", 0) or getattr(args, "batch", 0):
+        cfg = cfg.with_(name=cfg.name + "_resized", sq=args.seq_len or cfg.sq,
+                        b=args.batch or cfg.b)
     # N > 1: the ranks split the layer's query rows (contiguous ranges of equal
     # estimated work) and sum their dkv / dsink contributions with one
     # all-reduce; N = 1 runs the whole layer
@@ -736,6 +739,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing")
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload (one JSON line each, no variants, no e2e)")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="profiling aid: run the workload at this sq (not a bench line)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="profiling aid: run the workload at this b (not a bench line)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -16,10 +16,12 @@
 // B operand of S^T; P (16 KB, one 128-byte row of 64 heads per slot) is the
 // MN-major B operand of O^T.
 //
-// Each thread owns one slot (TMEM lane) and 32 heads in the softmax, so the
+// Each thread owns one slot (TMEM lane) and 16 heads in the softmax, so the
 // per-head maximum and sum over a tile's 128 slots are reductions across
-// lanes: a transposing butterfly (31 shuffles) leaves lane l with head l's
-// value, and four shared-memory entries per head join the lane quarters.
+// lanes: a transposing butterfly (16 shuffles) leaves lanes l and l + 16 with
+// head l's value, and four shared-memory entries per head join the lane
+// quarters.  O is normalized by the sum of the bf16-rounded probabilities
+// that enter its product (a convex combination), the LSE by the exact sum.
 // The running maximum is kept per head; O^T and the sums are rescaled only
 // when a head's maximum grows by more than 2^8 (the sink is the initial
 // state: m = sink, mass 1).  Slots are the query's window rows followed by
@@ -38,7 +40,7 @@ using namespace csa::umma;
 constexpr int kD = 512;
 constexpr int kH = 64;
 constexpr int kSlots = 128;
-constexpr int kThreads = 256;                  // 8 warps: TMEM lane quarter x head half
+constexpr int kThreads = 512;                  // 16 warps: TMEM lane quarter x head quarter
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 128;     // S^T: 64 columns; O^T: 4 x 64 columns
 constexpr uint32_t kQBlk = kH * 128;           // 8 KB: 64 head rows of 128 B
@@ -52,8 +54,8 @@ struct Layout {
   static constexpr uint32_t BARS = P + kSlots * 128;     // q, s, o
   static constexpr uint32_t TSLOT = BARS + 3 * 8;
   static constexpr uint32_t FLAG = TSLOT + 8;            // any-rescale flag, slot count
-  static constexpr uint32_t RED = FLAG + 8;              // [4][64] floats
-  static constexpr uint32_t MRUN = RED + 4 * kH * 4;     // [64] running max (log2)
+  static constexpr uint32_t RED = FLAG + 8;              // [2][4][64] floats
+  static constexpr uint32_t MRUN = RED + 8 * kH * 4;     // [64] running max (log2)
   static constexpr uint32_t FAC = MRUN + kH * 4;         // [64] rescale factor of the tile
   static constexpr uint32_t LSINK = FAC + kH * 4;        // [64] sink mass
   static constexpr uint32_t ROWS = LSINK + kH * 4;       // slot rows
@@ -65,13 +67,14 @@ __device__ __forceinline__ uint32_t kv_off(int r, int ch) {
   return (uint32_t)((ch >> 3) * kKvBlk + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
-// Transposing butterfly over the 32 lanes: v[c] holds this lane's value of
-// column c; afterwards lane l holds op over all lanes of column l in v[0].
+// Transposing butterfly over the 32 lanes: v[c] (c < 16) holds this lane's
+// value of column c; afterwards lanes l and l + 16 hold op over all 32 lanes
+// of column l % 16.
 template <bool kMax>
-__device__ __forceinline__ float lane_transpose_reduce(float (&v)[32]) {
+__device__ __forceinline__ float lane_transpose_reduce16(float (&v)[16]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int off = 16, n = 16; off >= 1; off >>= 1, n >>= 1) {
+  for (int off = 8, n = 8; off >= 1; off >>= 1, n >>= 1) {
     const bool up = (lane & off) != 0;
 #pragma unroll
     for (int i = 0; i < n; ++i) {
@@ -81,7 +84,8 @@ __device__ __forceinline__ float lane_transpose_reduce(float (&v)[32]) {
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  return v[0];
+  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return kMax ? fmaxf(v[0], other) : v[0] + other;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
@@ -144,13 +148,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
   const int S_total = flag[1];
   const int ntiles = (S_total + kSlots - 1) / kSlots;
 
-  const int qd = warp & 3, hf = warp >> 2;
+  const int qd = warp & 3, hq = warp >> 2;             // lane quarter, head quarter
   const int r = qd * 32 + lane;                        // TMEM lane: slot (S^T) or d (O^T)
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   const float sc2 = scale * kLog2e;
-  float l_part[32];                                    // this slot lane's mass per head
-#pragma unroll
-  for (int c = 0; c < 32; ++c) l_part[c] = 0.f;
+  float l_part[16], lr_part[16];                       // this slot lane's mass per head:
+#pragma unroll                                         // exact, and of the rounded P
+  for (int c = 0; c < 16; ++c) l_part[c] = lr_part[c] = 0.f;
 
   bool ok = __syncthreads_and(mbar_wait(bar_q, 0));
   int site = ok ? 0 : kSiteFwdQ;
@@ -194,18 +198,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
 
     // ---- softmax over the tile's slots, per head --------------------------
     const float bias = sbase + r < S_total ? 0.f : -INFINITY;
-    float x[32];
+    float x[16];
     {
-      uint32_t v[32];
-      tmem_ld32_wait(tmem + lane_base + kColS + hf * 32, v);
+      uint32_t v[16];
+      tmem_ld16_wait(tmem + lane_base + kColS + hq * 16, v);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) x[c] = fmaf(__uint_as_float(v[c]), sc2, bias);
+      for (int c = 0; c < 16; ++c) x[c] = fmaf(__uint_as_float(v[c]), sc2, bias);
     }
     {
-      float mx[32];
+      float mx[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) mx[c] = x[c];
-      red[qd * kH + hf * 32 + lane] = lane_transpose_reduce<true>(mx);
+      for (int c = 0; c < 16; ++c) mx[c] = x[c];
+      const float m = lane_transpose_reduce16<true>(mx);
+      if (lane < 16) red[qd * kH + hq * 16 + lane] = m;
     }
     if (tid == 0) flag[0] = 0;
     __syncthreads();
@@ -225,43 +230,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
     __syncthreads();
     if (flag[0]) {                                     // CTA-uniform
 #pragma unroll
-      for (int c = 0; c < 32; ++c) l_part[c] *= fac[hf * 32 + c];
+      for (int c = 0; c < 16; ++c) {
+        l_part[c] *= fac[hq * 16 + c];
+        lr_part[c] *= fac[hq * 16 + c];
+      }
       if (it > 0) {
-        // rescale O^T: this thread's d lane of M-tiles 2hf, 2hf+1, all heads
+        // rescale O^T: this thread's d lane of M-tile hq, all heads
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const uint32_t ta = tmem + lane_base + kColO + hq * kH + h2 * 32;
+          uint32_t v[32];
+          tmem_ld32_wait(ta, v);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const uint32_t ta = tmem + lane_base + kColO + (2 * hf + mt) * kH + h2 * 32;
-            uint32_t v[32];
-            tmem_ld32_wait(ta, v);
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              v[c] = __float_as_uint(__uint_as_float(v[c]) * fac[h2 * 32 + c]);
-            CSA_TMEM_ST32(ta, v);
-          }
+          for (int c = 0; c < 32; ++c)
+            v[c] = __float_as_uint(__uint_as_float(v[c]) * fac[h2 * 32 + c]);
+          CSA_TMEM_ST32(ta, v);
+          tmem_wait_st();
         }
-        tmem_wait_st();
       }
     }
-    // P = 2^(x - m) as bf16 into this slot's row of the P tile (heads of this
-    // half: 64 bytes = 4 swizzled 16-byte chunks)
+    // P = 2^(x - m) as bf16 into this slot's row of the P tile (this thread's
+    // 16 heads: 32 bytes = 2 swizzled 16-byte chunks)
     unsigned char* prow = sm + Layout::P + r * 128;
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
-      float p[8];
+    for (int c8 = 0; c8 < 2; ++c8) {
+      uint32_t pk[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
+      for (int e = 0; e < 8; e += 2) {
         const int c = c8 * 8 + e;
-        p[e] = ex2(x[c] - m_run[hf * 32 + c]);          // masked slots: 2^-inf = 0
-        l_part[c] += p[e];
+        const float p0 = ex2(x[c] - m_run[hq * 16 + c]);   // masked slots: 2^-inf = 0
+        const float p1 = ex2(x[c + 1] - m_run[hq * 16 + c + 1]);
+        l_part[c] += p0;
+        l_part[c + 1] += p1;
+        const __nv_bfloat162 h2v = __floats2bfloat162_rn(p0, p1);
+        const float2 back = __bfloat1622float2(h2v);
+        lr_part[c] += back.x;
+        lr_part[c + 1] += back.y;
+        pk[e / 2] = *reinterpret_cast<const uint32_t*>(&h2v);
       }
-      uint4 u;
-      u.x = pack_bf16x2(p[0], p[1]);
-      u.y = pack_bf16x2(p[2], p[3]);
-      u.z = pack_bf16x2(p[4], p[5]);
-      u.w = pack_bf16x2(p[6], p[7]);
-      *reinterpret_cast<uint4*>(prow + ((((hf * 4 + c8) ^ (r & 7))) << 4)) = u;
+      *reinterpret_cast<uint4*>(prow + ((((hq * 2 + c8) ^ (r & 7))) << 4)) =
+          make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
     fence_proxy_async_smem();
     fence_before();
@@ -293,29 +301,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
   fence_after();
 
   // ---- epilogue: per-head mass, LSE, O = O^T^T / l ------------------------------
-  red[qd * kH + hf * 32 + lane] = lane_transpose_reduce<false>(l_part);
+  {
+    const float le = lane_transpose_reduce16<false>(l_part);
+    const float lr = lane_transpose_reduce16<false>(lr_part);
+    if (lane < 16) {
+      red[qd * kH + hq * 16 + lane] = le;
+      red[4 * kH + qd * kH + hq * 16 + lane] = lr;
+    }
+  }
   __syncthreads();
   if (tid < kH) {
     const float l_tot = (red[tid] + red[kH + tid]) + (red[2 * kH + tid] + red[3 * kH + tid]) +
                         lsink[tid];
-    fac[tid] = 1.f / l_tot;
+    const float* rr = red + 4 * kH;
+    const float lr_tot = (rr[tid] + rr[kH + tid]) + (rr[2 * kH + tid] + rr[3 * kH + tid]) +
+                         lsink[tid];
+    fac[tid] = 1.f / lr_tot;
     if (ok) lse[((long long)bi * sq + t) * kH + tid] = (m_run[tid] + log2f(l_tot)) * kLn2;
   }
   __syncthreads();
   if (ok) {
     __nv_bfloat16* orow = o + ((long long)bi * sq + t) * kH * kD;
+    const int dcol = hq * 128 + r;                     // this thread's d
+#pragma unroll 1
+    for (int h4 = 0; h4 < 4; ++h4) {
+      uint32_t v[16];
+      tmem_ld16_wait(tmem + lane_base + kColO + hq * kH + h4 * 16, v);
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int dcol = (2 * hf + mt) * 128 + r;      // this thread's d
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t v[32];
-        tmem_ld32_wait(tmem + lane_base + kColO + (2 * hf + mt) * kH + h2 * 32, v);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int h = h2 * 32 + c;
-          orow[(long long)h * kD + dcol] = __float2bfloat16_rn(__uint_as_float(v[c]) * fac[h]);
-        }
+      for (int c = 0; c < 16; ++c) {
+        const int h = h4 * 16 + c;
+        orow[(long long)h * kD + dcol] = __float2bfloat16_rn(__uint_as_float(v[c]) * fac[h]);
       }
     }
   }
