@@ -46,13 +46,14 @@ constexpr uint32_t kColS = 0, kColO = 128;     // S^T: 64 columns; O^T: 4 x 64 c
 constexpr uint32_t kQBlk = kH * 128;           // 8 KB: 64 head rows of 128 B
 constexpr uint32_t kKvBlk = kSlots * 128;      // 16 KB: 128 slot rows of 128 B
 constexpr float kRescale = 8.f;                // lazy rescale threshold (log2 domain)
+constexpr int kGather = kThreads - 32;         // warps 1-15 gather the KV tiles
 
 struct Layout {
   static constexpr uint32_t Q = 0;                       // [8][64 rows][128 B]
   static constexpr uint32_t KV = 8 * kQBlk;              // [8][128 rows][128 B]
   static constexpr uint32_t P = KV + 8 * kKvBlk;         // [128 rows][128 B]
-  static constexpr uint32_t BARS = P + kSlots * 128;     // q, s, o
-  static constexpr uint32_t TSLOT = BARS + 3 * 8;
+  static constexpr uint32_t BARS = P + kSlots * 128;     // q, s, kv[4], o[4]
+  static constexpr uint32_t TSLOT = BARS + 10 * 8;
   static constexpr uint32_t FLAG = TSLOT + 8;            // any-rescale flag, slot count
   static constexpr uint32_t RED = FLAG + 8;              // [2][4][64] floats
   static constexpr uint32_t MRUN = RED + 8 * kH * 4;     // [64] running max (log2)
@@ -65,6 +66,21 @@ struct Layout {
 // KV tile (eight 64-element K blocks of 128 rows).
 __device__ __forceinline__ uint32_t kv_off(int r, int ch) {
   return (uint32_t)((ch >> 3) * kKvBlk + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+// 16-byte asynchronous copy that reads src_bytes (16 or 0) and zero-fills
+// the rest: a padding slot becomes zeros through the same copy path.
+__device__ __forceinline__ void cp_async_16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Transposing butterfly over the 32 lanes: v[c] (c < 16) holds this lane's
@@ -98,8 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + Layout::BARS);
-  uint64_t* bar_s = bar_q + 1;
-  uint64_t* bar_o = bar_q + 2;
+  uint64_t* bar_s = bar_q + 1;          // S^T of the tile complete
+  uint64_t* bar_kv = bar_q + 2;         // [4] the tile's d-block pair mt gathered
+  uint64_t* bar_of = bar_q + 6;         // [4] O^T M-tile mt of the tile complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Layout::TSLOT);
   int* flag = reinterpret_cast<int*>(sm + Layout::FLAG);
   float* red = reinterpret_cast<float*>(sm + Layout::RED);
@@ -119,7 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
   if (tid == 0) {
     mbar_init(bar_q, 1);
     mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bar_kv[i], kGather);
+      mbar_init(&bar_of[i], 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -158,43 +178,73 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
 
   bool ok = __syncthreads_and(mbar_wait(bar_q, 0));
   int site = ok ? 0 : kSiteFwdQ;
+  bool fail = false;                                   // a bounded wait of this thread gave up
 
-  for (int it = 0; it < ntiles && ok; ++it) {
-    if (it > 0) {
-      ok = __syncthreads_and(mbar_wait(bar_o, (it - 1) & 1));
-      if (!ok) { site = kSiteFwdO; break; }
-    }
-    // gather the tile's KV rows (16-byte chunks into the swizzled K-major
-    // layout); padding slots past the list are zero-filled
+  // Gather of tile it by warps 1-15, one pair of 64-wide d blocks at a time:
+  // pair mt of the KV buffer is free once the previous tile's O^T M-tile mt
+  // (which reads those blocks) has completed; its arrival is signalled on
+  // bar_kv[mt] so that the S^T K-steps over it can start.  Padding slots past
+  // the list are zero-filled by the same copies.
+  auto gather = [&](int it) {
+    const int g = tid - 32;
     const int sbase = it * kSlots;
-    for (int c = tid; c < kSlots * 64; c += kThreads) {
-      const int rr = c >> 6, ch = c & 63;
-      const int s = sbase + rr;
-      if (s >= S_total) {
-        *reinterpret_cast<uint4*>(sm + Layout::KV + kv_off(rr, ch)) = make_uint4(0u, 0u, 0u, 0u);
-        continue;
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+      bool good = true;
+      if (it > 0) good = mbar_wait(&bar_of[mt], (it - 1) & 1);
+      fail |= !good;
+      if (good) {
+        for (int c = g; c < kSlots * 16; c += kGather) {
+          const int rr = c >> 4, ch = mt * 16 + (c & 15);
+          const int s = sbase + rr;
+          const bool pad = s >= S_total;
+          const __nv_bfloat16* src = kv_b + (pad ? 0ll : (long long)rows[s] * kD) + ch * 8;
+          cp_async_16_zfill(sm + Layout::KV + kv_off(rr, ch), src, pad ? 0u : 16u);
+        }
       }
-      cp_async_16(sm + Layout::KV + kv_off(rr, ch), kv_b + (long long)rows[s] * kD + ch * 8);
+      cp_async_commit();
+      if (mt > 0) {
+        cp_async_wait_group<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&bar_kv[mt - 1]);
+      }
     }
-    cp_async_wait_all_();
+    cp_async_wait_group<0>();
     fence_proxy_async_smem();
-    fence_before();
-    __syncthreads();
-    if (tid == 0) {
+    mbar_arrive(&bar_kv[3]);
+  };
+  // S^T of tile it, issued by one thread pair by pair as the gather lands
+  auto issue_s = [&](int it) {
+    constexpr uint32_t idesc = idesc_bf16_f32_major(kSlots, kH, 0, 0);
+    const uint32_t kva = smem_addr(sm + Layout::KV), qa = smem_addr(sm + Layout::Q);
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+      if (!mbar_wait(&bar_kv[mt], it & 1)) {
+        fail = true;
+        return;
+      }
       fence_after();
-      constexpr uint32_t idesc = idesc_bf16_f32_major(kSlots, kH, 0, 0);
-      const uint32_t kva = smem_addr(sm + Layout::KV), qa = smem_addr(sm + Layout::Q);
 #pragma unroll
-      for (int k = 0; k < kD / 16; ++k) {
+      for (int kk = 0; kk < 8; ++kk) {
+        const int k = mt * 8 + kk;
         const uint32_t ka = kva + (k >> 2) * kKvBlk + (k & 3) * 32;
         const uint32_t qb = qa + (k >> 2) * kQBlk + (k & 3) * 32;
         mma_bf16_ss(tmem + kColS, sw128_desc(ka), sw128_desc(qb), idesc, k > 0 ? 1u : 0u);
       }
-      mma_commit(bar_s);
     }
-    ok = __syncthreads_and(mbar_wait(bar_s, it & 1));
+    mma_commit(bar_s);
+  };
+  if (ok && ntiles > 0) {
+    if (warp > 0) gather(0);
+    else if (lane == 0) issue_s(0);
+  }
+
+  for (int it = 0; it < ntiles && ok; ++it) {
+    __syncwarp();
+    ok = __syncthreads_and(mbar_wait(bar_s, it & 1) && !fail);
     if (!ok) { site = kSiteFwdS; break; }
     fence_after();
+    const int sbase = it * kSlots;
 
     // ---- softmax over the tile's slots, per head --------------------------
     const float bias = sbase + r < S_total ? 0.f : -INFINITY;
@@ -235,7 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
         lr_part[c] *= fac[hq * 16 + c];
       }
       if (it > 0) {
-        // rescale O^T: this thread's d lane of M-tile hq, all heads
+        // rescale O^T: this thread's d lane of M-tile hq, all heads (the
+        // previous tile's MMAs into it have completed; the wait returns at once)
+        if (!mbar_wait(&bar_of[hq], (it - 1) & 1)) fail = true;
 #pragma unroll 1
         for (int h2 = 0; h2 < 2; ++h2) {
           const uint32_t ta = tmem + lane_base + kColO + hq * kH + h2 * 32;
@@ -289,14 +341,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc512_kernel(
           const uint64_t bdesc = sw128_desc_mn(pa + k * 2048, kKvBlk);
           mma_bf16_ss(tmem + kColO + mt * kH, a, bdesc, idesc, (it > 0 || k > 0) ? 1u : 0u);
         }
+        mma_commit(&bar_of[mt]);
       }
-      mma_commit(bar_o);
+    }
+    // the next tile's gather streams in behind these MMAs, and its S^T
+    // follows the gather
+    if (it + 1 < ntiles) {
+      if (warp > 0) gather(it + 1);
+      else if (lane == 0) issue_s(it + 1);
     }
   }
+  __syncwarp();
   if (ok && ntiles > 0) {
-    ok = __syncthreads_and(mbar_wait(bar_o, (ntiles - 1) & 1));
+    ok = __syncthreads_and(mbar_wait(&bar_of[hq], (ntiles - 1) & 1) && !fail);
     if (!ok) site = kSiteFwdLast;
   }
+  cp_async_wait_all_();                                // no copy in flight past this point
   if (!ok && tid == 0) set_status(status, kDevTimeout, site);
   fence_after();
 
