@@ -34,6 +34,12 @@ cudaError_t launch_quantize_e4m3(const void* x, long long rows, int d, bool bf16
                                  float* scale, cudaStream_t s);
 bool attn_mma_supported(int H, int d, int window, int K);
 bool attn_tc512_supported(int H, int d, int window, int Kl);
+bool attn_tc512_bwd_supported(int H, int d, int window, int Kl);
+cudaError_t launch_attn_bwd_tc512(const void* q, const void* kv, const int32_t* idx,
+                                  const float* sink, float scale, const float* lse,
+                                  const void* dO, float* dq, float* dkv, float* dsink, int b,
+                                  int sq, int n_c, int ratio, int window, int K, int* status,
+                                  cudaStream_t s, const int32_t* doc, int tb, int te);
 cudaError_t launch_attn_fwd_tc512(const void* q, const void* kv, const int32_t* idx,
                                   const float* sink, float scale, void* o, float* lse, int b,
                                   int sq, int n_c, int ratio, int window, int K, int* status,
@@ -525,6 +531,10 @@ csa_status_t attn_bwd_rows(const void* q, const void* kv_full, const int32_t* id
     return from_cuda(csa::launch_attn_bwd_tc(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                              dsink, b, sq, H, n_c, ratio, window, Kl,
                                              device_status_ptr(), s, doc_ids, tb, te));
+  if (dt == CSA_BF16 && !warp_mma_forced() && csa::attn_tc512_bwd_supported(H, d, window, Kl))
+    return from_cuda(csa::launch_attn_bwd_tc512(q, kv_full, idx, sink, scale, lse, dO, dq, dkv,
+                                                dsink, b, sq, n_c, ratio, window, Kl,
+                                                device_status_ptr(), s, doc_ids, tb, te));
   if (dt == CSA_BF16 && csa::attn_mma_supported(H, d, window, Kl))
     return from_cuda(csa::launch_attn_bwd_mma(q, kv_full, idx, sink, scale, o, lse, dO, dq, dkv,
                                               dsink, b, sq, H, d, n_c, ratio, window, Kl, s,

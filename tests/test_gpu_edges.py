@@ -96,8 +96,8 @@ def test_ragged_shapes(dtype, shape):
     dict(b=1, sq=9, ratio=4, window=3, K=2, sink=True),         # n_c = 2, ragged tail
 ])
 def test_tc512_forward_edges(case):
-    """The transposed tcgen05 forward at the production width against the
-    oracle (the backward runs on the warp-MMA kernel at this width)."""
+    """The transposed tcgen05 forward and backward at the production width
+    against the oracle."""
     c = dict(case)
     sink = c.pop("sink")
     q, kv, idx, snk, dO = _rand_attn(12, H=64, d=512, dtype="bf16", sink=sink, **c)

@@ -37,6 +37,7 @@ def _gpu():
 CASES = {
     "csa4_bf16": CONFIGS["csa4_bf16"],                                   # tcgen05 kernels
     "prod_small": CONFIGS["prod_bf16"].with_(name="prod_small", sq=512, b=1, H=16),  # d=512
+    "prod_tc": CONFIGS["prod_bf16"].with_(name="prod_tc", sq=264, b=2),   # tcgen05, d=512 H=64
     "hca_small": CONFIGS["hca_bf16"].with_(name="hca_small", sq=2048, b=2),      # dense lists
     "tiny_fp32": CONFIGS["tiny_fp32"],                                   # CUDA-core fp32
 }
