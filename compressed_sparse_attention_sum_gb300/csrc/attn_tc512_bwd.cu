@@ -18,7 +18,8 @@
 // dS (320 KB), so all three stream through it in pairs of 64-wide d blocks
 // (128 d: the KV rows of the tile 32 KB, Q and dO 16 KB each, the last two
 // by TMA from L2): the S^T / dP^T K-steps and the dQ^T M-tile / dKV chunk of
-// a pair run on the pair in place.  Pass 1 forms D = sum p dP exactly; pass 2
+// a pair run on the pair in place.  Two 64 KB stages: the next pair streams
+// in while the tensor core works on the current one.  Pass 1 forms D = sum p dP exactly; pass 2
 // forms P and dS * scale as bf16 hi + lo (about 16 significant bits, so the
 // fp32 sums of hot rows over thousands of queries stay accurate), then per
 // pair dQ^T and the tile's dKV chunk, which is added into the compact buffer
@@ -43,16 +44,20 @@ constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDKV = 384;
 constexpr uint32_t kKvBlk = kSlots * 128;       // 16 KB: 128 slot rows of 128 B
 constexpr uint32_t kHBlk = kH * 128;            // 8 KB: 64 head rows of 128 B
 
+constexpr uint32_t kStage = 2 * kKvBlk + 4 * kHBlk;   // 64 KB: KV, Q, dO of one d pair
+
 struct Layout {
-  static constexpr uint32_t KV = 0;                      // [2][128 rows][128 B] d-pair
-  static constexpr uint32_t Q = KV + 2 * kKvBlk;         // [2][64 rows][128 B]
-  static constexpr uint32_t G = Q + 2 * kHBlk;           // dO pair
-  static constexpr uint32_t PH = G + 2 * kHBlk;          // [128 slot rows][128 B]
+  // stage st at st * kStage: KV pair [2][128 rows][128 B], then Q pair
+  // [2][64 rows][128 B], then dO pair
+  static constexpr uint32_t KV = 0;
+  static constexpr uint32_t Q = 2 * kKvBlk;              // within a stage
+  static constexpr uint32_t G = Q + 2 * kHBlk;           // within a stage
+  static constexpr uint32_t PH = 2 * kStage;             // [128 slot rows][128 B]
   static constexpr uint32_t PL = PH + kKvBlk;
   static constexpr uint32_t DH = PL + kKvBlk;
   static constexpr uint32_t DL = DH + kKvBlk;
-  static constexpr uint32_t BARS = DL + kKvBlk;          // ld, mma
-  static constexpr uint32_t TSLOT = BARS + 2 * 8;
+  static constexpr uint32_t BARS = DL + kKvBlk;          // ld[2], mma
+  static constexpr uint32_t TSLOT = BARS + 3 * 8;
   static constexpr uint32_t SCAL = TSLOT + 8;            // slot count
   static constexpr uint32_t RED = SCAL + 8;              // [4][64] floats
   static constexpr uint32_t LSE2 = RED + 4 * kH * 4;     // [64]
@@ -109,8 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc512_kernel(
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + Layout::BARS);   // Q / dO pair by TMA
-  uint64_t* bar_mma = bar_ld + 1;                                       // MMA group done
+  uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + Layout::BARS);   // [2] Q / dO by TMA
+  uint64_t* bar_mma = bar_ld + 2;                                       // MMA group done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Layout::TSLOT);
   int* scal = reinterpret_cast<int*>(sm + Layout::SCAL);
   float* red = reinterpret_cast<float*>(sm + Layout::RED);
@@ -128,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc512_kernel(
   const long long qrow = ((long long)bi * sq + t) * kH;
 
   if (tid == 0) {
-    mbar_init(bar_ld, 1);
+    mbar_init(&bar_ld[0], 1);
+    mbar_init(&bar_ld[1], 1);
     mbar_init(bar_mma, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -150,134 +156,87 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc512_kernel(
   const int r = qd * 32 + lane;                        // TMEM lane: slot or d
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   const float sc2 = scale * kLog2e;
-  uint32_t n_ld = 0, n_mma = 0;                        // completed phases of the barriers
+  uint32_t n_mma = 0;                                  // completed phases of bar_mma
+  int n_issued = 0, n_waited = 0;                      // jobs whose stage was issued / waited
   bool ok = true;
   int site = 0;
 
-  // Stage the d-pair p (d in [128p, 128p + 128)) of tile `it`: the tile's KV
-  // rows (every thread, 16-byte copies, padding slots zero-filled) and the
-  // query's Q and dO (thread 0, TMA), then wait for all of it.
-  auto stage = [&](int it, int p) -> bool {
+  // The jobs of the query, in order: pass 1 (D) runs S^T / dP^T over the four
+  // d pairs of every tile; pass 2 runs, per tile, S^T / dP^T over the pairs,
+  // then dQ^T / dKV over the pairs.  Job j streams its pair into stage j & 1.
+  const int J1 = 4 * ntiles, J = 12 * ntiles;
+  auto job = [&](int j, int* it, int* p, bool* sdp) {
+    if (j < J1) {
+      *it = j >> 2; *p = j & 3; *sdp = true;
+    } else {
+      const int jj = j - J1;
+      *it = jj >> 3; *p = jj & 3; *sdp = (jj & 7) < 4;
+    }
+  };
+  // Issue the copies of job j's pair into stage j & 1: the tile's KV rows
+  // (every thread, 16-byte copies, padding slots zero-filled) and the
+  // query's Q and dO (thread 0, TMA).
+  auto stage_issue = [&](int j) {
+    int it, p;
+    bool sdp;
+    job(j, &it, &p, &sdp);
+    unsigned char* st = sm + (j & 1) * kStage;
     const int sbase = it * kSlots;
+    ++n_issued;
     for (int c = tid; c < kSlots * 16; c += kThreads) {
       const int rr = c >> 4, chp = c & 15;              // chunk within the pair's 128 d
       const int s = sbase + rr;
       const bool pad = s >= S_total;
       const __nv_bfloat16* src = kv_b + (pad ? 0ll : (long long)rows[s] * kD) + p * 128 + chp * 8;
       const uint32_t off = (chp >> 3) * kKvBlk + rr * 128 + ((((chp & 7) ^ (rr & 7))) << 4);
-      cp_async_16_zfill(sm + Layout::KV + off, src, pad ? 0u : 16u);
+      cp_async_16_zfill(st + Layout::KV + off, src, pad ? 0u : 16u);
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid == 0) {
-      mbar_expect_tx(bar_ld, 4 * kHBlk);
-      tma_load_2d(sm + Layout::Q, &tmap_q, bar_ld, p * 128, (int)qrow);
-      tma_load_2d(sm + Layout::Q + kHBlk, &tmap_q, bar_ld, p * 128 + 64, (int)qrow);
-      tma_load_2d(sm + Layout::G, &tmap_do, bar_ld, p * 128, (int)qrow);
-      tma_load_2d(sm + Layout::G + kHBlk, &tmap_do, bar_ld, p * 128 + 64, (int)qrow);
+      uint64_t* bl = &bar_ld[j & 1];
+      mbar_expect_tx(bl, 4 * kHBlk);
+      tma_load_2d(st + Layout::Q, &tmap_q, bl, p * 128, (int)qrow);
+      tma_load_2d(st + Layout::Q + kHBlk, &tmap_q, bl, p * 128 + 64, (int)qrow);
+      tma_load_2d(st + Layout::G, &tmap_do, bl, p * 128, (int)qrow);
+      tma_load_2d(st + Layout::G + kHBlk, &tmap_do, bl, p * 128 + 64, (int)qrow);
     }
+  };
+  // Wait for job j's stage (its copies are the only ones in flight here).
+  auto stage_wait = [&](int j) -> bool {
     cp_async_wait_all_();
     fence_proxy_async_smem();
-    const bool got = mbar_wait(bar_ld, n_ld & 1);
-    ++n_ld;
+    const bool got = mbar_wait(&bar_ld[j & 1], (j >> 1) & 1);
+    ++n_waited;
     fence_before();
     return __syncthreads_and(got);
   };
-  auto wait_mma = [&]() -> bool {
-    const bool got = __syncthreads_and(mbar_wait(bar_mma, n_mma & 1));
-    ++n_mma;
-    fence_after();
-    return got;
-  };
-  // S^T += KV_p Q_p^T and dP^T += KV_p dO_p^T over the pair's 128 d (8 K-steps)
-  auto issue_sdp = [&](int p) {
-    constexpr uint32_t idesc = idesc_bf16_f32_major(kSlots, kH, 0, 0);
-    const uint32_t kva = smem_addr(sm + Layout::KV), qa = smem_addr(sm + Layout::Q),
-                   ga = smem_addr(sm + Layout::G);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t ka = kva + (k >> 2) * kKvBlk + (k & 3) * 32;
-      const uint32_t qo = (k >> 2) * kHBlk + (k & 3) * 32;
-      const uint32_t acc = (p > 0 || k > 0) ? 1u : 0u;
-      mma_bf16_ss(tmem + kColS, sw128_desc(ka), sw128_desc(qa + qo), idesc, acc);
-      mma_bf16_ss(tmem + kColDP, sw128_desc(ka), sw128_desc(ga + qo), idesc, acc);
-    }
-    mma_commit(bar_mma);
-  };
-  // S^T and dP^T of tile `it`, all four pairs
-  auto tile_sdp = [&](int it) -> bool {
-    for (int p = 0; p < 4; ++p) {
-      if (!stage(it, p)) { site = kSiteBwdQ; return false; }
-      if (tid == 0) {
-        fence_after();
-        issue_sdp(p);
-      }
-      if (!wait_mma()) { site = kSiteBwdS; return false; }
-    }
-    return true;
-  };
 
-  // ---- pass 1: D_h = sum_i p_i dP_i ------------------------------------------
   float dpart[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c) dpart[c] = 0.f;
-  for (int it = 0; it < ntiles && ok; ++it) {
-    ok = tile_sdp(it);
-    if (!ok) break;
-    const float bias = it * kSlots + r < S_total ? 0.f : -INFINITY;
-    uint32_t vs[16], vp[16];
-    tmem_ld16_wait(tmem + lane_base + kColS + hq * 16, vs);
-    tmem_ld16_wait(tmem + lane_base + kColDP + hq * 16, vp);
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      dpart[c] = fmaf(ex2(fmaf(__uint_as_float(vs[c]), sc2, bias - lse2_s[hq * 16 + c])),
-                      __uint_as_float(vp[c]), dpart[c]);
-    fence_before();
-    __syncthreads();                                   // S^T / dP^T read before they are rewritten
-  }
-  {
-    const float v = lane_transpose_sum16(dpart);
-    if (lane < 16) red[qd * kH + hq * 16 + lane] = v;
-  }
-  __syncthreads();
-  if (tid < kH) D_s[tid] = (red[tid] + red[kH + tid]) + (red[2 * kH + tid] + red[3 * kH + tid]);
-  __syncthreads();
-
-  // ---- pass 2 ---------------------------------------------------------------------
   float Dh[16];
+  if (J > 0) stage_issue(0);
+  for (int j = 0; j < J && ok; ++j) {
+    int it, p;
+    bool sdp;
+    job(j, &it, &p, &sdp);
+    if (!stage_wait(j)) { ok = false; site = kSiteBwdQ; break; }
+    if (tid == 0) {
+      fence_after();
+      const uint32_t st = smem_addr(sm + (j & 1) * kStage);
+      const uint32_t kva = st + Layout::KV, qa = st + Layout::Q, ga = st + Layout::G;
+      if (sdp) {
+        // S^T += KV_p Q_p^T and dP^T += KV_p dO_p^T over the pair's 128 d
+        constexpr uint32_t idesc = idesc_bf16_f32_major(kSlots, kH, 0, 0);
 #pragma unroll
-  for (int c = 0; c < 16; ++c) Dh[c] = D_s[hq * 16 + c];
-  for (int it = 0; it < ntiles && ok; ++it) {
-    ok = tile_sdp(it);
-    if (!ok) break;
-    // P and dS * scale (hi + lo) into this slot's rows of PH/PL and DH/DL
-    {
-      const float bias = it * kSlots + r < S_total ? 0.f : -INFINITY;
-      uint32_t vs[16], vp[16];
-      tmem_ld16_wait(tmem + lane_base + kColS + hq * 16, vs);
-      tmem_ld16_wait(tmem + lane_base + kColDP + hq * 16, vp);
-#pragma unroll
-      for (int c8 = 0; c8 < 2; ++c8) {
-        float pv[8], dv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;
-          pv[e] = ex2(fmaf(__uint_as_float(vs[c]), sc2, bias - lse2_s[hq * 16 + c]));
-          dv[e] = pv[e] * (__uint_as_float(vp[c]) - Dh[c]) * scale;
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t ka = kva + (k >> 2) * kKvBlk + (k & 3) * 32;
+          const uint32_t qo = (k >> 2) * kHBlk + (k & 3) * 32;
+          const uint32_t acc = (p > 0 || k > 0) ? 1u : 0u;
+          mma_bf16_ss(tmem + kColS, sw128_desc(ka), sw128_desc(qa + qo), idesc, acc);
+          mma_bf16_ss(tmem + kColDP, sw128_desc(ka), sw128_desc(ga + qo), idesc, acc);
         }
-        const uint32_t off = r * 128 + ((((hq * 2 + c8) ^ (r & 7))) << 4);
-        store_hi_lo8(sm + Layout::PH, sm + Layout::PL, off, pv);
-        store_hi_lo8(sm + Layout::DH, sm + Layout::DL, off, dv);
-      }
-    }
-    fence_proxy_async_smem();
-    fence_before();
-    __syncthreads();
-    // per pair: dQ^T M-tile p and the tile's dKV chunk of the pair's 128 d
-    for (int p = 0; p < 4 && ok; ++p) {
-      if (!stage(it, p)) { ok = false; site = kSiteBwdQ; break; }
-      if (tid == 0) {
-        fence_after();
-        const uint32_t kva = smem_addr(sm + Layout::KV), qa = smem_addr(sm + Layout::Q),
-                       ga = smem_addr(sm + Layout::G);
+      } else {
         const uint32_t pha = smem_addr(sm + Layout::PH), pla = smem_addr(sm + Layout::PL);
         const uint32_t dha = smem_addr(sm + Layout::DH), dla = smem_addr(sm + Layout::DL);
         // dQ^T[d, h] += KV^T[d, slots] dS^T[slots, h]: A = the KV pair read
@@ -303,27 +262,78 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc512_kernel(
           mma_bf16_ss(tmem + kColDKV, sw128_desc(dha + k * 32), bq, idesc_kv, 1u);
           mma_bf16_ss(tmem + kColDKV, sw128_desc(dla + k * 32), bq, idesc_kv, 1u);
         }
-        mma_commit(bar_mma);
       }
-      if (!wait_mma()) { ok = false; site = kSiteBwdDS; break; }
+      mma_commit(bar_mma);
+    }
+    // the next job's pair streams into the other stage (the MMAs that read it
+    // last, those of job j - 1, have completed)
+    if (j + 1 < J) stage_issue(j + 1);
+    ok = __syncthreads_and(mbar_wait(bar_mma, n_mma & 1));
+    ++n_mma;
+    if (!ok) { site = sdp ? kSiteBwdS : kSiteBwdDS; break; }
+    fence_after();
+
+    if (sdp && p == 3) {
+      const float bias = it * kSlots + r < S_total ? 0.f : -INFINITY;
+      uint32_t vs[16], vp[16];
+      tmem_ld16_wait(tmem + lane_base + kColS + hq * 16, vs);
+      tmem_ld16_wait(tmem + lane_base + kColDP + hq * 16, vp);
+      if (j < J1) {
+        // pass 1: D = sum p dP
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          dpart[c] = fmaf(ex2(fmaf(__uint_as_float(vs[c]), sc2, bias - lse2_s[hq * 16 + c])),
+                          __uint_as_float(vp[c]), dpart[c]);
+      } else {
+        // pass 2: P and dS * scale (hi + lo) into this slot's rows of PH/PL, DH/DL
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8) {
+          float pv[8], dv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int c = c8 * 8 + e;
+            pv[e] = ex2(fmaf(__uint_as_float(vs[c]), sc2, bias - lse2_s[hq * 16 + c]));
+            dv[e] = pv[e] * (__uint_as_float(vp[c]) - Dh[c]) * scale;
+          }
+          const uint32_t off = r * 128 + ((((hq * 2 + c8) ^ (r & 7))) << 4);
+          store_hi_lo8(sm + Layout::PH, sm + Layout::PL, off, pv);
+          store_hi_lo8(sm + Layout::DH, sm + Layout::DL, off, dv);
+        }
+        fence_proxy_async_smem();
+      }
+      fence_before();
+      __syncthreads();                                 // S^T / dP^T read before they are rewritten
+      if (j == J1 - 1) {
+        // end of pass 1: D per head
+        const float v = lane_transpose_sum16(dpart);
+        if (lane < 16) red[qd * kH + hq * 16 + lane] = v;
+        __syncthreads();
+        if (tid < kH)
+          D_s[tid] = (red[tid] + red[kH + tid]) + (red[2 * kH + tid] + red[3 * kH + tid]);
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) Dh[c] = D_s[hq * 16 + c];
+      }
+    } else if (!sdp) {
       // add this slot's 128 d of the chunk into its compact dKV row (warp
       // (qd, hq) takes 32 of the columns)
-      {
-        uint32_t v[32];
-        tmem_ld32_wait(tmem + lane_base + kColDKV + hq * 32, v);
-        const int s = it * kSlots + r;
-        if (s < S_total) {
-          float* dst = dkv_b + (long long)rows[s] * kD + p * 128 + hq * 32;
+      uint32_t v[32];
+      tmem_ld32_wait(tmem + lane_base + kColDKV + hq * 32, v);
+      const int s = it * kSlots + r;
+      if (s < S_total) {
+        float* dst = dkv_b + (long long)rows[s] * kD + p * 128 + hq * 32;
 #pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            red_add_v4(dst + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                       __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-        }
+        for (int c = 0; c < 32; c += 4)
+          red_add_v4(dst + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                     __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
       }
       fence_before();
       __syncthreads();                                 // chunk read before it is rewritten
     }
   }
+  cp_async_wait_all_();                                // no copy in flight past this point
+  for (int j = n_waited; !ok && j < n_issued; ++j)     // nor a TMA load (bounded waits)
+    mbar_wait(&bar_ld[j & 1], (j >> 1) & 1);
   if (!ok && tid == 0) set_status(status, kDevTimeout, site);
 
   // ---- dq rows and the sink gradient --------------------------------------------
