@@ -13,7 +13,10 @@
 //   S^T = KV Q^T, dP^T = KV dO^T          (M = 128 slots, N = 64, K = 512)
 //   dQ^T [d, h] += KV^T dS^T              (four M = 128 tiles of d)
 //   dKV [slots, d] = P^T dO + dS^T Q      (M = 128 slots, N = 128 d at a time)
-// TMEM: S^T 64 columns, dP^T 64, dQ^T 256, one 128-column dKV chunk.
+// TMEM: S^T 64 columns, dP^T 64, dQ^T 256, one 128-column dKV chunk; the
+// chunks of odd pairs use those 128 columns and the chunks of even pairs the
+// S^T / dP^T columns (free once P and dS are formed), so that a chunk is
+// drained into the compact buffer while the next pair's MMAs run.
 // Q, dO and the tile's KV rows do not fit shared memory together with P and
 // dS (320 KB), so all three stream through it in pairs of 64-wide d blocks
 // (128 d: the KV rows of the tile 32 KB, Q and dO 16 KB each, the last two
@@ -41,6 +44,7 @@ constexpr int kSlots = 128;
 constexpr int kThreads = 512;                   // 16 warps: TMEM lane quarter x head quarter
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 64, kColDQ = 128, kColDKV = 384;
+__device__ __forceinline__ uint32_t dkv_col(int p) { return (p & 1) ? kColDKV : kColS; }
 constexpr uint32_t kKvBlk = kSlots * 128;       // 16 KB: 128 slot rows of 128 B
 constexpr uint32_t kHBlk = kH * 128;            // 8 KB: 64 head rows of 128 B
 
@@ -211,6 +215,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc512_kernel(
     return __syncthreads_and(got);
   };
 
+  // add a slot's 128 d of a pair's dKV chunk into its compact dKV row
+  // (warp (qd, hq) takes 32 of the columns)
+  auto drain = [&](int it, int p) {
+    uint32_t v[32];
+    tmem_ld32_wait(tmem + lane_base + dkv_col(p) + hq * 32, v);
+    const int s = it * kSlots + r;
+    if (s < S_total) {
+      float* dst = dkv_b + (long long)rows[s] * kD + p * 128 + hq * 32;
+#pragma unroll
+      for (int c = 0; c < 32; c += 4)
+        red_add_v4(dst + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                   __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    }
+  };
+  int def_it = -1, def_p = 0;                          // the chunk waiting to be drained
+
   float dpart[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c) dpart[c] = 0.f;
@@ -257,17 +277,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc512_kernel(
         for (int k = 0; k < kH / 16; ++k) {
           const uint64_t bg = sw128_desc_mn(ga + k * 2048, kHBlk);
           const uint64_t bq = sw128_desc_mn(qa + k * 2048, kHBlk);
-          mma_bf16_ss(tmem + kColDKV, sw128_desc(pha + k * 32), bg, idesc_kv, k > 0 ? 1u : 0u);
-          mma_bf16_ss(tmem + kColDKV, sw128_desc(pla + k * 32), bg, idesc_kv, 1u);
-          mma_bf16_ss(tmem + kColDKV, sw128_desc(dha + k * 32), bq, idesc_kv, 1u);
-          mma_bf16_ss(tmem + kColDKV, sw128_desc(dla + k * 32), bq, idesc_kv, 1u);
+          const uint32_t dc = tmem + dkv_col(p);
+          mma_bf16_ss(dc, sw128_desc(pha + k * 32), bg, idesc_kv, k > 0 ? 1u : 0u);
+          mma_bf16_ss(dc, sw128_desc(pla + k * 32), bg, idesc_kv, 1u);
+          mma_bf16_ss(dc, sw128_desc(dha + k * 32), bq, idesc_kv, 1u);
+          mma_bf16_ss(dc, sw128_desc(dla + k * 32), bq, idesc_kv, 1u);
         }
       }
       mma_commit(bar_mma);
     }
     // the next job's pair streams into the other stage (the MMAs that read it
-    // last, those of job j - 1, have completed)
+    // last, those of job j - 1, have completed), and the previous chunk is
+    // drained while these MMAs run
     if (j + 1 < J) stage_issue(j + 1);
+    if (def_it >= 0) {
+      drain(def_it, def_p);
+      def_it = -1;
+    }
     ok = __syncthreads_and(mbar_wait(bar_mma, n_mma & 1));
     ++n_mma;
     if (!ok) { site = sdp ? kSiteBwdS : kSiteBwdDS; break; }
@@ -315,22 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc512_kernel(
         for (int c = 0; c < 16; ++c) Dh[c] = D_s[hq * 16 + c];
       }
     } else if (!sdp) {
-      // add this slot's 128 d of the chunk into its compact dKV row (warp
-      // (qd, hq) takes 32 of the columns)
-      uint32_t v[32];
-      tmem_ld32_wait(tmem + lane_base + kColDKV + hq * 32, v);
-      const int s = it * kSlots + r;
-      if (s < S_total) {
-        float* dst = dkv_b + (long long)rows[s] * kD + p * 128 + hq * 32;
-#pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          red_add_v4(dst + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                     __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-      }
-      fence_before();
-      __syncthreads();                                 // chunk read before it is rewritten
+      // drained during the next job (the chunk's columns are next written
+      // two jobs later, after at least one more barrier)
+      def_it = it;
+      def_p = p;
     }
   }
+  if (ok && def_it >= 0) drain(def_it, def_p);
   cp_async_wait_all_();                                // no copy in flight past this point
   for (int j = n_waited; !ok && j < n_issued; ++j)     // nor a TMA load (bounded waits)
     mbar_wait(&bar_ld[j & 1], (j >> 1) & 1);
