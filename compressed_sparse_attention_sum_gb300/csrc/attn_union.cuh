@@ -23,47 +23,14 @@ __device__ __forceinline__ void heavy_first_block(int nblk, int* bi, int* xb) {
   *xb = nblk - 1 - id / b;
 }
 
-// Count multiplicities and build the ascending union list; returns its size.
-// cnt must be zeroed and visible to all threads (after a barrier) on entry.
-// idx == nullptr selects every visible block (dense mode).  The block's
-// queries are t0 .. t0+QB-1 below t_end (t_end <= sq; sq is the row stride of
-// idx).
+// Ascending compaction of the blocks below vmax with a non-zero count into
+// ulist; returns the union size.  cnt must be complete and visible to all
+// threads (after a barrier) on entry.
 template <int QB, int kThreads>
-__device__ __forceinline__ int build_union(const int32_t* __restrict__ idx, int bi, int sq, int K,
-                                           int t0, int t_end, int ratio, int n_c, uint64_t* cnt,
-                                           int* ulist, int* wsum, int* scal) {
+__device__ __forceinline__ int union_compact(int vmax, const uint64_t* cnt, int* ulist, int* wsum,
+                                             int* scal) {
   constexpr int NW = (QB + 3) / 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t_last = min(t0 + QB, t_end) - 1;
-  const int vmax = min((t_last + 1) / ratio, n_c);
-  if (idx != nullptr) {
-    for (int s0 = 0; s0 < K; s0 += kThreads) {
-      const int s = s0 + tid;
-      // all of this thread's loads are in flight before the first atomic
-      int jv[QB];
-#pragma unroll
-      for (int q = 0; q < QB; ++q)
-        jv[q] = (s < K && t0 + q < t_end) ? __ldg(idx + ((long long)bi * sq + t0 + q) * K + s)
-                                          : -1;
-#pragma unroll
-      for (int q = 0; q < QB; ++q) {
-        const int vis = min((t0 + q + 1) / ratio, n_c);
-        if (jv[q] >= 0 && jv[q] < vis)
-          atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[jv[q] * NW + (q >> 2)]),
-                    1ull << (16 * (q & 3)));
-      }
-    }
-  } else {
-    for (int q = 0; q < QB; ++q) {
-      const int t = t0 + q;
-      if (t >= t_end) break;
-      const int vis = min((t + 1) / ratio, n_c);
-      for (int j = tid; j < vis; j += kThreads)
-        atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[j * NW + (q >> 2)]),
-                  1ull << (16 * (q & 3)));
-    }
-  }
-  __syncthreads();
   // ascending compaction: each thread scans a contiguous range of blocks
   const int per = (vmax + kThreads - 1) / kThreads;
   const int j0 = tid * per, j1 = min(vmax, j0 + per);
@@ -94,6 +61,50 @@ __device__ __forceinline__ int build_union(const int32_t* __restrict__ idx, int 
   if (tid == kThreads - 1) scal[0] = base + incl;
   __syncthreads();
   return scal[0];
+}
+
+// Count multiplicities and build the ascending union list; returns its size.
+// cnt must be zeroed and visible to all threads (after a barrier) on entry.
+// idx == nullptr selects every visible block (dense mode).  The block's
+// queries are t0 .. t0+QB-1 below t_end (t_end <= sq; sq is the row stride of
+// idx).
+template <int QB, int kThreads>
+__device__ __forceinline__ int build_union(const int32_t* __restrict__ idx, int bi, int sq, int K,
+                                           int t0, int t_end, int ratio, int n_c, uint64_t* cnt,
+                                           int* ulist, int* wsum, int* scal) {
+  constexpr int NW = (QB + 3) / 4;
+  const int tid = threadIdx.x;
+  const int t_last = min(t0 + QB, t_end) - 1;
+  const int vmax = min((t_last + 1) / ratio, n_c);
+  if (idx != nullptr) {
+    for (int s0 = 0; s0 < K; s0 += kThreads) {
+      const int s = s0 + tid;
+      // all of this thread's loads are in flight before the first atomic
+      int jv[QB];
+#pragma unroll
+      for (int q = 0; q < QB; ++q)
+        jv[q] = (s < K && t0 + q < t_end) ? __ldg(idx + ((long long)bi * sq + t0 + q) * K + s)
+                                          : -1;
+#pragma unroll
+      for (int q = 0; q < QB; ++q) {
+        const int vis = min((t0 + q + 1) / ratio, n_c);
+        if (jv[q] >= 0 && jv[q] < vis)
+          atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[jv[q] * NW + (q >> 2)]),
+                    1ull << (16 * (q & 3)));
+      }
+    }
+  } else {
+    for (int q = 0; q < QB; ++q) {
+      const int t = t0 + q;
+      if (t >= t_end) break;
+      const int vis = min((t + 1) / ratio, n_c);
+      for (int j = tid; j < vis; j += kThreads)
+        atomicAdd(reinterpret_cast<unsigned long long*>(&cnt[j * NW + (q >> 2)]),
+                  1ull << (16 * (q & 3)));
+    }
+  }
+  __syncthreads();
+  return union_compact<QB, kThreads>(vmax, cnt, ulist, wsum, scal);
 }
 
 }  // namespace csa

@@ -86,6 +86,11 @@ cudaError_t launch_indexer_loss(const void* q_I, const void* k_I, const float* w
                                 const int32_t* idx, const float* target, float* loss, float* dq_I,
                                 float* dk_I, float* dw, int b, int sq, int H_I, int d_I, int n_c,
                                 int ratio, int K, bool bf16, cudaStream_t s);
+bool indexer_loss_tc_supported(int H_I, int d_I, int n_c);
+cudaError_t launch_indexer_loss_tc(const void* q_I, const void* k_I, const float* w,
+                                   const int32_t* idx, const float* target, float* loss,
+                                   float* dq_I, float* dk_I, float* dw, int b, int sq, int H_I,
+                                   int n_c, int ratio, int K, int* status, cudaStream_t s);
 }  // namespace csa
 
 #include <atomic>
@@ -471,7 +476,8 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
 namespace {
 
 // CSA_ATTN_WARP_MMA=1 selects the warp-level mma.sync kernels for bf16 even
-// where the tcgen05 kernels apply (same results up to rounding order).
+// where the tcgen05 kernels apply (the attention forward and backward and the
+// indexer loss; same results up to rounding order).
 bool warp_mma_forced() {
   const char* wm = getenv("CSA_ATTN_WARP_MMA");
   return wm != nullptr && wm[0] == '1';
@@ -624,6 +630,13 @@ csa_status_t csa_indexer_loss(const void* q_idx, const void* k_idx, const float*
     return CSA_ERR_INVALID_ARG;
   if (sq < ratio || n_c != sq / ratio) return CSA_ERR_INVALID_ARG;
   if (d_I > kMaxDI || H_I > kMaxH || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
+  if (dt == CSA_BF16 && !warp_mma_forced() && csa::indexer_loss_tc_supported(H_I, d_I, n_c)) {
+    int* status = device_status_ptr();
+    if (status == nullptr) return CSA_ERR_CUDA;
+    return from_cuda(csa::launch_indexer_loss_tc(q_idx, k_idx, w, idx, target, loss, dq_idx,
+                                                 dk_idx, dw, b, sq, H_I, n_c, ratio, K, status,
+                                                 (cudaStream_t)stream));
+  }
   const bool mma = dt == CSA_BF16 && csa::indexer_loss_mma_ok(H_I, d_I);
   if (csa::indexer_loss_smem(mma, H_I, d_I, K) > 227 * 1024) return CSA_ERR_UNSUPPORTED;
   return from_cuda(csa::launch_indexer_loss(q_idx, k_idx, w, idx, target, loss, dq_idx, dk_idx,

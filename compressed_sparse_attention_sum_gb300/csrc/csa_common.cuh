@@ -28,6 +28,7 @@ __device__ __forceinline__ void set_status(int* status, int code, int site = 0) 
 constexpr int kSiteIdxProducer = 0x11, kSiteIdxMma = 0x12, kSiteIdxEpilogue = 0x13;
 constexpr int kSiteFwdQ = 0x21, kSiteFwdS = 0x22, kSiteFwdO = 0x23, kSiteFwdLast = 0x24;
 constexpr int kSiteBwdQ = 0x31, kSiteBwdS = 0x32, kSiteBwdP = 0x33, kSiteBwdDS = 0x34;
+constexpr int kSiteLossQ = 0x51, kSiteLossX = 0x52, kSiteLossG = 0x53;
 // Sites recorded with CSA_ERR_DEVICE_CHECK: the tensor-core forward's union
 // of selected blocks larger than its n_c-entry list; a packed document that
 // starts inside a compressed block.
@@ -77,7 +78,10 @@ __device__ __forceinline__ void store8(float* p, const float* f) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
 }
 
-// fp32 vector atomic add into global memory (no return value).
+// fp32 atomic adds into global memory (no return value).
+__device__ __forceinline__ void red_add_f32(float* addr, float a) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
 __device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
   asm volatile("red.relaxed.gpu.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b)
                : "memory");

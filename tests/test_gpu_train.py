@@ -2,8 +2,9 @@
 the C ABI: the distillation teacher (csa_indexer_teacher) and the student's
 KL loss with its gradients (csa_indexer_loss).
 
-Both kernels families are covered: warp-level MMA for bf16 with d (d_I) in
-the supported set, the CUDA-core kernel for fp32 and other shapes; index
+Every kernel family is covered: the tcgen05 loss kernel for bf16 with
+d_I = 128 and H_I in {32, 64}, warp-level MMA for the other bf16 shapes with
+d (d_I) in the supported set, the CUDA-core kernel for fp32 and other shapes; index
 rows carry repeated, padded, out-of-range and not-yet-visible entries, and
 some rows have no valid entry at all or an all-zero target.
 """
@@ -160,6 +161,32 @@ def test_loss_random_rows(dtype, H_I, d_I):
     target = target / target.sum(-1, keepdim=True).clamp_min(1e-30)
     loss, dq, dk, dw = _check_loss(q_I, k_I, w, idx, target, ratio, dtype)
     assert torch.all(dq[:, 7] == 0) and torch.all(dw[:, 7] == 0) and torch.all(loss[:, 7] == 0)
+
+
+@pytest.mark.parametrize("H_I,sq,ratio,K", [
+    (64, 101, 2, 37),     # tensor-core kernel, 2 queries per CTA, a partial last block
+    (32, 102, 2, 37),     # 4 queries per CTA, a partial last block
+    (64, 600, 2, 200),    # unions of up to 300 blocks: three tiles of 128
+    (32, 520, 2, 160),    # 4 queries per CTA over three tiles
+])
+def test_loss_tensor_core_shapes(H_I, sq, ratio, K):
+    """bf16, d_I = 128 and H_I in {32, 64} take the tcgen05 kernel (queries
+    sharing the union of their selections): messy index rows (repeats,
+    padding, out-of-range and not-yet-visible entries), rows without valid
+    entries or without target mass, and unions spanning several tiles."""
+    b, d_I = 2, 128
+    g = torch.Generator().manual_seed(60 + H_I + sq)
+    n_c = sq // ratio
+    q_I = torch.randn(b, sq, H_I, d_I, generator=g).to(torch.bfloat16)
+    k_I = torch.randn(b, n_c, d_I, generator=g).to(torch.bfloat16)
+    w = torch.randn(b, sq, H_I, generator=g) * 0.5
+    idx = _messy_idx(g, b, sq, n_c, K)
+    target = torch.rand(b, sq, K, generator=g)
+    target[:, 7] = 0.0
+    target = target / target.sum(-1, keepdim=True).clamp_min(1e-30)
+    loss, dq, dk, dw = _check_loss(q_I, k_I, w, idx, target, ratio, "bf16")
+    assert torch.all(dq[:, 7] == 0) and torch.all(dw[:, 7] == 0) and torch.all(loss[:, 7] == 0)
+    assert torch.all(dq[:, 5] == 0) and torch.all(dw[:, 5] == 0) and torch.all(loss[:, 5] == 0)
 
 
 @pytest.mark.parametrize("name", ["debug_bf16", "csa4_bf16"])
