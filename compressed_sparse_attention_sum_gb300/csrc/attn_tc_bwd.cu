@@ -26,6 +26,9 @@
 // The hi/lo split carries ~16 significant bits of P and dS into the
 // products, so the fp32 sums over thousands of queries stay accurate.
 // KV tiles are double-buffered: the next tile's gather overlaps this tile.
+// The CTAs are persistent (one per SM) and walk the query blocks heaviest
+// first; the next block's Q and dO tiles are requested as soon as the last
+// products of the current block have read them.
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 #include "tcgen05.cuh"
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     const float* __restrict__ sink, float scale, const __nv_bfloat16* __restrict__ o,
     const float* __restrict__ lse, float* __restrict__ dq, float* __restrict__ dkv, float* __restrict__ dsink, int sq, int H,
     int n_c, int ratio, int window, int K, int* __restrict__ status,
-    const int32_t* __restrict__ doc, int tb, int te) {
+    const int32_t* __restrict__ doc, int tb, int te, int njobs) {
   constexpr int NW = (QB + 3) / 4;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -118,14 +121,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   unsigned char* Y = sm + Layout::Y;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int bi, xb;
-  heavy_first_block((te - tb + QB - 1) / QB, &bi, &xb);
-  const int t0 = tb + xb * QB;       // rows t0 .. t0+QB-1 below te are this block's queries
+  const int nblk = (te - tb + QB - 1) / QB;
+  const int nb = njobs / nblk;       // batch elements
   const int n_kv = sq + n_c;
-  const __nv_bfloat16* kv_b = kv + (long long)bi * n_kv * kD;
-  float* dkv_b = dkv + (long long)bi * n_kv * kD;
+  // Persistent CTAs: job j is query block nblk-1-j/nb of batch element j%nb
+  // (the work of a block grows with its position, so the jobs run heaviest
+  // first), dealt to the CTAs in rounds whose order alternates (CTA c takes
+  // job c of round 0, job 2G-1-c of round 1, ...), which evens out the
+  // CTAs' totals
+  const int G = (int)gridDim.x;
+  auto job_of = [&](int round) -> int {
+    const int c = (round & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const int j = round * G + c;
+    return j < njobs ? j : -1;
+  };
 
-  // ---- set-up: barriers, TMEM, Q and dO tiles --------------------------------
+  // ---- set-up (once per CTA): barriers, TMEM ------------------------------------
   if (tid == 0) {
     mbar_init(bar_q, 1);
     mbar_init(bar_sp, 1);
@@ -136,21 +147,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
-  for (int e = tid; e < n_c * NW; e += kThreads) cnt[e] = 0ull;
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (tid == 0) {
+  // Q and dO tiles of job j (issued by thread 0)
+  auto load_qdo = [&](int j) {
+    const int row0 = ((j % nb) * sq + tb + (nblk - 1 - j / nb) * QB) * H;
     mbar_expect_tx(bar_q, 4 * kBlk);
-    const int row0 = (bi * sq + t0) * H;
     tma_load_2d(sm + Layout::Q, &tmap_q, bar_q, 0, row0);
     tma_load_2d(sm + Layout::Q + kBlk, &tmap_q, bar_q, 64, row0);
     tma_load_2d(sm + Layout::DO, &tmap_do, bar_q, 0, row0);
     tma_load_2d(sm + Layout::DO + kBlk, &tmap_do, bar_q, 64, row0);
-  }
+  };
+
+  // ---- per-thread state -------------------------------------------------------
+  const int qd = warp & 3, hf = warp >> 2;         // hf: column group (32 columns)
+  const int r = qd * 32 + lane;                    // TMEM lane: row (S, dP, dQ) or slot (dKV)
+  const int q = r / H, h = r % H;
+  const float sc2 = scale * kLog2e;
+  const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+  const uint32_t tS = tmem + lane_base + kColS + hf * 32;
+  const uint32_t tDP = tmem + lane_base + kColDP + hf * 32;
+  const uint32_t tDKV = tmem + lane_base + kColDKV + hf * 32;
+  const uint32_t tDQ = tmem + lane_base + kColDQ + hf * 32;
+  // completed phases of the barriers, carried across this CTA's jobs
+  uint32_t n_q = 0, n_sp = 0, n_p = 0, n_ds = 0, n_d1a = 0, n_d1b = 0;
+  bool ok = true;
+  int site = 0;
+  int job = job_of(0);
+  if (tid == 0 && job >= 0) load_qdo(job);
+
+  for (int round = 0; job >= 0; ++round) {
+  const int bi = job % nb, xb = nblk - 1 - job / nb;
+  const int t0 = tb + xb * QB;       // rows t0 .. t0+QB-1 below te are this block's queries
+  const __nv_bfloat16* kv_b = kv + (long long)bi * n_kv * kD;
+  float* dkv_b = dkv + (long long)bi * n_kv * kD;
+  const int next = job_of(round + 1);
 
   // ---- union of the block's selected compressed blocks ----------------------
+  for (int e = tid; e < n_c * NW; e += kThreads) cnt[e] = 0ull;
+  __syncthreads();
   const int t_last = min(t0 + QB, te) - 1;
   const int nu = build_union<QB, kThreads>(idx, bi, sq, K, t0, te, ratio, n_c, cnt, ulist, wsum,
                                            scal);
@@ -197,22 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     }
   };
 
-  // ---- per-thread state -------------------------------------------------------
-  const int qd = warp & 3, hf = warp >> 2;         // hf: column group (32 columns)
-  const int r = qd * 32 + lane;                    // TMEM lane: row (S, dP, dQ) or slot (dKV)
-  const int q = r / H, h = r % H;
+  // ---- this block's rows ------------------------------------------------------
   const int t = t0 + q;
   const bool row_ok = t < te;
-  const float sc2 = scale * kLog2e;
   const float lse2 = row_ok ? lse[(long long)(bi * sq + t0) * H + r] * kLog2e : INFINITY;
-  const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-  const uint32_t tS = tmem + lane_base + kColS + hf * 32;
-  const uint32_t tDP = tmem + lane_base + kColDP + hf * 32;
-  const uint32_t tDKV = tmem + lane_base + kColDKV + hf * 32;
-  const uint32_t tDQ = tmem + lane_base + kColDQ + hf * 32;
-  uint32_t n_sp = 0;          // completed phases of bar_sp
-  bool ok = __syncthreads_and(mbar_wait(bar_q, 0));
-  int site = ok ? 0 : kSiteBwdQ;
+  ok = __syncthreads_and(mbar_wait(bar_q, n_q & 1));
+  ++n_q;
+  if (!ok) { site = kSiteBwdQ; break; }
 
   auto issue_s_dp = [&](int it) {
     constexpr uint32_t idesc = idesc_bf16_f32_major(kRows, kSlots, 0, 0);
@@ -273,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
           issue_pass1(it + 1, tid == 32);
         }
       }
-      ok = __syncthreads_and(mbar_wait(&bar_d1[it & 1], (it >> 1) & 1));
+      ok = __syncthreads_and(
+          mbar_wait(&bar_d1[it & 1], (((it & 1) ? n_d1b : n_d1a) + (it >> 1)) & 1));
       if (!ok) { site = kSiteBwdS; break; }
       fence_after();
       const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 32;
@@ -297,7 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       if (it + 2 < ntiles) stage_tile(it + 2);
     }
     red[hf * kRows + r] = dpart;
+    n_d1a += (ntiles + 1) / 2;
+    n_d1b += ntiles / 2;
   }
+  if (!ok) break;
   // the tile's dKV accumulator starts from zero: every MMA into it accumulates,
   // so that its hi and lo parts may be issued by two threads in any order
   {
@@ -312,7 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   const float Drow = (red[r] + red[kRows + r]) + (red[2 * kRows + r] + red[3 * kRows + r]);
 
   // ---- pass 2 ---------------------------------------------------------------------
-  uint32_t n_p = 0, n_ds = 0;
   if (ok && ntiles > 0) {
     stage_tile(0);
     cp_async_wait_group_<0>();
@@ -479,18 +510,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     }
     fence_before();
   }
+  if (!ok) break;
+  // the next job's Q and dO tiles (this block's last products, which read
+  // them, have completed) stream in under this block's last reductions and
+  // epilogue
+  if (tid == 0 && next >= 0) load_qdo(next);
   // ---- sink gradient: -exp(sink - lse) D, summed over the block's queries per head --
   if (hf == 0)
     contrib[r] = (row_ok && sink != nullptr) ? -exp2f(sink[h] * kLog2e - lse2) * Drow : 0.f;
   __syncthreads();
-  if (ok && sink != nullptr && tid < H) {
+  if (sink != nullptr && tid < H) {
     float sacc = 0.f;
     for (int qq = 0; qq < QB; ++qq) sacc += contrib[qq * H + tid];
     atomicAdd(&dsink[tid], sacc);
   }
-  if (!ok && tid == 0) set_status(status, kDevTimeout, site);
   // ---- dq rows -----------------------------------------------------------------
-  if (ok && ntiles > 0) {
+  if (ntiles > 0) {
     float* dqrow = dq + ((long long)(bi * sq + t0) * H + r) * kD + hf * 32;
     uint32_t v[32];
     tmem_ld32_wait(tDQ, v);
@@ -502,6 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
                         __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
     }
   }
+  // this block's TMEM and shared-memory reads are done before the next block
+  fence_before();
+  __syncthreads();
+  job = next;
+  }  // jobs
+
+  cp_async_wait_all_();                               // no copy in flight past this point
+  if (!ok && tid == 0) set_status(status, kDevTimeout, site);
   fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -563,7 +606,12 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
   if (!make_rows_map(&tq, q, rows) || !make_rows_map(&tg, dO, rows)) return cudaErrorInvalidValue;
   const int QB = 128 / H;
   const size_t smem = attn_tc_bwd_smem(QB, n_c);
-  dim3 grid((unsigned)(((te - tb + QB - 1) / QB) * b));   // heaviest blocks first
+  const int njobs = ((te - tb + QB - 1) / QB) * b;
+  int dev = 0, n_sm = 0;                                   // persistent CTAs: one per SM
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
+    return cudaErrorInvalidValue;
+  dim3 grid((unsigned)(njobs < n_sm ? njobs : n_sm));
 #define CSA_TC_BWD(QQ)                                                                        \
   {                                                                                           \
     auto k = atb::attn_bwd_tc_kernel<QQ>;                                                     \
@@ -571,7 +619,7 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
     k<<<grid, atb::kThreads, smem, s>>>(tq, tg, (const __nv_bfloat16*)kv,                   \
                                         (const __nv_bfloat16*)dO, idx, sink, scale,           \
                                         (const __nv_bfloat16*)o, lse, dq, dkv, dsink, sq, H,  \
-                                        n_c, ratio, window, K, status, doc, tb, te);          \
+                                        n_c, ratio, window, K, status, doc, tb, te, njobs);   \
     count_launches(1);                                                                        \
   }
   if (QB == 8) CSA_TC_BWD(8)
