@@ -126,13 +126,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   const int n_kv = sq + n_c;
   // Persistent CTAs: job j is query block nblk-1-j/nb of batch element j%nb
   // (the work of a block grows with its position, so the jobs run heaviest
-  // first), dealt to the CTAs in rounds whose order alternates (CTA c takes
-  // job c of round 0, job 2G-1-c of round 1, ...), which evens out the
-  // CTAs' totals
+  // first), dealt to the CTAs in sweeps of G jobs whose order alternates
+  // (CTA c takes job c of sweep 0, job 2G-1-c of sweep 1, ...), which evens
+  // out the CTAs' totals
   const int G = (int)gridDim.x;
-  auto job_of = [&](int round) -> int {
-    const int c = (round & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x;
-    const int j = round * G + c;
+  auto job_of = [&](int sweep) -> int {
+    const int c = (sweep & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    const int j = sweep * G + c;
     return j < njobs ? j : -1;
   };
 
@@ -178,12 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   int job = job_of(0);
   if (tid == 0 && job >= 0) load_qdo(job);
 
-  for (int round = 0; job >= 0; ++round) {
+  for (int sweep = 0; job >= 0; ++sweep) {
   const int bi = job % nb, xb = nblk - 1 - job / nb;
   const int t0 = tb + xb * QB;       // rows t0 .. t0+QB-1 below te are this block's queries
   const __nv_bfloat16* kv_b = kv + (long long)bi * n_kv * kD;
   float* dkv_b = dkv + (long long)bi * n_kv * kD;
-  const int next = job_of(round + 1);
+  const int next = job_of(sweep + 1);
 
   // ---- union of the block's selected compressed blocks ----------------------
   for (int e = tid; e < n_c * NW; e += kThreads) cnt[e] = 0ull;
