@@ -556,8 +556,11 @@ csa_status_t csa_indexer_loss(const void* q_idx, const void* k_idx, const float*
  *   CSA_ERR_TIMEOUT: 0x11-0x13 the indexer's TMA producer, MMA issuer or
  *   epilogue waits; 0x21-0x24 the tensor-core attention forward's waits for
  *   the Q tile, the score MMA, the PV MMA inside the loop and the last PV
- *   MMA; 0x31-0x34 the tensor-core backward's waits for the Q/dO tiles, the
- *   S/dP MMAs, the P^T dO MMAs and the dS MMAs.
+ *   MMA (the d = 512 forward records the same sites); 0x31-0x34 the
+ *   tensor-core backward's waits for the Q/dO tiles, the S/dP MMAs, the P^T dO
+ *   MMAs and the dS MMAs (the d = 512 backward: 0x31 its Q/dO/KV stages, 0x32
+ *   and 0x34 its products); 0x51-0x53 the tensor-core indexer loss's waits
+ *   for the q_idx tile, the dots X^T and the dq_idx / dk_idx products.
  *   CSA_ERR_DEVICE_CHECK: 0x25 the tensor-core forward found the union of a
  *   query block's selected blocks larger than its n_c-entry list; 0x41 a
  *   packed document (doc_ids of csa_indexer_topk / csa_indexer_topk_fp8)
