@@ -199,6 +199,38 @@ def test_indexer_shapes(dtype, case):
     _check_indexer(q_I, k_I, w, case["topk"], case["ratio"])
 
 
+@pytest.mark.parametrize("dtype,case", [
+    # n_c 4100: more than 2048 blocks per row, the shared-memory select kernel
+    ("bf16", dict(b=1, sq=8200, H_I=2, d_I=64, ratio=2, topk=300, ties=False)),
+    # n_c 16384, the largest supported (the default workspace takes 8 chunks
+    # of 2048 rows); duplicated key rows and ReLU zeros give exact ties
+    ("bf16", dict(b=1, sq=16384, H_I=1, d_I=64, ratio=1, topk=64, ties=True)),
+    # CUDA-core fp32 scores into the same select, b = 2, exact ties
+    ("fp32", dict(b=2, sq=5000, H_I=3, d_I=32, ratio=2, topk=128, ties=True)),
+])
+def test_indexer_wide_rows_sampled(dtype, case):
+    """Rows of more than 2048 visible blocks, up to the largest n_c: sampled
+    rows (spread over the sequence, and its last two) against the oracle's
+    score rows, bit-exact sets where the K-th gap exceeds 1e-3 or is a tie."""
+    b, sq, ratio = case["b"], case["sq"], case["ratio"]
+    q_I, k_I, w = _indexer_case(40, b, sq, case["H_I"], case["d_I"], ratio, dtype,
+                                ties=case["ties"])
+    n_c = sq // ratio
+    K = min(case["topk"], n_c)
+    idx = csa.csa_indexer_topk(q_I.cuda(), k_I.cuda(), w.cuda(), case["topk"],
+                               ratio).cpu().numpy()
+    qn, kn, wn = f64(q_I), f64(k_I), f64(w)
+    rows = list(range(0, sq, max(1, sq // 48))) + [sq - 2, sq - 1]
+    n_exact = 0
+    for bi in range(b):
+        for t in rows:
+            v = orc.indexer_scores_row(qn[bi, t], kn[bi], wn[bi, t], t, ratio)
+            ok, exact = compare_topk_row(idx[bi, t], v, K)
+            assert ok, (bi, t, idx[bi, t][:8])
+            n_exact += exact
+    assert n_exact >= len(rows) // 2       # most rows are held to the exact set
+
+
 def test_indexer_chunked_workspace_identical():
     q_I, k_I, w = _indexer_case(7, 2, 1000, 4, 128, 4, "bf16")
     full, sc_full = _check_indexer(q_I, k_I, w, 96, 4)

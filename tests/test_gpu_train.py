@@ -163,18 +163,19 @@ def test_loss_random_rows(dtype, H_I, d_I):
     assert torch.all(dq[:, 7] == 0) and torch.all(dw[:, 7] == 0) and torch.all(loss[:, 7] == 0)
 
 
-@pytest.mark.parametrize("H_I,sq,ratio,K", [
-    (64, 101, 2, 37),     # tensor-core kernel, 2 queries per CTA, a partial last block
-    (32, 102, 2, 37),     # 4 queries per CTA, a partial last block
-    (64, 600, 2, 200),    # unions of up to 300 blocks: three tiles of 128
-    (32, 520, 2, 160),    # 4 queries per CTA over three tiles
+@pytest.mark.parametrize("H_I,sq,ratio,K,b", [
+    (64, 101, 2, 37, 2),     # tensor-core kernel, 2 queries per CTA, a partial last block
+    (32, 102, 2, 37, 2),     # 4 queries per CTA, a partial last block
+    (64, 600, 2, 200, 2),    # unions of up to 300 blocks: three tiles of 128
+    (32, 520, 2, 160, 2),    # 4 queries per CTA over three tiles
+    (64, 2048, 1, 512, 1),   # n_c 2048, the largest its shared memory takes at H_I 64
 ])
-def test_loss_tensor_core_shapes(H_I, sq, ratio, K):
+def test_loss_tensor_core_shapes(H_I, sq, ratio, K, b):
     """bf16, d_I = 128 and H_I in {32, 64} take the tcgen05 kernel (queries
     sharing the union of their selections): messy index rows (repeats,
     padding, out-of-range and not-yet-visible entries), rows without valid
     entries or without target mass, and unions spanning several tiles."""
-    b, d_I = 2, 128
+    d_I = 128
     g = torch.Generator().manual_seed(60 + H_I + sq)
     n_c = sq // ratio
     q_I = torch.randn(b, sq, H_I, d_I, generator=g).to(torch.bfloat16)
