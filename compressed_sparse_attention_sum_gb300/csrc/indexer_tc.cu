@@ -80,6 +80,10 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
   const int tq_end = min(t0 + nt, tq0 + kTileM);
   const int vis_max = min(tq_end / ratio, n_c);
   const int j0 = kt * kTileN;
+  // The select kernel that follows may be scheduled now (it waits for this
+  // grid's completion before reading the scores): it then takes free SMs
+  // while the score tiles run instead of starting after a launch gap.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tq0 >= tq_end || j0 >= vis_max) return;   // tile above the causal boundary
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;

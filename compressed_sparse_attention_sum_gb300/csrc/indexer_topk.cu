@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
                                                           int ratio, int K,
                                                           const int32_t* __restrict__ doc) {
   extern __shared__ uint32_t smk[];
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the score grid has completed
   const int warps = blockDim.x / 32;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
@@ -277,6 +278,7 @@ __global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __res
                                                               int n_c, int ratio, int K,
                                                               const int32_t* __restrict__ doc) {
   __shared__ int hist_all[4][256];
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the score grid has completed
   const int warps = blockDim.x / 32;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
@@ -477,6 +479,25 @@ cudaError_t launch_doc_boundary_check(const int32_t* doc, int b, int sq, int rat
   return cudaGetLastError();
 }
 
+// Launch a kernel that may be scheduled before the preceding kernel on the
+// stream has completed (programmatic dependent launch): the kernel waits for
+// it with griddepcontrol.wait before reading its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem,
+                             cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_score, int t0,
                                int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s,
                                const int32_t* doc) {
@@ -484,13 +505,16 @@ cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_s
   if (n_c <= 2048) {
     const unsigned grid = (unsigned)((rows + 3) / 4);   // 4 rows (warps) per CTA
 #define CSA_SEL(P)                                                                            \
-  if (doc)                                                                                    \
-    topk_select_reg_kernel<P, true><<<grid, 128, 0, s>>>(ws, topk_idx, topk_score, t0, nt, b, \
-                                                         sq, n_c, ratio, K, doc);             \
-  else                                                                                        \
-    topk_select_reg_kernel<P, false><<<grid, 128, 0, s>>>(ws, topk_idx, topk_score, t0, nt,   \
-                                                          b, sq, n_c, ratio, K, nullptr);     \
-  count_launches(1);
+  {                                                                                           \
+    cudaError_t e_ = doc ? launch_dependent(topk_select_reg_kernel<P, true>, grid, 128, 0, s, \
+                                            ws, topk_idx, topk_score, t0, nt, b, sq, n_c,     \
+                                            ratio, K, doc)                                    \
+                         : launch_dependent(topk_select_reg_kernel<P, false>, grid, 128, 0, s,\
+                                            ws, topk_idx, topk_score, t0, nt, b, sq, n_c,     \
+                                            ratio, K, (const int32_t*)nullptr);               \
+    if (e_ != cudaSuccess) return e_;                                                         \
+    count_launches(1);                                                                        \
+  }
     if (n_c <= 256) { CSA_SEL(8) }
     else if (n_c <= 512) { CSA_SEL(16) }
     else if (n_c <= 1024) { CSA_SEL(32) }
@@ -504,8 +528,9 @@ cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_s
   const size_t smem = per_warp * warps;
   dim3 grid((unsigned)((rows + warps - 1) / warps));
   cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  topk_select_kernel<<<grid, warps * 32, smem, s>>>(ws, topk_idx, topk_score, t0, nt, b, sq, n_c,
-                                                    ratio, K, doc);
+  cudaError_t e = launch_dependent(topk_select_kernel, grid, warps * 32, smem, s, ws, topk_idx,
+                                   topk_score, t0, nt, b, sq, n_c, ratio, K, doc);
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }
