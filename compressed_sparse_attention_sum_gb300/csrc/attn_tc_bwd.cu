@@ -611,7 +611,11 @@ cudaError_t launch_attn_bwd_tc(const void* q, const void* kv, const int32_t* idx
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
     return cudaErrorInvalidValue;
-  dim3 grid((unsigned)(njobs < n_sm ? njobs : n_sm));
+  // With packed documents the work of a block restarts at every document,
+  // so the alternating deal of the heaviest-first order does not balance the
+  // CTAs: one CTA per job then (the hardware places them as SMs free up).
+  const int ncta = doc != nullptr ? njobs : (njobs < n_sm ? njobs : n_sm);
+  dim3 grid((unsigned)ncta);
 #define CSA_TC_BWD(QQ)                                                                        \
   {                                                                                           \
     auto k = atb::attn_bwd_tc_kernel<QQ>;                                                     \
