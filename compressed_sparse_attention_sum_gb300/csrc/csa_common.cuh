@@ -78,6 +78,21 @@ __device__ __forceinline__ void store8(float* p, const float* f) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
 }
 
+// Two independent fp32 fused multiply-adds in one instruction (fma.rn.f32x2,
+// sm_100 and later): a += w.x * y0, b += w.y * y1, each rounded once to
+// nearest exactly as fmaf rounds, so results are bit-identical to two fmaf.
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void fma_f32x2(float& a, float& b, unsigned long long w,
+                                          float y0, float y1) {
+  unsigned long long acc = pack_f32x2(a, b);
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w), "l"(pack_f32x2(y0, y1)));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(acc));
+}
+
 // fp32 atomic adds into global memory (no return value).
 __device__ __forceinline__ void red_add_f32(float* addr, float a) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");

@@ -201,10 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
       if (lane == 0) mbar_arrive(&acc_empty[a]);
       float wv = __ldg(wrow + h);
       if constexpr (F8) wv *= __ldg(q_scale + ((long long)bi * sq + tw) * H_I + h);
+      // the weighted ReLU sum as paired fma (one instruction per two columns;
+      // the ReLU stays a max)
+      const unsigned long long w2 = pack_f32x2(wv, wv);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        acc[c] = fmaf(wv, fmaxf(__uint_as_float(v0[c]), 0.f), acc[c]);
-        acc[32 + c] = fmaf(wv, fmaxf(__uint_as_float(v1[c]), 0.f), acc[32 + c]);
+      for (int c = 0; c < 32; c += 2) {
+        fma_f32x2(acc[c], acc[c + 1], w2, fmaxf(__uint_as_float(v0[c]), 0.f),
+                  fmaxf(__uint_as_float(v0[c + 1]), 0.f));
+        fma_f32x2(acc[32 + c], acc[33 + c], w2, fmaxf(__uint_as_float(v1[c]), 0.f),
+                  fmaxf(__uint_as_float(v1[c + 1]), 0.f));
       }
     }
     if (!ok) {

@@ -169,8 +169,12 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
   const unsigned lt_mask = (1u << lane) - 1u;
   uint32_t* keys = smk + (size_t)wid * (n_c + 256);
   int* hist = reinterpret_cast<int*>(keys + n_c);
-  const int r = blockIdx.x * warps + wid;
-  if (r >= b * nt) return;
+  // rows by descending query position (batch elements interleaved): the later
+  // queries see the most blocks, so the heavy rows are dealt first and the
+  // light ones fill in behind them
+  const int r0 = blockIdx.x * warps + wid;
+  if (r0 >= b * nt) return;
+  const int r = (r0 % b) * nt + (nt - 1 - r0 / b);
   const int bi = r / nt, t = t0 + r % nt;
   const int vis = min((t + 1) / ratio, n_c);
   const float* row = ws + (size_t)r * n_c;
@@ -284,8 +288,12 @@ __global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __res
   const unsigned FULL = 0xffffffffu;
   const unsigned lt_mask = (1u << lane) - 1u;
   int* hist = hist_all[wid];
-  const int r = blockIdx.x * warps + wid;
-  if (r >= b * nt) return;
+  // rows by descending query position (batch elements interleaved): the later
+  // queries see the most blocks, so the heavy rows are dealt first and the
+  // light ones fill in behind them
+  const int r0 = blockIdx.x * warps + wid;
+  if (r0 >= b * nt) return;
+  const int r = (r0 % b) * nt + (nt - 1 - r0 / b);
   const int bi = r / nt, t = t0 + r % nt;
   const int vis = min((t + 1) / ratio, n_c);
   const float* row = ws + (size_t)r * n_c;
