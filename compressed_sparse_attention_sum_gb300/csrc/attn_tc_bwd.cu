@@ -344,26 +344,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   const float Drow = (red[r] + red[kRows + r]) + (red[2 * kRows + r] + red[3 * kRows + r]);
 
   // ---- pass 2 ---------------------------------------------------------------------
-  if (ok && ntiles > 0) {
-    stage_tile(0);
-    cp_async_wait_group_<0>();
-    fence_proxy_async_smem();
-    fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      fence_after();
-      issue_s_dp(0);
-    }
+  // Tiles in descending order: pass 1 left its last two tiles (and their bias
+  // tables) in the two KV buffers, so the first two need no gather (the
+  // barrier above ordered every read of pass 1's TMEM before this issue).
+  if (ok && ntiles > 0 && tid == 0) {
+    fence_after();
+    issue_s_dp(ntiles - 1);
   }
   for (int it = 0; it < ntiles && ok; ++it) {
-    // the next tile's gather overlaps this tile (its buffers were released
-    // when the previous tile's MMAs completed)
-    if (it + 1 < ntiles) stage_tile(it + 1);
+    const int tt = ntiles - 1 - it;    // the tile of this iteration
+    // the gather of tile tt-1 overlaps this tile (the buffer of tile tt+1 was
+    // released when that tile's MMAs completed); tile ntiles-2 is resident
+    if (it > 0 && tt > 0) stage_tile(tt - 1);
     ok = __syncthreads_and(mbar_wait(bar_sp, n_sp & 1));
     ++n_sp;
     if (!ok) { site = kSiteBwdS; break; }
     fence_after();
-    const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 32;
+    const float* bq = bias + (tt & 1) * QB * kSlots + q * kSlots + hf * 32;
     // P (hi, lo) -> X, Y
     {
       uint32_t vs[32];
@@ -420,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     for (int c8 = 0; c8 < 4; ++c8)
       store_hi_lo8(X, Y, sw_off(r, hf * 4 + c8),
                    *reinterpret_cast<const float(*)[8]>(dsv + c8 * 8));
-    if (it + 1 < ntiles) cp_async_wait_group_<0>();
+    if (it > 0 && tt > 0) cp_async_wait_group_<0>();
     fence_proxy_async_smem();
     fence_before();
     __syncthreads();
@@ -428,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       fence_after();
       const uint32_t xa = smem_addr(X), ya = smem_addr(Y);
       const uint32_t qa = smem_addr(sm + Layout::Q);
-      const uint32_t ka = smem_addr(sm + Layout::KV + (it & 1) * 2 * kBlk);
+      const uint32_t ka = smem_addr(sm + Layout::KV + (tt & 1) * 2 * kBlk);
       // dKV += dS^T Q
       constexpr uint32_t idesc_kv = idesc_bf16_f32_major(kSlots, kD, 1, 1);
 #pragma unroll
@@ -493,18 +490,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       // its KV rows arrived before them): thread 0 issues them here, so that
       // the issue, which blocks while the MMA queue drains, overlaps the
       // reductions of the other warps instead of delaying everyone
-      if (tid == 0 && it + 1 < ntiles) {
+      if (tid == 0 && tt > 0) {
         fence_after();
-        issue_s_dp(it + 1);
+        issue_s_dp(tt - 1);
       }
       // warps 1..15, one staged row each at a time: its 32 lanes add the
       // row's 512 B with one coalesced vector reduction (X|Y is free again
       // once every thread has passed the next barrier)
-      const int nrow = min(kSlots, S_total - it * kSlots);
+      const int nrow = min(kSlots, S_total - tt * kSlots);
 #pragma unroll 4
       for (int rr = warp - 1; warp > 0 && rr < nrow; rr += kThreads / 32 - 1) {
         const float4 v4 = *reinterpret_cast<const float4*>(stg + rr * kD + lane * 4);
-        red_add_v4(dkv_b + (long long)slot_row(it * kSlots + rr) * kD + lane * 4, v4.x, v4.y,
+        red_add_v4(dkv_b + (long long)slot_row(tt * kSlots + rr) * kD + lane * 4, v4.x, v4.y,
                    v4.z, v4.w);
       }
     }
