@@ -155,6 +155,22 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Row (b-major index into the chunk) of warp slot r0.  A row whose visible
+// blocks number at most K selects all of them, so it needs no score: those
+// rows come first, in ascending position, and run while the score grid is
+// still busy (the select is its dependent launch); then the other rows, the
+// most visible blocks first (the heavy rows start as soon as the scores are
+// complete).  Batch elements are interleaved.  vis(t) <= K exactly for
+// t <= (K+1)*ratio - 2 when n_c > K.
+__device__ __forceinline__ int select_row(int r0, int b, int nt, int t0, int ratio, int n_c,
+                                          int K) {
+  const int ts = n_c <= K ? nt : min(max((K + 1) * ratio - 1 - t0, 0), nt);
+  const int n_triv = b * ts;
+  if (r0 < n_triv) return (r0 % b) * nt + r0 / b;
+  const int r1 = r0 - n_triv;
+  return (r1 % b) * nt + (nt - 1 - r1 / b);
+}
+
 __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restrict__ ws,
                                                           int32_t* __restrict__ out_idx,
                                                           float* __restrict__ out_score, int t0,
@@ -162,24 +178,24 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
                                                           int ratio, int K,
                                                           const int32_t* __restrict__ doc) {
   extern __shared__ uint32_t smk[];
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the score grid has completed
   const int warps = blockDim.x / 32;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
   const unsigned lt_mask = (1u << lane) - 1u;
   uint32_t* keys = smk + (size_t)wid * (n_c + 256);
   int* hist = reinterpret_cast<int*>(keys + n_c);
-  // rows by descending query position (batch elements interleaved): the later
-  // queries see the most blocks, so the heavy rows are dealt first and the
-  // light ones fill in behind them
   const int r0 = blockIdx.x * warps + wid;
   if (r0 >= b * nt) return;
-  const int r = (r0 % b) * nt + (nt - 1 - r0 / b);
+  const int r = select_row(r0, b, nt, t0, ratio, n_c, K);
   const int bi = r / nt, t = t0 + r % nt;
   const int vis = min((t + 1) / ratio, n_c);
   const float* row = ws + (size_t)r * n_c;
   int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
   float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
+  // the score grid's output is read only where the selection depends on it
+  // or the scores are returned (every thread of the warp decides alike)
+  const bool scored = vis > K || os != nullptr;
+  if (scored) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (doc == nullptr && vis <= K) {
     for (int s = lane; s < K; s += 32) {
       oi[s] = s < vis ? s : -1;
@@ -192,7 +208,7 @@ __global__ void __launch_bounds__(256) topk_select_kernel(const float* __restric
   int ncand = 0;
   for (int j = lane; j < vis; j += 32) {
     const bool ok = docb == nullptr || __ldg(docb + (size_t)j * ratio) == dt;
-    keys[j] = ok ? order_key(row[j]) : 0u;
+    keys[j] = ok ? (scored ? order_key(row[j]) : 1u) : 0u;   // unscored: ncand <= vis <= K
     ncand += ok;
   }
   __syncwarp();
@@ -282,23 +298,23 @@ __global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __res
                                                               int n_c, int ratio, int K,
                                                               const int32_t* __restrict__ doc) {
   __shared__ int hist_all[4][256];
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the score grid has completed
   const int warps = blockDim.x / 32;
   const int wid = threadIdx.x / 32, lane = threadIdx.x & 31;
   const unsigned FULL = 0xffffffffu;
   const unsigned lt_mask = (1u << lane) - 1u;
   int* hist = hist_all[wid];
-  // rows by descending query position (batch elements interleaved): the later
-  // queries see the most blocks, so the heavy rows are dealt first and the
-  // light ones fill in behind them
   const int r0 = blockIdx.x * warps + wid;
   if (r0 >= b * nt) return;
-  const int r = (r0 % b) * nt + (nt - 1 - r0 / b);
+  const int r = select_row(r0, b, nt, t0, ratio, n_c, K);
   const int bi = r / nt, t = t0 + r % nt;
   const int vis = min((t + 1) / ratio, n_c);
   const float* row = ws + (size_t)r * n_c;
   int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
   float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
+  // the score grid's output is read only where the selection depends on it
+  // or the scores are returned (every thread of the warp decides alike)
+  const bool scored = vis > K || os != nullptr;
+  if (scored) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!DOC && vis <= K) {
     for (int s = lane; s < K; s += 32) {
       oi[s] = s < vis ? s : -1;
@@ -314,7 +330,8 @@ __global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __res
   for (int i = 0; i < PER; ++i) {
     const int j = lane + 32 * i;
     const bool ok = j < vis && (!DOC || __ldg(docb + (size_t)j * ratio) == dt);
-    key[i] = ok ? order_key(row[j]) : 0u;           // 0: not a candidate
+    // 0: not a candidate; unscored rows (ncand <= vis <= K) only mark them
+    key[i] = ok ? (scored ? order_key(row[j]) : 1u) : 0u;
     ncand += ok;
   }
   if (DOC) ncand = __reduce_add_sync(FULL, ncand);
