@@ -443,8 +443,8 @@ def run_gpu(args, rank, world, local_rank, workload=None, variants_on=True, e2e_
             "teacher_tflops": round(2.0 * H * d * slots_sel / (t_teach / 1e3) / 1e12, 2),
             "loss_tflops": round(3 * 2.0 * cfg.H_I * cfg.d_I * slots_sel / (t_loss / 1e3) / 1e12,
                                  2),
-            "kernels": ("teacher: warp-level MMA (mma.sync), one CTA per query; loss: tcgen05, "
-                        "128 / H_I queries per CTA over the union of their selections"),
+            "kernels": ("teacher and loss: tcgen05, 128 / H (128 / H_I) queries per job over the "
+                        "union of their selections (teacher: persistent CTAs)"),
         }
         # the FP8 indexer: per-row e4m3 quantization of q_I and k_I, then the
         # indexer top-k on the codes (tcgen05 kind::f8f6f4); the overlap is the

@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   const bool row_ok = t < te;
   const float lse2 = row_ok ? lse[(long long)(bi * sq + t0) * H + r] * kLog2e : INFINITY;
   ok = __syncthreads_and(mbar_wait(bar_q, n_q & 1));
-  ++n_q;
   if (!ok) { site = kSiteBwdQ; break; }
+  ++n_q;
 
   auto issue_s_dp = [&](int it) {
     constexpr uint32_t idesc = idesc_bf16_f32_major(kRows, kSlots, 0, 0);
@@ -541,6 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   }  // jobs
 
   cp_async_wait_all_();                               // no copy in flight past this point
+  // a failed wait for the prefetched tiles may leave them in flight (every
+  // other wait precedes the next prefetch): wait for them once more (bounded)
+  if (site == kSiteBwdQ && tid == 0) mbar_wait(bar_q, n_q & 1);
   if (!ok && tid == 0) set_status(status, kDevTimeout, site);
   fence_before();
   __syncthreads();

@@ -34,6 +34,11 @@ cudaError_t launch_quantize_e4m3(const void* x, long long rows, int d, bool bf16
                                  float* scale, cudaStream_t s);
 bool attn_mma_supported(int H, int d, int window, int K);
 bool attn_tc512_supported(int H, int d, int window, int Kl);
+bool indexer_teacher_tc_supported(int H, int d, int n_c, int K);
+cudaError_t launch_indexer_teacher_tc(const void* q, const void* kv, const int32_t* idx,
+                                      const float* lse, float scale, float* target, int b, int sq,
+                                      int H, int n_c, int ratio, int K, int* status,
+                                      cudaStream_t s);
 bool attn_tc512_bwd_supported(int H, int d, int window, int Kl);
 cudaError_t launch_attn_bwd_tc512(const void* q, const void* kv, const int32_t* idx,
                                   const float* sink, float scale, const float* lse,
@@ -476,8 +481,8 @@ csa_status_t csa_indexer_topk_fp8(const uint8_t* q8, const float* q_scale, const
 namespace {
 
 // CSA_ATTN_WARP_MMA=1 selects the warp-level mma.sync kernels for bf16 even
-// where the tcgen05 kernels apply (the attention forward and backward and the
-// indexer loss; same results up to rounding order).
+// where the tcgen05 kernels apply (the attention forward and backward, the
+// indexer teacher and loss; same results up to rounding order).
 bool warp_mma_forced() {
   const char* wm = getenv("CSA_ATTN_WARP_MMA");
   return wm != nullptr && wm[0] == '1';
@@ -605,6 +610,10 @@ csa_status_t csa_indexer_teacher(const void* q, const void* kv_full, const int32
     return CSA_ERR_INVALID_ARG;
   if (sq < ratio || n_c != sq / ratio || !(scale == scale)) return CSA_ERR_INVALID_ARG;
   if (d > kMaxD || H > kMaxH || n_c > kMaxNc) return CSA_ERR_UNSUPPORTED;
+  if (dt == CSA_BF16 && !warp_mma_forced() && csa::indexer_teacher_tc_supported(H, d, n_c, K))
+    return from_cuda(csa::launch_indexer_teacher_tc(q, kv_full, idx, lse, scale, target, b, sq, H,
+                                                    n_c, ratio, K, device_status_ptr(),
+                                                    (cudaStream_t)stream));
   const bool mma = dt == CSA_BF16 && csa::indexer_teacher_mma_ok(H, d);
   if (csa::indexer_teacher_smem(mma, H, d, K) > 227 * 1024) return CSA_ERR_UNSUPPORTED;
   return from_cuda(csa::launch_indexer_teacher(q, kv_full, idx, lse, scale, target, b, sq, H, d,

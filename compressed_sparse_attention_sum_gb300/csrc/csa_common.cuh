@@ -29,6 +29,7 @@ constexpr int kSiteIdxProducer = 0x11, kSiteIdxMma = 0x12, kSiteIdxEpilogue = 0x
 constexpr int kSiteFwdQ = 0x21, kSiteFwdS = 0x22, kSiteFwdO = 0x23, kSiteFwdLast = 0x24;
 constexpr int kSiteBwdQ = 0x31, kSiteBwdS = 0x32, kSiteBwdP = 0x33, kSiteBwdDS = 0x34;
 constexpr int kSiteLossQ = 0x51, kSiteLossX = 0x52, kSiteLossG = 0x53;
+constexpr int kSiteTeacherQ = 0x61, kSiteTeacherS = 0x62;
 // Sites recorded with CSA_ERR_DEVICE_CHECK: the tensor-core forward's union
 // of selected blocks larger than its n_c-entry list; a packed document that
 // starts inside a compressed block.

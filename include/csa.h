@@ -560,7 +560,9 @@ csa_status_t csa_indexer_loss(const void* q_idx, const void* k_idx, const float*
  *   tensor-core backward's waits for the Q/dO tiles, the S/dP MMAs, the P^T dO
  *   MMAs and the dS MMAs (the d = 512 backward: 0x31 its Q/dO/KV stages, 0x32
  *   and 0x34 its products); 0x51-0x53 the tensor-core indexer loss's waits
- *   for the q_idx tile, the dots X^T and the dq_idx / dk_idx products.
+ *   for the q_idx tile, the dots X^T and the dq_idx / dk_idx products;
+ *   0x61-0x62 the tensor-core indexer teacher's waits for the Q tile and the
+ *   transposed scores S^T.
  *   CSA_ERR_DEVICE_CHECK: 0x25 the tensor-core forward found the union of a
  *   query block's selected blocks larger than its n_c-entry list; 0x41 a
  *   packed document (doc_ids of csa_indexer_topk / csa_indexer_topk_fp8)

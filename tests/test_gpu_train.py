@@ -55,7 +55,9 @@ def _messy_idx(g, b, sq, n_c, K):
     ("fp32", 4, 64),      # CUDA-core kernel
     ("bf16", 6, 64),      # warp MMA, heads padded to 16
     ("bf16", 20, 40),     # CUDA-core kernel for a head dim outside the MMA set
-    ("bf16", 32, 128),    # warp MMA
+    ("bf16", 16, 128),    # tcgen05 kernel, 8 queries per CTA
+    ("bf16", 32, 128),    # tcgen05 kernel, 4 queries per CTA
+    ("bf16", 64, 128),    # tcgen05 kernel, a query's heads over two column groups
     ("bf16", 64, 512),    # warp MMA, widest rows
 ])
 def test_teacher_random_rows(dtype, H, d):
