@@ -206,11 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1) teacher_tc_kernel(
         issue(it + 1);
       }
     }
-    ok = __syncthreads_and(
-        mbar_wait(&bar_s[it & 1], (((it & 1) ? n_s1 : n_s0) + (it >> 1)) & 1));
-    if (!ok) { site = kSiteTeacherS; break; }
-    fence_after();
-    {
+    // per-warp wait: a warp starts its sums as soon as the scores are there,
+    // not after the issuing thread has handed the next tile's product over
+    const bool got =
+        __all_sync(0xffffffffu, mbar_wait(&bar_s[it & 1], (((it & 1) ? n_s1 : n_s0) + (it >> 1)) & 1));
+    if (got) {
+      fence_after();
       uint32_t v[32];
       tmem_ld32_wait(tmem + ((uint32_t)(qd * 32) << 16) + (it & 1) * 128 + cg * 32, v);
       const int u = it * kSlots + r;
@@ -240,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) teacher_tc_kernel(
     fence_before();
     // every thread is done with this tile's TMEM buffer; its KV buffer was
     // released when the product completed: stage tile it+2 there
-    __syncthreads();
+    ok = !__syncthreads_or(!got);
+    if (!ok) { site = kSiteTeacherS; break; }
     if (it + 2 < ntiles) stage_tile(it + 2);
   }
   if (!ok) break;
