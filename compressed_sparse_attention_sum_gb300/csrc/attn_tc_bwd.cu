@@ -301,13 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
           issue_pass1(it + 1, tid == 32);
         }
       }
-      ok = __syncthreads_and(
-          mbar_wait(&bar_d1[it & 1], (((it & 1) ? n_d1b : n_d1a) + (it >> 1)) & 1));
-      if (!ok) { site = kSiteBwdS; break; }
-      fence_after();
-      const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 32;
-      const uint32_t cs = lane_base + (it & 1) * 256 + hf * 32;
-      {
+      // per-warp wait: a warp sums as soon as the products are there, not
+      // after the two issuing threads have handed the next tile's over (the
+      // barrier below carries a failed wait to every thread)
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&bar_d1[it & 1], (((it & 1) ? n_d1b : n_d1a) + (it >> 1)) & 1));
+      if (ok) {
+        fence_after();
+        const float* bq = bias + (it & 1) * QB * kSlots + q * kSlots + hf * 32;
+        const uint32_t cs = lane_base + (it & 1) * 256 + hf * 32;
         uint32_t vs[32], vp[32];
         CSA_TMEM_LD32(tmem + cs, vs);
         CSA_TMEM_LD32(tmem + cs + 128, vp);
@@ -322,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
       fence_before();
       // everyone is done with this tile's bias table and TMEM buffer; its KV
       // buffer was released when its MMAs completed: stage tile it+2 there
-      __syncthreads();
+      ok = __syncthreads_and(ok);
+      if (!ok) { site = kSiteBwdS; break; }
       if (it + 2 < ntiles) stage_tile(it + 2);
     }
     red[hf * kRows + r] = dpart;
