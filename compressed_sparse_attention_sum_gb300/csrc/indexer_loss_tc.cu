@@ -323,11 +323,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
         fence_after();
         issue_x((it + 1) & 3, ((it + 1) & 3) * 128, &bar_x[(it + 1) & 3]);
       }
+    } else {
+      __syncthreads();     // the previous tile's combine has read `red`
     }
-    ok = __syncthreads_and(mbar_wait(&bar_x[it & 3], (it >> 2) & 1));
-    if (!ok) { site = kSiteLossX; break; }
-    fence_after();
-    {
+    // per-warp wait: a warp scores its columns as soon as X^T is there, not
+    // after the issuing thread has handed the next tile's product over (the
+    // barrier below carries a failed wait to every thread)
+    ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[it & 3], (it >> 2) & 1));
+    if (ok) {
+      fence_after();
       uint32_t v[32];
       tmem_ld32_wait(tmem + lane_base + (it & 3) * 128 + cg * 32, v);
       const float4* w4 = reinterpret_cast<const float4*>(wr + cg * 32);
@@ -343,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
       red[cg * kRows + r] = part;
     }
     fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok);
+    if (!ok) { site = kSiteLossX; break; }
     if (tid < kSlots) {
       const int u = it * kSlots + tid;
       if (u < n_u) {
@@ -426,10 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
     }
   }
   for (int it = 0; it < ntiles && ok; ++it) {
-    ok = __syncthreads_and(mbar_wait(&bar_s[it & 1], (it >> 1) & 1) && !fail);
-    if (!ok) { site = kSiteLossX; break; }
-    fence_after();
-    {
+    // per-warp wait (the barrier below carries a failed wait, or one of the
+    // previous tile's product waits, to every thread)
+    ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[it & 1], (it >> 1) & 1) && !fail);
+    if (ok) {
+      fence_after();
       const int u = it * kSlots + r;
       const float dI = u < n_u ? Iu[myq * n_c + u] : 0.f;
       uint32_t v[32];
@@ -453,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
     if (it + 1 < ntiles) cp_wait<0>();              // tile it+1's rows
     fence_proxy_async_smem();
     fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok);
+    if (!ok) { site = kSiteLossX; break; }
     if (tid == 0) {
       fence_after();
       const uint32_t ga = smem_addr(GH), la = smem_addr(GL);
