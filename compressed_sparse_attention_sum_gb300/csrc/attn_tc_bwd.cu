@@ -352,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
   // barrier above ordered every read of pass 1's TMEM before this issue).
   if (ok && ntiles > 0 && tid == 0) {
     fence_after();
+    bulk_wait_read_all();      // the previous block's dq copy has read X|Y
     issue_s_dp(ntiles - 1);
   }
   for (int it = 0; it < ntiles && ok; ++it) {
@@ -524,26 +525,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_tc_kernel(
     for (int qq = 0; qq < QB; ++qq) sacc += contrib[qq * H + tid];
     atomicAdd(&dsink[tid], sacc);
   }
-  // ---- dq rows -----------------------------------------------------------------
+  // ---- dq rows: staged in X|Y (the last drain has read its rows), then one
+  // bulk copy of the block's contiguous rows, so that no warp waits for the
+  // stores behind the last reductions; X|Y is next written in the next
+  // block's pass 2, after the copy has read it -----------------------------------
   if (ntiles > 0) {
-    float* dqrow = dq + ((long long)(bi * sq + t0) * H + r) * kD + hf * 32;
     uint32_t v[32];
     tmem_ld32_wait(tDQ, v);
-    if (row_ok) {
+    float* srow = reinterpret_cast<float*>(X) + r * kD + hf * 32;
+    // chunk (c + lane) % 8 at step c: the 32 rows, 512 B apart, hit
+    // different banks (the drain's rotation)
+    float4 ch[8];
 #pragma unroll
-      for (int c = 0; c < 32; c += 4)
-        *reinterpret_cast<float4*>(dqrow + c) =
-            make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                        __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    for (int c = 0; c < 8; ++c)
+      ch[c] = make_float4(__uint_as_float(v[c * 4]), __uint_as_float(v[c * 4 + 1]),
+                          __uint_as_float(v[c * 4 + 2]), __uint_as_float(v[c * 4 + 3]));
+#pragma unroll
+    for (int k = 1; k < 8; k <<= 1) {
+      const bool rot = (lane & k) != 0;
+      float4 tmp[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) tmp[c] = rot ? ch[(c + k) & 7] : ch[c];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ch[c] = tmp[c];
     }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<float4*>(srow + ((c + lane) & 7) * 4) = ch[c];
+    fence_proxy_async_smem();
   }
   // this block's TMEM and shared-memory reads are done before the next block
   fence_before();
   __syncthreads();
+  if (tid == 0 && ntiles > 0) {
+    const int nrows = min(QB, te - t0) * H;
+    bulk_store(dq + (long long)(bi * sq + t0) * H * kD, X, (uint32_t)nrows * kD * 4u);
+    bulk_commit();
+  }
   job = next;
   }  // jobs
 
   cp_async_wait_all_();                               // no copy in flight past this point
+  if (tid == 0) bulk_wait_all();                       // nor a dq copy
   // a failed wait for the prefetched tiles may leave them in flight (every
   // other wait precedes the next prefetch): wait for them once more (bounded)
   if (site == kSiteBwdQ && tid == 0) mbar_wait(bar_q, n_q & 1);

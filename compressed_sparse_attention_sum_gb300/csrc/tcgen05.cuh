@@ -267,6 +267,13 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssr
       "r"(smem_addr(ssrc)), "r"(bytes)
       : "memory");
 }
+// Bulk (non-tensor) asynchronous copy of `bytes` contiguous bytes from shared
+// to global memory (both 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(ssrc)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
