@@ -546,6 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
       if (tid % H_I == 0) loss[(long long)bi * sq + t] = qst[q * 8 + kStLoss];
     }
   }
+  // dq_I rows: staged in G hi|lo (free: the last products have completed),
+  // then one bulk copy of the block's contiguous rows instead of plain
+  // stores queued behind the dk_I reductions
   if (ok) {
     fence_after();
     uint32_t v[32];
@@ -555,14 +558,19 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
 #pragma unroll
       for (int c = 0; c < 32; ++c) v[c] = 0u;
     }
+    float* stg = reinterpret_cast<float*>(GH);       // [128 rows][128 d] fp32 = 64 KB
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int row = cg * 32 + c, q = row / H_I, t = t0 + q;
-      if (t < sq) dq_I[(((long long)bi * sq + t) * H_I + row % H_I) * kDI + r] = __uint_as_float(v[c]);
-    }
+    for (int c = 0; c < 32; ++c) stg[(cg * 32 + c) * kDI + r] = __uint_as_float(v[c]);
+    fence_proxy_async_smem();
   }
   fence_before();
   __syncthreads();
+  if (ok && tid == 0) {
+    const int nrows = min(QB, sq - t0) * H_I;
+    bulk_store(dq_I + ((long long)bi * sq + t0) * H_I * kDI, GH, (uint32_t)nrows * kDI * 4u);
+    bulk_commit();
+    bulk_wait_read_all();      // the copy has read the staging before the CTA exits
+  }
   if (warp == 0) {
     fence_after();
     tmem_dealloc(tmem, kTmemCols);
