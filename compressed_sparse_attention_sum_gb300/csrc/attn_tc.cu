@@ -322,28 +322,51 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_tc_kernel(
     const float l_tot = lsum[r] + lsum[kRows + r];
     // every thread loads its TMEM half row (.sync.aligned); only valid rows store
     const float inv = row_ok ? 1.f / l_tot : 0.f;
-    __nv_bfloat16* orow = o + ((long long)(bi * sq + t0) * H + r) * kD + hf * 64;
+    // O rows staged in the P buffer (free: the last PV product has completed),
+    // [128 rows][256 B] with the 16-byte chunks of a row rotated by the lane
+    // so that the 32 rows of a warp hit different banks, then written by one
+    // bulk copy of the block's contiguous rows
+    unsigned char* orow_s = sm + Layout::P + r * (kD * 2) + hf * 128;
+    uint4 u[8];                                  // this thread's 8 chunks of 16 B
 #pragma unroll
     for (int c4 = 0; c4 < 2; ++c4) {
       uint32_t v[32];
       tmem_ld32_wait(tO + c4 * 32, v);
-      if (row_ok) {
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(v[c8 * 8 + 0]) * inv, __uint_as_float(v[c8 * 8 + 1]) * inv);
-          u.y = pack_bf16x2(__uint_as_float(v[c8 * 8 + 2]) * inv, __uint_as_float(v[c8 * 8 + 3]) * inv);
-          u.z = pack_bf16x2(__uint_as_float(v[c8 * 8 + 4]) * inv, __uint_as_float(v[c8 * 8 + 5]) * inv);
-          u.w = pack_bf16x2(__uint_as_float(v[c8 * 8 + 6]) * inv, __uint_as_float(v[c8 * 8 + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + c4 * 32 + c8 * 8) = u;
-        }
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint4& w = u[c4 * 4 + c8];
+        w.x = pack_bf16x2(__uint_as_float(v[c8 * 8 + 0]) * inv, __uint_as_float(v[c8 * 8 + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(v[c8 * 8 + 2]) * inv, __uint_as_float(v[c8 * 8 + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(v[c8 * 8 + 4]) * inv, __uint_as_float(v[c8 * 8 + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(v[c8 * 8 + 6]) * inv, __uint_as_float(v[c8 * 8 + 7]) * inv);
       }
     }
+    // store chunk (c + lane) % 8 at step c (a 3-stage barrel shift keeps the
+    // register indices static)
+#pragma unroll
+    for (int k = 1; k < 8; k <<= 1) {
+      const bool rot = (lane & k) != 0;
+      uint4 tmp[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) tmp[c] = rot ? u[(c + k) & 7] : u[c];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) u[c] = tmp[c];
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(orow_s + ((c + lane) & 7) * 16) = u[c];
     if (row_ok && hf == 0)
       lse[(long long)(bi * sq + t0) * H + r] = (m_run + log2f(l_tot)) * kLn2;
+    fence_proxy_async_smem();
   }
   fence_before();
   __syncthreads();
+  if (ok && tid == 0) {
+    const int nrows = min(QB, te - t0) * H;
+    bulk_store(o + (long long)(bi * sq + t0) * H * kD, sm + Layout::P, (uint32_t)nrows * kD * 2u);
+    bulk_commit();
+    bulk_wait_read_all();      // the copy has read the staging before the CTA exits
+  }
   if (warp == 0) {
     fence_after();
     tmem_dealloc(tmem, kTmemCols);
