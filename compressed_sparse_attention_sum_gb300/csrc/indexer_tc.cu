@@ -34,6 +34,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 #include "tcgen05.cuh"
@@ -55,6 +57,7 @@ constexpr uint32_t kTmemCols = kAcc * 128;
 template <int DI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+    const __grid_constant__ CUtensorMap tmap_ws, int ws_tma,
     const float* __restrict__ w, float* __restrict__ ws, int t0, int nt, int sq, int n_c,
     int H_I, int ratio, int* __restrict__ status, const float* __restrict__ q_scale,
     const float* __restrict__ k_scale) {
@@ -217,15 +220,44 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
       s_abort = 1;
     }
     const int t = tq0 + row;
-    if (ok && t < tq_end) {
-      const int vis = min((t + 1) / ratio, n_c);
-      const int jb = j0 + half * 64;
-      float* dst = ws + ((long long)bi * nt + (t - t0)) * n_c + jb;
-      if constexpr (F8) {
+    const int jb = j0 + half * 64;
+    if constexpr (F8) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          acc[c] *= jb + c < n_c ? __ldg(k_scale + (long long)bi * n_c + jb + c) : 0.f;
+      for (int c = 0; c < 64; ++c)
+        acc[c] *= jb + c < n_c ? __ldg(k_scale + (long long)bi * n_c + jb + c) : 0.f;
+    }
+    if (ok && ws_tma) {
+      // the tile goes through the q_I ring (every head's product has
+      // completed) to one TMA store, which clips the rows past the chunk and
+      // the blocks past n_c; entries past a row's visible blocks are written
+      // too (the select never reads them).  A row's 16-byte chunks are
+      // rotated by the lane so that the warp's 32 rows hit different banks.
+      float* srow = reinterpret_cast<float*>(sA) + row * kTileN + half * 64;
+#pragma unroll
+      for (int c8 = 0; c8 < 2; ++c8) {          // two groups of 8 chunks
+        float4 ch[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int e = c8 * 32 + c * 4;
+          ch[c] = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+        }
+#pragma unroll
+        for (int k = 1; k < 8; k <<= 1) {
+          const bool rot = (lane & k) != 0;
+          float4 tmp[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) tmp[c] = rot ? ch[(c + k) & 7] : ch[c];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) ch[c] = tmp[c];
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(srow + c8 * 32 + ((c + lane) & 7) * 4) = ch[c];
       }
+      fence_proxy_async_smem();
+    } else if (ok && t < tq_end) {
+      const int vis = min((t + 1) / ratio, n_c);
+      float* dst = ws + ((long long)bi * nt + (t - t0)) * n_c + jb;
       if (jb + 64 <= vis && (n_c & 3) == 0) {
 #pragma unroll
         for (int c = 0; c < 64; c += 4)
@@ -240,6 +272,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_scores_tc_kernel(
   }
   fence_before();
   __syncthreads();
+  if (ws_tma && threadIdx.x == 0 && !s_abort) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            &tmap_ws),
+        "r"(j0), "r"(tq0 - t0), "r"(bi), "r"(smem_addr(sA))
+        : "memory");
+    bulk_commit();
+    bulk_wait_read_all();      // the store has read the staging before the CTA exits
+  }
   if (warp == 1) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -309,6 +350,23 @@ cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const
         CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // the score tiles leave by TMA when the workspace rows suit a tensor map
+  // (16-byte row stride and base)
+  CUtensorMap tws;
+  int ws_tma = 0;
+  if ((n_c & 3) == 0 && (reinterpret_cast<uintptr_t>(ws) & 15) == 0) {
+    // [b][nt rows][n_c]: a partial query tile is clipped at its own batch
+    // element's rows
+    const cuuint64_t dims[3] = {(cuuint64_t)n_c, (cuuint64_t)nt, (cuuint64_t)b};
+    const cuuint64_t strides[2] = {(cuuint64_t)n_c * 4, (cuuint64_t)nt * n_c * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)tc::kTileN, (cuuint32_t)tc::kTileM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    ws_tma = encode(&tws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ws, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+             CUDA_SUCCESS;
+  }
+  if (!ws_tma) memset(&tws, 0, sizeof(tws));
   const size_t smem = indexer_tc_smem(d_I, f8);
   dim3 grid((unsigned)((n_c + tc::kTileN - 1) / tc::kTileN),
             (unsigned)((nt + tc::kTileM - 1) / tc::kTileM), (unsigned)b);
@@ -316,7 +374,8 @@ cudaError_t launch_indexer_scores_tc(const void* q_idx, const void* k_idx, const
   {                                                                                             \
     auto k = tc::indexer_scores_tc_kernel<DD, FF>;                                              \
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);           \
-    k<<<grid, tc::kThreads, smem, s>>>(tq, tk, w, ws, t0, nt, sq, n_c, H_I, ratio, status,    \
+    k<<<grid, tc::kThreads, smem, s>>>(tq, tk, tws, ws_tma, w, ws, t0, nt, sq, n_c, H_I,      \
+                                       ratio, status,                                          \
                                        q_scale, k_scale);                                       \
     count_launches(1);                                                                          \
   }
