@@ -14,8 +14,9 @@ region.  `roofline` describes the kernel with the largest share of the
 step.  `cpu_baseline` is the fp64 oracle on the host cores over a bounded
 sample of query rows of the same workload.
 
---impl reference times the oracle itself: the pages ship no code to run, so
-the reference arm is the fp64 oracle on the host cores.
+--impl reference times the oracle itself: the sources cited above ship no
+runnable implementation, so the reference arm is the fp64 oracle on the host
+cores.
 --workload picks one of the five workloads; --sweep times all of them.
 Multi-GPU: one process per GPU (torchrun); the ranks split the layer's query
 rows into contiguous ranges of equal estimated work (row-range calls of the
