@@ -14,9 +14,8 @@ region.  `roofline` describes the kernel with the largest share of the
 step.  `cpu_baseline` is the fp64 oracle on the host cores over a bounded
 sample of query rows of the same workload.
 
---impl reference times the oracle itself: the sources cited above ship no
-runnable implementation, so the reference arm is the fp64 oracle on the host
-cores.
+--impl reference times the fp64 oracle on the host cores (the method's
+published sources include no runnable implementation to time instead).
 --workload picks one of the five workloads; --sweep times all of them.
 Multi-GPU: one process per GPU (torchrun); the ranks split the layer's query
 rows into contiguous ranges of equal estimated work (row-range calls of the
