@@ -11,10 +11,11 @@
 // arithmetic, so one memory latency covers it; other small ratios walk the
 // tokens with an online (running max) softmax, reading the scores in one
 // pass; ratios of 16 and more (HCA: 128) split each block's tokens over the
-// threads of a CTA and merge the partial softmax statistics.
+// threads of a CTA and reduce the block's softmax statistics across them.
 #include "compress_pool.cuh"
 #include "csa_common.cuh"
 #include "csa_kernels.h"
+#include "tcgen05.cuh"
 
 namespace csa {
 
@@ -203,78 +204,132 @@ __global__ void __launch_bounds__(64) compress_overlap_bwd_kernel(
   }
 }
 
-// Large ratios (the HCA ratio 128): one CTA per block, whose threads split
-// the block's tokens into TS ranges as well as its channels (8 per thread).
-// Each thread forms the online softmax of its tokens; the partial (max, sum,
-// weighted sum) triples are merged in shared memory.  A thread per (block,
-// 8 channels) walking all `ratio` tokens, as above, would leave a few
-// thousand threads each waiting on `ratio` dependent loads in turn.
+// Large ratios (the HCA ratio 128): a CTA per (block, batch, channel slice).
+// A slice is G groups of 8 channels (G the largest power of two dividing d/8,
+// at most 8: C = 8G channels); the CTA's 256 threads form TS = 256/G token
+// lanes of G threads, token lane ts taking the block's tokens ts, ts + TS, ...
+// Every thread loads its first kSplitCache tokens before any arithmetic, so
+// one memory latency covers the block.  The softmax statistics then come from
+// two reductions, each over a warp's lanes by shuffles and over the CTA's
+// warps in shared memory: the block maximum M per channel, then the sums of
+// e_t = 2^(s_t log2(e) - M log2(e)) and of e_t kv_t under that common maximum
+// (one exponential per element, no rescaling of partial sums).
 constexpr int kSplitThreads = 256;
+constexpr int kSplitWarps = kSplitThreads / 32;
+constexpr int kSplitCache = 4;
 constexpr int kSplitMinRatio = 16;
 
+int split_slice_groups(int groups) {
+  int g = 1;
+  while (g < 8 && groups % (2 * g) == 0) g *= 2;
+  return g;
+}
+
+struct SplitShared {
+  float red[kSplitWarps][2][64];   // per-warp partial maxima / sums of the C channels
+  float M2[64], L[64], P[64];      // M log2(e), sum of e_t, pooled value
+};
+
 template <typename T>
-__device__ __forceinline__ void split_partial(const T* kvp, const T* scp, int d, int score_width,
-                                              int c0, int t_lo, int t_hi, float* m, float* l,
-                                              float* acc) {
+__device__ __forceinline__ void load_score8(const T* scp, int t, int score_width, int c0, float* s) {
+  if (score_width == 1) {
+    const float s1 = to_f(scp[t]);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) { m[i] = -INFINITY; l[i] = 0.f; acc[i] = 0.f; }
-  for (int t = t_lo; t < t_hi; ++t) {
-    float vt[8], st[8];
-    load_token(kvp, scp, t, d, score_width, c0, vt, st);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float mn = fmaxf(m[i], st[i]);
-      const float alpha = expf(m[i] - mn);    // 0 on the first token (m = -inf)
-      const float e = expf(st[i] - mn);
-      l[i] = l[i] * alpha + e;
-      acc[i] = acc[i] * alpha + e * vt[i];
-      m[i] = mn;
-    }
+    for (int i = 0; i < 8; ++i) s[i] = s1;
+  } else {
+    load8(scp + (long long)t * score_width + c0, s);
   }
 }
 
-// The block's statistics per channel: the TS partials of this CTA merged by
-// the threads of token range 0 into (M, L, pooled), left in shared memory
-// (sm[0..3*groups*8)) for every thread.  kvp points at channel 0 of the
-// block's first token.
+// The block's statistics for the thread's 8 channels (c0..c0+7) and, in S, for
+// the CTA's C channels.  kvp points at channel c0 of the block's first token,
+// scp at the block's first score.  On return vc/sc hold the kv and score values
+// of the thread's first min(n_my, kSplitCache) tokens.
 template <typename T>
-__device__ __forceinline__ void split_stats(const T* kvp, const T* scp, int d, int score_width,
-                                            int ratio, float* sm, int groups, int TS, int cg,
-                                            int ts) {
-  const int per = (ratio + TS - 1) / TS;
-  float m[8], l[8], acc[8];
-  const int t_lo = min(ratio, ts * per), t_hi = min(ratio, t_lo + per);
-  if (ts < TS) {
-    split_partial(kvp + cg * 8, scp, d, score_width, cg * 8, t_lo, t_hi, m, l, acc);
-    float* pm = sm + ((size_t)ts * groups + cg) * 24;
+__device__ __forceinline__ void split_block_stats(const T* kvp, const T* scp, int d,
+                                                  int score_width, int TS, int G, int ts,
+                                                  int cgl, int c0, int n_my,
+                                                  float (&vc)[kSplitCache][8],
+                                                  float (&sc)[kSplitCache][8], SplitShared& S) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, C = 8 * G;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { pm[i] = m[i]; pm[8 + i] = l[i]; pm[16 + i] = acc[i]; }
+  for (int k = 0; k < kSplitCache; ++k)
+    if (k < n_my) load_token(kvp, scp, ts + k * TS, d, score_width, c0, vc[k], sc[k]);
+  float r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kSplitCache; ++k)
+    if (k < n_my) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) r[i] = fmaxf(r[i], sc[k][i]);
+    }
+  for (int k = kSplitCache; k < n_my; ++k) {
+    float st[8];
+    load_score8(scp, ts + k * TS, score_width, c0, st);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = fmaxf(r[i], st[i]);
+  }
+  for (int o = G; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = fmaxf(r[i], __shfl_xor_sync(0xffffffffu, r[i], o));
+  }
+  if (lane < G) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S.red[warp][0][cgl * 8 + i] = r[i];
   }
   __syncthreads();
-  float M[8], L[8], A[8];
-  if (ts == 0) {
+  if (tid < C) {
+    float m = S.red[0][0][tid];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { M[i] = -INFINITY; L[i] = 0.f; A[i] = 0.f; }
-    for (int k = 0; k < TS; ++k) {
-      const float* pm = sm + ((size_t)k * groups + cg) * 24;
+    for (int w = 1; w < kSplitWarps; ++w) m = fmaxf(m, S.red[w][0][tid]);
+    S.M2[tid] = m * kLog2e;
+  }
+  __syncthreads();
+  float m2[8], l[8], a[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) M[i] = fmaxf(M[i], pm[i]);
-    }
-    for (int k = 0; k < TS; ++k) {
-      const float* pm = sm + ((size_t)k * groups + cg) * 24;
+  for (int i = 0; i < 8; ++i) { m2[i] = S.M2[cgl * 8 + i]; l[i] = 0.f; a[i] = 0.f; }
+#pragma unroll
+  for (int k = 0; k < kSplitCache; ++k)
+    if (k < n_my) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float f = expf(pm[i] - M[i]);   // 0 for an empty range (m = -inf)
-        L[i] = fmaf(pm[8 + i], f, L[i]);
-        A[i] = fmaf(pm[16 + i], f, A[i]);
+        const float e = umma::ex2(fmaf(sc[k][i], kLog2e, -m2[i]));
+        l[i] += e;
+        a[i] = fmaf(e, vc[k][i], a[i]);
       }
     }
-  }
-  __syncthreads();              // every partial has been read
-  if (ts == 0) {
-    float* st = sm + (size_t)cg * 24;
+  for (int k = kSplitCache; k < n_my; ++k) {
+    float vt[8], st[8];
+    load_token(kvp, scp, ts + k * TS, d, score_width, c0, vt, st);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { st[i] = M[i]; st[8 + i] = L[i]; st[16 + i] = A[i] / L[i]; }
+    for (int i = 0; i < 8; ++i) {
+      const float e = umma::ex2(fmaf(st[i], kLog2e, -m2[i]));
+      l[i] += e;
+      a[i] = fmaf(e, vt[i], a[i]);
+    }
+  }
+  for (int o = G; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      l[i] += __shfl_xor_sync(0xffffffffu, l[i], o);
+      a[i] += __shfl_xor_sync(0xffffffffu, a[i], o);
+    }
+  }
+  if (lane < G) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      S.red[warp][0][cgl * 8 + i] = l[i];
+      S.red[warp][1][cgl * 8 + i] = a[i];
+    }
+  }
+  __syncthreads();
+  if (tid < C) {
+    float L = 0.f, A = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSplitWarps; ++w) { L += S.red[w][0][tid]; A += S.red[w][1][tid]; }
+    S.L[tid] = L;
+    S.P[tid] = A / L;
   }
   __syncthreads();
 }
@@ -282,85 +337,113 @@ __device__ __forceinline__ void split_stats(const T* kvp, const T* scp, int d, i
 template <typename T>
 __global__ void __launch_bounds__(kSplitThreads) compress_split_kernel(
     const T* __restrict__ kv, long long kv_bs, const T* __restrict__ score, int score_width,
-    T* __restrict__ out, long long out_bs, int sq, int d, int ratio) {
-  extern __shared__ float sm_split[];
-  const int groups = d / 8, TS = kSplitThreads / groups;
-  const int j = blockIdx.x, bi = blockIdx.y;
-  const int cg = threadIdx.x % groups, ts = threadIdx.x / groups;
-  const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d;
+    T* __restrict__ out, long long out_bs, int sq, int d, int ratio, int G) {
+  __shared__ SplitShared S;
+  const int TS = kSplitThreads / G, cgl = threadIdx.x % G, ts = threadIdx.x / G;
+  const int j = blockIdx.x, bi = blockIdx.y, cb = blockIdx.z * G * 8, c0 = cb + cgl * 8;
+  const int n_my = ts < ratio ? (ratio - 1 - ts) / TS + 1 : 0;
+  const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d + c0;
   const T* scp = score + ((long long)bi * sq + (long long)j * ratio) * score_width;
-  split_stats(kvp, scp, d, score_width, ratio, sm_split, groups, TS, cg, ts);
-  if (ts == 0) store8(out + bi * out_bs + (long long)j * d + cg * 8, sm_split + cg * 24 + 16);
+  float vc[kSplitCache][8], sc[kSplitCache][8];
+  split_block_stats(kvp, scp, d, score_width, TS, G, ts, cgl, c0, n_my, vc, sc, S);
+  if (threadIdx.x < 8 * G)
+    out[bi * out_bs + (long long)j * d + cb + threadIdx.x] = from_f<T>(S.P[threadIdx.x]);
 }
 
 // Its backward: the block's statistics as above, then every thread adds
-// w_t g to its tokens' dkv rows and writes their score gradients (the CTA
-// past the last block writes the zero score gradient of the tail tokens).
+// w_t g to its tokens' dkv rows (fetched into shared memory at the start, so
+// their latency overlaps the statistics) and writes their score gradients;
+// with one score per token the G lanes of a token sum theirs before one atomic
+// add.  The CTAs past the last block write the zero score gradient of the tail
+// tokens (per-channel scores).
 template <typename T>
-__global__ void __launch_bounds__(kSplitThreads) compress_bwd_split_kernel(
+__global__ void __launch_bounds__(kSplitThreads, 2) compress_bwd_split_kernel(
     const T* __restrict__ kv, long long kv_bs, const T* __restrict__ score, int score_width,
     const float* __restrict__ g, long long g_bs, float* __restrict__ dkv, long long dkv_bs,
-    float* __restrict__ dscore, int sq, int d, int ratio, int n_c) {
-  extern __shared__ float sm_split[];
-  const int groups = d / 8, TS = kSplitThreads / groups;
-  const int j = blockIdx.x, bi = blockIdx.y;
-  const int cg = threadIdx.x % groups, ts = threadIdx.x / groups;
-  if (j >= n_c) {             // tail tokens: zero score gradient (per-channel scores)
+    float* __restrict__ dscore, int sq, int d, int ratio, int n_c, int G) {
+  __shared__ SplitShared S;
+  __shared__ __align__(16) float dk_s[kSplitCache][2][kSplitThreads][4];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int TS = kSplitThreads / G, cgl = tid % G, ts = tid / G;
+  const int j = blockIdx.x, bi = blockIdx.y, cb = blockIdx.z * G * 8, c0 = cb + cgl * 8;
+  if (j >= n_c) {
     const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int t = n_c * ratio + ts; ts < TS && t < sq; t += TS)
-      store8(dscore + ((long long)bi * sq + t) * score_width + cg * 8, z);
+    for (int t = n_c * ratio + ts; t < sq; t += TS)
+      store8(dscore + ((long long)bi * sq + t) * score_width + c0, z);
     return;
   }
-  const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d;
-  const T* scp = score + ((long long)bi * sq + (long long)j * ratio) * score_width;
-  split_stats(kvp, scp, d, score_width, ratio, sm_split, groups, TS, cg, ts);
-  if (ts >= TS) return;
-  const int c0 = cg * 8;
-  float M[8], L[8], P[8], gv[8];
-  const float* st = sm_split + cg * 24;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) { M[i] = st[i]; L[i] = st[8 + i]; P[i] = st[16 + i]; }
-  load8(g + bi * g_bs + (long long)j * d + c0, gv);
-  const int per = (ratio + TS - 1) / TS;
-  const int t_lo = min(ratio, ts * per), t_hi = min(ratio, t_lo + per);
+  const int n_my = ts < ratio ? (ratio - 1 - ts) / TS + 1 : 0;
   float* dkp = dkv + bi * dkv_bs + (long long)j * ratio * d + c0;
-  for (int t = t_lo; t < t_hi; ++t) {
-    float vt[8], sv[8], dt[8];
-    load_token(kvp + c0, scp, t, d, score_width, c0, vt, sv);
-    load8(dkp + (long long)t * d, dt);
+#pragma unroll
+  for (int k = 0; k < kSplitCache; ++k)
+    if (k < n_my) {
+      const float* src = dkp + (long long)(ts + k * TS) * d;
+      umma::cp_async_16(&dk_s[k][0][tid][0], src);
+      umma::cp_async_16(&dk_s[k][1][tid][0], src + 4);
+    }
+  float gv[8];
+  load8(g + bi * g_bs + (long long)j * d + c0, gv);
+  const T* kvp = kv + bi * kv_bs + (long long)j * ratio * d + c0;
+  const T* scp = score + ((long long)bi * sq + (long long)j * ratio) * score_width;
+  float vc[kSplitCache][8], sc[kSplitCache][8];
+  split_block_stats(kvp, scp, d, score_width, TS, G, ts, cgl, c0, n_my, vc, sc, S);
+  // w_t = 2^(s_t log2(e) - b2) with b2 = M log2(e) + log2(L)
+  float b2[8], P[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    b2[i] = S.M2[cgl * 8 + i] + log2f(S.L[cgl * 8 + i]);
+    P[i] = S.P[cgl * 8 + i];
+  }
+  umma::cp_async_wait_all_();
+  const unsigned gmask = ((1u << G) - 1u) << (lane & ~(G - 1));
+  float* dsp = dscore + ((long long)bi * sq + (long long)j * ratio) * score_width;
+  auto grad = [&](int t, const float* vt, const float* st, float* dt) {
     float ds[8], dsum = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float w = expf(sv[i] - M[i]) / L[i];
+      const float w = umma::ex2(fmaf(st[i], kLog2e, -b2[i]));
       dt[i] = fmaf(w, gv[i], dt[i]);
       ds[i] = w * gv[i] * (vt[i] - P[i]);
       dsum += ds[i];
     }
     store8(dkp + (long long)t * d, dt);
-    const long long tok = (long long)j * ratio + t;
-    if (score_width == 1)
-      atomicAdd(dscore + (long long)bi * sq + tok, dsum);
-    else
-      store8(dscore + ((long long)bi * sq + tok) * score_width + c0, ds);
+    if (score_width == 1) {
+      for (int o = 1; o < G; o <<= 1) dsum += __shfl_xor_sync(gmask, dsum, o);
+      if (cgl == 0) atomicAdd(dsp + t, dsum);
+    } else {
+      store8(dsp + (long long)t * score_width + c0, ds);
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < kSplitCache; ++k)
+    if (k < n_my) {
+      const float4 lo = *reinterpret_cast<const float4*>(&dk_s[k][0][tid][0]);
+      const float4 hi = *reinterpret_cast<const float4*>(&dk_s[k][1][tid][0]);
+      float dt[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      grad(ts + k * TS, vc[k], sc[k], dt);
+    }
+  for (int k = kSplitCache; k < n_my; ++k) {
+    const int t = ts + k * TS;
+    float vt[8], st[8], dt[8];
+    load_token(kvp, scp, t, d, score_width, c0, vt, st);
+    load8(dkp + (long long)t * d, dt);
+    grad(t, vt, st, dt);
   }
 }
 
 namespace {
 constexpr int kCompressThreads = 64;
 
-size_t split_smem(int d) {
-  const int groups = d / 8;
-  return (size_t)(kSplitThreads / groups) * groups * 24 * sizeof(float);
-}
-
 template <typename T, int R>
 void compress_fwd_t(const void* kv, long long kv_bs, const void* score, int score_width,
                     void* out, long long out_bs, int b, int sq, int d, int ratio, cudaStream_t s) {
   const int n_c = sq / ratio;
   if (R == 0 && ratio >= kSplitMinRatio) {
-    compress_split_kernel<T><<<dim3((unsigned)n_c, (unsigned)b), kSplitThreads, split_smem(d),
-                               s>>>((const T*)kv, kv_bs, (const T*)score, score_width, (T*)out,
-                                    out_bs, sq, d, ratio);
+    const int G = split_slice_groups(d / 8);
+    compress_split_kernel<T><<<dim3((unsigned)n_c, (unsigned)b, (unsigned)(d / 8 / G)),
+                               kSplitThreads, 0, s>>>((const T*)kv, kv_bs, (const T*)score,
+                                                      score_width, (T*)out, out_bs, sq, d,
+                                                      ratio, G);
     count_launches(1);
     return;
   }
@@ -380,9 +463,10 @@ void compress_bwd_t(const void* kv, long long kv_bs, const void* score, int scor
   const int tail = score_width == 1 ? 0 : sq - n_c * ratio;
   if (R == 0 && ratio >= kSplitMinRatio) {
     const unsigned nx = (unsigned)(n_c + (tail > 0 ? 1 : 0));
-    compress_bwd_split_kernel<T><<<dim3(nx, (unsigned)b), kSplitThreads, split_smem(d), s>>>(
-        (const T*)kv, kv_bs, (const T*)score, score_width, g, g_bs, dkv, dkv_bs, dscore, sq, d,
-        ratio, n_c);
+    const int G = split_slice_groups(d / 8);
+    compress_bwd_split_kernel<T><<<dim3(nx, (unsigned)b, (unsigned)(d / 8 / G)), kSplitThreads, 0,
+                                   s>>>((const T*)kv, kv_bs, (const T*)score, score_width, g, g_bs,
+                                        dkv, dkv_bs, dscore, sq, d, ratio, n_c, G);
     count_launches(1);
     return;
   }

@@ -278,6 +278,8 @@ def test_tc_forward_dense_mode_and_large_logits(H):
     (2, 200, 24, 37),      # token-split kernel: odd ratio, 3 channel groups, 15-token tail
     (1, 300, 512, 128),    # token-split kernel at the HCA ratio, d = 512, 44-token tail
     (1, 1091, 64, 17),     # token-split kernel, ratio just above its threshold
+    (1, 70, 8, 16),        # token-split kernel, one channel group: most token lanes idle
+    (1, 600, 64, 272),     # token-split kernel, 9 tokens a lane: past the register-held ones
 ])
 def test_compress_fwd_bwd_ragged_and_scalar_score(dtype, score_width, b, sq, d, ratio):
     g = torch.Generator().manual_seed(11)
