@@ -136,6 +136,26 @@ __device__ __forceinline__ float lane_transpose_sum16(float (&v)[16]) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
+// 4x4 transposes within each quad of lanes: on entry lane 4a+b holds in x[j]
+// the element (row b, column j) of its quad's block, on return in x[i] the
+// element (row i, column b).  Two exchange steps (partner lane ^ 2, then
+// ^ 1), each moving the elements whose row and column differ in that bit.
+__device__ __forceinline__ void quad_transpose4(float (&x)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 2; s >= 1; s >>= 1) {
+    const bool hi = (lane & s) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j & s) continue;
+      const float send = hi ? x[j] : x[j ^ s];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+      if (hi) x[j] = recv;
+      else x[j ^ s] = recv;
+    }
+  }
+}
+
 template <int QB>
 __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __nv_bfloat16* __restrict__ k_I,
@@ -502,9 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
     const bool dq_ok = mbar_wait(bar_dq, it & 1);
     fail |= !dq_ok;
     if (dq_ok && it + 2 < ntiles) stage(it + 2, it & 1);
-    // dK done: thread (d = its TMEM lane) adds its 32 slot columns straight
-    // from TMEM into dk_I (a warp covers 128 contiguous bytes of one block
-    // row per instruction) while the tensor core forms X^T
+    // dK done: thread (d = its TMEM lane) reads its 32 slot columns from
+    // TMEM; quad transposes give lane 4a+b four consecutive d of slot 4k+b,
+    // so each vector reduction of a warp covers 128 contiguous bytes of four
+    // block rows (a quarter of the reduction instructions of one scalar per
+    // column), while the tensor core forms X^T
     const bool dk_ok = __all_sync(0xffffffffu, mbar_wait(bar_dk, it & 1));
     fail |= !dk_ok;
     if (dk_ok) {
@@ -512,9 +534,15 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
       uint32_t v[32];
       tmem_ld32_wait(tmem + lane_base + kColDK + cg * 32, v);
       const int u0 = it * kSlots + cg * 32;
+      float* dk_q = dk_b + qd * 32 + 4 * (lane >> 2);
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (u0 + c < n_u) red_add_f32(dk_b + (long long)ulist[u0 + c] * kDI + r, __uint_as_float(v[c]));
+      for (int k = 0; k < 8; ++k) {
+        float x[4] = {__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                      __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])};
+        quad_transpose4(x);
+        const int u = u0 + 4 * k + (lane & 3);
+        if (u < n_u) red_add_v4(dk_q + (long long)ulist[u] * kDI, x[0], x[1], x[2], x[3]);
+      }
     }
     fence_before();
     if (it + 1 == ntiles) {
