@@ -16,6 +16,8 @@
 // read, and a chunk is sized to stay resident in L2 between the two kernels.
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 
@@ -439,6 +441,176 @@ __global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __res
   }
 }
 
+// Rows without document ids, a CTA of four warps per row that has more than
+// K visible blocks (a warp per row only for the rows that take all their
+// blocks): thread i holds the keys of blocks i, i+128, ..., the radix passes
+// count into a CTA-shared histogram (two, alternating, so that one is cleared
+// while the other is scanned), and the row is written in ascending block order
+// from per-warp counts.  A row's selection then takes a quarter of the
+// dependent steps of one warp walking all its keys, which matters because the
+// rows that depend on the scores all start when the score grid completes.
+// CTAs [0, light) take four rows that keep all their blocks each (ascending
+// positions, no wait unless scores are returned), the others one row with
+// more than K blocks each, heaviest first, batch elements interleaved.
+template <int PH>
+__global__ void __launch_bounds__(128) topk_select_cta_kernel(const float* __restrict__ ws,
+                                                              int32_t* __restrict__ out_idx,
+                                                              float* __restrict__ out_score,
+                                                              int t0, int nt, int b, int sq,
+                                                              int n_c, int ratio, int K) {
+  __shared__ int hist[2][256];
+  __shared__ int res[2][4];
+  __shared__ int wcount[2][4][PH];           // per (warp, key index): ties, then selected
+  const int tid = threadIdx.x, wid = tid >> 5, lane = tid & 31;
+  const unsigned FULL = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int ts = n_c <= K ? nt : min(max((K + 1) * ratio - 1 - t0, 0), nt);
+  const int n_light = b * ts, light_ctas = (n_light + 3) / 4;
+  if ((int)blockIdx.x < light_ctas) {
+    const int r0 = blockIdx.x * 4 + wid;
+    if (r0 >= n_light) return;
+    const int r = (r0 % b) * nt + r0 / b;
+    const int bi = r / nt, t = t0 + r % nt;
+    const int vis = min((t + 1) / ratio, n_c);
+    const float* row = ws + (size_t)r * n_c;
+    int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
+    float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
+    if (os) asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int s2 = lane; s2 < K; s2 += 32) {
+      oi[s2] = s2 < vis ? s2 : -1;
+      if (os) os[s2] = s2 < vis ? row[s2] : 0.f;
+    }
+    return;
+  }
+  const int h = blockIdx.x - light_ctas;
+  const int r = (h % b) * nt + (nt - 1 - h / b);
+  const int bi = r / nt, t = t0 + r % nt;
+  const int vis = min((t + 1) / ratio, n_c);         // > K
+  const float* row = ws + (size_t)r * n_c;
+  int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
+  float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
+  for (int e = tid; e < 512; e += 128) (&hist[0][0])[e] = 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  uint32_t key[PH];
+#pragma unroll
+  for (int i = 0; i < PH; ++i) {
+    const int j = tid + 128 * i;
+    key[i] = j < vis ? order_key(row[j]) : 0u;
+  }
+  __syncthreads();
+  uint32_t prefix = 0, pmask = 0;
+  int need = K;
+  bool exact = false;
+  for (int shift = 24, ps = 0; shift >= 0; shift -= 8, ps ^= 1) {
+    int* H = hist[ps];
+#pragma unroll
+    for (int i = 0; i < PH; ++i) {
+      const int j = tid + 128 * i;
+      if (j < vis && (key[i] & pmask) == prefix) atomicAdd(&H[(key[i] >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (wid == 0) {
+      // bins in descending order: lane l scans bins 8(31-l)+7 .. 8(31-l)
+      int cnt[8];
+      int tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = H[8 * (31 - lane) + 7 - i];
+        tot += cnt[i];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int excl = incl - tot;
+      if (excl < need && need <= incl) {              // exactly one lane
+        int run = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (run + cnt[i] >= need) {
+            res[ps][0] = 8 * (31 - lane) + 7 - i;
+            res[ps][1] = run;
+            res[ps][2] = cnt[i];
+            break;
+          }
+          run += cnt[i];
+        }
+      }
+    } else if (wid == 1) {
+      // the other histogram (last read by the previous pass's scan) for the next pass
+      for (int e = lane; e < 256; e += 32) hist[ps ^ 1][e] = 0;
+    }
+    __syncthreads();
+    const int bin = res[ps][0], above = res[ps][1], inbin = res[ps][2];
+    need -= above;
+    prefix |= (uint32_t)bin << shift;
+    pmask |= 255u << shift;
+    if (inbin == need) {
+      exact = true;
+      break;
+    }
+  }
+  // selection in ascending block order j = 128 i + 32 wid + lane
+  bool sel[PH];
+  if (exact) {
+#pragma unroll
+    for (int i = 0; i < PH; ++i)
+      sel[i] = tid + 128 * i < vis && (key[i] & pmask) >= prefix;
+  } else {
+    // the threshold key's `need` lowest-index copies are taken
+    unsigned eqm[PH];
+#pragma unroll
+    for (int i = 0; i < PH; ++i) {
+      const bool eq = tid + 128 * i < vis && key[i] == prefix;
+      eqm[i] = __ballot_sync(FULL, eq);
+      if (lane == 0) wcount[0][wid][i] = __popc(eqm[i]);
+    }
+    __syncthreads();
+    int run = 0;
+#pragma unroll
+    for (int i = 0; i < PH; ++i) {
+      int before = 0, tot = 0;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int c = wcount[0][w][i];
+        before += w < wid ? c : 0;
+        tot += c;
+      }
+      const bool valid = tid + 128 * i < vis;
+      const bool eq = (eqm[i] >> lane) & 1u;
+      sel[i] = (valid && key[i] > prefix) || (eq && run + before + __popc(eqm[i] & lt_mask) < need);
+      run += tot;
+    }
+  }
+  unsigned selm[PH];
+#pragma unroll
+  for (int i = 0; i < PH; ++i) {
+    selm[i] = __ballot_sync(FULL, sel[i]);
+    if (lane == 0) wcount[1][wid][i] = __popc(selm[i]);
+  }
+  __syncthreads();
+  int run = 0;
+#pragma unroll
+  for (int i = 0; i < PH; ++i) {
+    int before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int c = wcount[1][w][i];
+      before += w < wid ? c : 0;
+      tot += c;
+    }
+    const int pos = run + before + __popc(selm[i] & lt_mask);
+    if (sel[i] && pos < K) {
+      const int j = tid + 128 * i;
+      oi[pos] = j;
+      if (os) os[pos] = row[j];
+    }
+    run += tot;
+  }
+}
+
 cudaError_t launch_indexer_scores_simt(const void* q_idx, const void* k_idx, const float* w,
                                        float* ws, int t0, int nt, int b, int sq, int n_c, int H_I,
                                        int d_I, int ratio, bool bf16, cudaStream_t s) {
@@ -527,6 +699,23 @@ cudaError_t launch_topk_select(const float* ws, int32_t* topk_idx, float* topk_s
                                int nt, int b, int sq, int n_c, int ratio, int K, cudaStream_t s,
                                const int32_t* doc) {
   const int rows = b * nt;
+  if (doc == nullptr && n_c <= 2048) {
+    const int ts = n_c <= K ? nt : std::min(std::max((K + 1) * ratio - 1 - t0, 0), nt);
+    const unsigned grid = (unsigned)((b * ts + 3) / 4 + b * (nt - ts));
+#define CSA_SELC(P)                                                                           \
+  {                                                                                           \
+    cudaError_t e_ = launch_dependent(topk_select_cta_kernel<P>, grid, 128, 0, s, ws, topk_idx,\
+                                      topk_score, t0, nt, b, sq, n_c, ratio, K);              \
+    if (e_ != cudaSuccess) return e_;                                                         \
+    count_launches(1);                                                                        \
+  }
+    if (n_c <= 256) { CSA_SELC(2) }
+    else if (n_c <= 512) { CSA_SELC(4) }
+    else if (n_c <= 1024) { CSA_SELC(8) }
+    else { CSA_SELC(16) }
+#undef CSA_SELC
+    return cudaGetLastError();
+  }
   if (n_c <= 2048) {
     const unsigned grid = (unsigned)((rows + 3) / 4);   // 4 rows (warps) per CTA
 #define CSA_SEL(P)                                                                            \
