@@ -231,6 +231,21 @@ def test_indexer_wide_rows_sampled(dtype, case):
     assert n_exact >= len(rows) // 2       # most rows are held to the exact set
 
 
+@pytest.mark.parametrize("case", [
+    dict(sq=480, ratio=1, topk=40),      # 256 < n_c <= 512: four keys per thread
+    dict(sq=1600, ratio=1, topk=300),    # 1024 < n_c <= 2048: sixteen keys per thread
+    dict(sq=1030, ratio=1, topk=1000),   # K close to n_c: few rows above K blocks
+])
+def test_indexer_select_cta_rows_with_ties(case):
+    """Every row of layers whose rows above K visible blocks take a CTA each
+    (duplicated key rows and ReLU zeros give exact ties at the K-th score),
+    with the scores returned and without."""
+    q_I, k_I, w = _indexer_case(12, 1, case["sq"], 2, 64, case["ratio"], "bf16", ties=True)
+    idx, _ = _check_indexer(q_I, k_I, w, case["topk"], case["ratio"])
+    plain = csa.csa_indexer_topk(q_I.cuda(), k_I.cuda(), w.cuda(), case["topk"], case["ratio"])
+    assert np.array_equal(plain.cpu().numpy(), idx)
+
+
 def test_indexer_chunked_workspace_identical():
     q_I, k_I, w = _indexer_case(7, 2, 1000, 4, 128, 4, "bf16")
     full, sc_full = _check_indexer(q_I, k_I, w, 96, 4)
