@@ -22,11 +22,18 @@
 //   X^T [slots, rows]  = K [slots, d] . Q^T            (dots; K-major A and B)
 //   dQ^T [d, rows]    += K^T [d, slots] . G^T           (A = K and B = G MN-major)
 //   dK^T [d, slots]    = Q^T [d, rows] . G [rows, slots] (A = Q MN-major, B = G K-major)
-// TMEM: two 128-column X^T buffers, dQ^T and the tile's dK^T.  G carries bf16
-// hi + lo parts (about 16 significant bits).  Pass A forms I for every union
-// entry (one CTA-wide softmax per query follows); pass B recomputes X^T per
-// tile, forms G and dw, and adds the tile's dK^T columns into dk_I with fp32
-// reductions, a warp covering 128 contiguous bytes of one block row.
+// G carries bf16 hi + lo parts (about 16 significant bits).  Pass A forms X^T
+// and I for every union entry (two 128-column X^T buffers in TMEM) and keeps
+// the sign of every dot, one bit per (entry, row), in TMEM; one CTA-wide
+// softmax per query follows.  Pass B needs no dots: G comes from the sign
+// bits, dI and w; dQ^T accumulates in TMEM and dK^T alternates between the
+// two former X^T buffers, so a tile's dK^T columns are added into dk_I (fp32
+// vector reductions, four block rows of 128 bytes per warp instruction) while
+// the tensor core forms the next tile's products.  dw needs the dots' values:
+//   dw[t,h] = sum_s dI[s] [dot > 0] (q_I[t,h] . k_I[j_s]) = q_I[t,h] . dq_I[t,h] / w[t,h],
+// formed from dQ^T and the Q rows at the end (a row whose |w| is below 2^-60
+// takes G with weight 1 instead, its dq_I scaled by w afterwards, and its Q
+// row zeroed for the dK^T product).
 #include "csa_common.cuh"
 #include "csa_kernels.h"
 #include "tcgen05.cuh"
@@ -44,9 +51,11 @@ constexpr int kRows = 128;                      // (query, head) rows: QB x H_I
 constexpr int kSlots = 128;                     // union entries per tile
 constexpr int kThreads = 512;                   // 16 warps: TMEM lane quarter x column quarter
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: X^T buffers of 128 at 0 and 128 (pass A: four, over all 512),
-// dQ^T at 256, the tile's dK^T at 384
-constexpr uint32_t kColDQ = 256, kColDK = 384;
+// TMEM columns: pass A's X^T buffers (pass B: dK^T buffers) of 128 at 0 and
+// 128, dQ^T at 256, the sign bits at 384 (four columns per tile: at most 32
+// tiles, i.e. n_c <= 4096)
+constexpr uint32_t kColDQ = 256, kColMask = 384;
+constexpr float kTinyW = 8.673617379884035e-19f;   // 2^-60
 constexpr uint32_t kBlk = 128 * 128;            // 16 KB: 128 lines of 128 B
 
 struct Layout {
@@ -62,7 +71,8 @@ struct Layout {
   static constexpr uint32_t QST = RED + 2048;   // [4][8] floats: per-query statistics
   static constexpr uint32_t SCR = QST + 128;    // [16][12] floats: block reductions
   static constexpr uint32_t WSUM = SCR + 768;   // [16] ints
-  static constexpr uint32_t DYN = WSUM + 64;    // cnt, ulist, I/dI, T
+  static constexpr uint32_t WG = WSUM + 64;     // [128] floats: G's weight per row
+  static constexpr uint32_t DYN = WG + 512;     // cnt, ulist, I/dI, T
 };
 // per-query statistics in QST[q * 8 + k]
 constexpr int kStS = 0, kStA = 1, kStLoss = 2, kStN = 3;
@@ -158,8 +168,9 @@ __device__ __forceinline__ void quad_transpose4(float (&x)[4]) {
 
 template <int QB>
 __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
-    const __grid_constant__ CUtensorMap tmap_q, const __nv_bfloat16* __restrict__ k_I,
-    const float* __restrict__ w, const int32_t* __restrict__ idx,
+    const __grid_constant__ CUtensorMap tmap_q, const __nv_bfloat16* __restrict__ q_I,
+    const __nv_bfloat16* __restrict__ k_I, const float* __restrict__ w,
+    const int32_t* __restrict__ idx,
     const float* __restrict__ target, float* __restrict__ loss, float* __restrict__ dq_I,
     float* __restrict__ dk_I, float* __restrict__ dw, int sq, int n_c, int ratio, int K,
     int* __restrict__ status) {
@@ -170,13 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + Layout::BARS);
-  uint64_t* bar_x = bar_q + 1;                  // [4] pass-A X^T buffers
-  uint64_t* bar_s = bar_q + 5;                  // [2] pass-B X^T buffers
-  uint64_t* bar_dq = bar_q + 7;                 // pass-B dQ^T MMAs
-  uint64_t* bar_dk = bar_q + 8;                 // pass-B dQ^T and dK^T MMAs
+  uint64_t* bar_x = bar_q + 1;                  // [2] pass-A X^T buffers
+  uint64_t* bar_dk = bar_q + 3;                 // pass-B dQ^T and dK^T MMAs of a tile
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Layout::TSLOT);
   int* scal = reinterpret_cast<int*>(sm + Layout::SCAL);
   float* wr = reinterpret_cast<float*>(sm + Layout::W);
+  float* wg = reinterpret_cast<float*>(sm + Layout::WG);
   float* red = reinterpret_cast<float*>(sm + Layout::RED);
   float* qst = reinterpret_cast<float*>(sm + Layout::QST);
   float* scr = reinterpret_cast<float*>(sm + Layout::SCR);
@@ -198,9 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
   // ---- set-up: barriers, TMEM, Q tile, head weights ----------------------------
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&bar_x[i], 1);
-    for (int i = 0; i < 2; ++i) mbar_init(&bar_s[i], 1);
-    mbar_init(bar_dq, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&bar_x[i], 1);
     mbar_init(bar_dk, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -311,8 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
   };
 
   // ---- pass A: I for every union entry, with a running (max, sum) per query --------
-  // Four KV buffers and four X^T buffers (all 512 TMEM columns; dQ^T and dK^T
-  // are not live yet): tile it+3 is gathered while tile it is reduced.
+  // Four KV buffers (tile it+3 is gathered while tile it is reduced) and two
+  // X^T buffers (tile it+1's product runs while tile it is reduced); each
+  // thread keeps the signs of its 32 dots of the tile in one TMEM word.
   float m_run[QB], z_run[QB];
 #pragma unroll
   for (int q = 0; q < QB; ++q) {
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
       __syncthreads();
       if (tid == 0) {
         fence_after();
-        issue_x((it + 1) & 3, ((it + 1) & 3) * 128, &bar_x[(it + 1) & 3]);
+        issue_x((it + 1) & 3, ((it + 1) & 1) * 128, &bar_x[(it + 1) & 1]);
       }
     } else {
       __syncthreads();     // the previous tile's combine has read `red`
@@ -349,22 +358,28 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
     // per-warp wait: a warp scores its columns as soon as X^T is there, not
     // after the issuing thread has handed the next tile's product over (the
     // barrier below carries a failed wait to every thread)
-    ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[it & 3], (it >> 2) & 1));
+    ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[it & 1], (it >> 1) & 1));
     if (ok) {
       fence_after();
       uint32_t v[32];
-      tmem_ld32_wait(tmem + lane_base + (it & 3) * 128 + cg * 32, v);
+      tmem_ld32_wait(tmem + lane_base + (it & 1) * 128 + cg * 32, v);
       const float4* w4 = reinterpret_cast<const float4*>(wr + cg * 32);
       float part = 0.f;
+      uint32_t signs = 0u;
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 wv = w4[c4];
-        part = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * c4]), 0.f), part);
-        part = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * c4 + 1]), 0.f), part);
-        part = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * c4 + 2]), 0.f), part);
-        part = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * c4 + 3]), 0.f), part);
+        const float x0 = __uint_as_float(v[4 * c4]), x1 = __uint_as_float(v[4 * c4 + 1]);
+        const float x2 = __uint_as_float(v[4 * c4 + 2]), x3 = __uint_as_float(v[4 * c4 + 3]);
+        part = fmaf(wv.x, fmaxf(x0, 0.f), part);
+        part = fmaf(wv.y, fmaxf(x1, 0.f), part);
+        part = fmaf(wv.z, fmaxf(x2, 0.f), part);
+        part = fmaf(wv.w, fmaxf(x3, 0.f), part);
+        signs |= ((x0 > 0.f ? 1u : 0u) | (x1 > 0.f ? 2u : 0u) | (x2 > 0.f ? 4u : 0u) |
+                  (x3 > 0.f ? 8u : 0u)) << (4 * c4);
       }
       red[cg * kRows + r] = part;
+      tmem_st1(tmem + lane_base + kColMask + it * 4 + cg, signs);
     }
     fence_before();
     ok = __syncthreads_and(ok);
@@ -429,68 +444,80 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
   }
   __syncthreads();
 
-  // ---- pass B: X^T again, G and dw, dQ^T += K^T G^T, dK^T = Q^T G --------------------
-  float dwp[32];
+  // ---- pass B: G from the signs, dQ^T += K^T G^T, dK^T = Q^T G ------------------------
+  // G's weight per row: w, or 1 where |w| < 2^-60 (there the Q row is zeroed,
+  // so that the row adds nothing to dK^T, and dq_I is scaled by w at the end)
+  tmem_wait_st();                                     // the sign words are in TMEM
+  if (tid < kRows) {
+    const bool tiny = fabsf(wr[tid]) < kTinyW;
+    wg[tid] = tiny ? 1.f : wr[tid];
+    if (tiny) {
 #pragma unroll
-  for (int c = 0; c < 32; ++c) dwp[c] = 0.f;
+      for (int ch = 0; ch < 16; ++ch)
+        *reinterpret_cast<uint4*>(sm + Layout::Q + sw_off(tid, ch)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // dK^T of tile it drained from TMEM (buffer it & 1): quad transposes give
+  // lane 4a+b four consecutive d of slot 4k+b, so each vector reduction of a
+  // warp covers 128 contiguous bytes of four block rows
+  auto drain_dk = [&](int it) {
+    uint32_t v[32];
+    tmem_ld32_wait(tmem + lane_base + (uint32_t)(it & 1) * 128 + cg * 32, v);
+    const int u0 = it * kSlots + cg * 32;
+    float* dk_q = dk_b + qd * 32 + 4 * (lane >> 2);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float x[4] = {__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                    __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])};
+      quad_transpose4(x);
+      const int u = u0 + 4 * k + (lane & 3);
+      if (u < n_u) red_add_v4(dk_q + (long long)ulist[u] * kDI, x[0], x[1], x[2], x[3]);
+    }
+  };
   bool fail = false;                                 // a per-warp wait of this thread gave up
   if (ok && ntiles > 0) {
     stage(0, 0);
-    if (ntiles > 1) {
-      stage(1, 1);
-      cp_wait<1>();
-    } else {
-      cp_wait<0>();
-    }
-    fence_proxy_async_smem();
-    fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      fence_after();
-      issue_x(0, 0, &bar_s[0]);
-    }
+    if (ntiles > 1) stage(1, 1);
   }
   for (int it = 0; it < ntiles && ok; ++it) {
-    // per-warp wait (the barrier below carries a failed wait, or one of the
-    // previous tile's product waits, to every thread)
-    ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[it & 1], (it >> 1) & 1) && !fail);
-    if (ok) {
+    // tile it-1's products are complete: G and KV buffer (it+1) & 1 are free
+    if (it > 0) {
+      const bool k_ok = __all_sync(0xffffffffu, mbar_wait(bar_dk, (it - 1) & 1));
+      fail |= !k_ok;
+      if (k_ok && it + 1 < ntiles) stage(it + 1, (it + 1) & 1);
+    }
+    if (!fail) {
       fence_after();
+      const uint32_t signs = tmem_ld1_wait(tmem + lane_base + kColMask + it * 4 + cg);
       const int u = it * kSlots + r;
       const float dI = u < n_u ? Iu[myq * n_c + u] : 0.f;
-      uint32_t v[32];
-      tmem_ld32_wait(tmem + lane_base + (it & 1) * 128 + cg * 32, v);
-      const float4* w4 = reinterpret_cast<const float4*>(wr + cg * 32);
+      const float4* w4 = reinterpret_cast<const float4*>(wg + cg * 32);
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         const float4 wa = w4[2 * c8], wb = w4[2 * c8 + 1];
         const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
         float g[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = c8 * 8 + e;
-          const float x = __uint_as_float(v[c]);
-          g[e] = x > 0.f ? dI * wv[e] : 0.f;
-          dwp[c] = fmaf(dI, fmaxf(x, 0.f), dwp[c]);
-        }
+        for (int e = 0; e < 8; ++e) g[e] = (signs >> (c8 * 8 + e)) & 1u ? dI * wv[e] : 0.f;
         store_hi_lo8(GH, GL, sw_off(r, cg * 4 + c8), g);
       }
     }
-    if (it + 1 < ntiles) cp_wait<0>();              // tile it+1's rows
+    // tile it's rows (tile it+1's, staged above, may still be in flight)
+    if (it + 1 < ntiles) cp_wait<1>();
+    else cp_wait<0>();
     fence_proxy_async_smem();
     fence_before();
-    ok = __syncthreads_and(ok);
-    if (!ok) { site = kSiteLossX; break; }
+    ok = __syncthreads_and(!fail);
+    if (!ok) { site = kSiteLossG; break; }
     if (tid == 0) {
       fence_after();
       const uint32_t ga = smem_addr(GH), la = smem_addr(GL);
       const uint32_t ka = smem_addr(sm + Layout::KV + (it & 1) * 2 * kBlk);
       const uint32_t qa = smem_addr(sm + Layout::Q);
       // dQ^T [d, rows] += K^T [d, slots] G^T [slots, rows]: A = K tile and B = G
-      // read MN-major (16 slot lines per K step); committed first, so that
-      // the KV buffer is refilled early.  (G's lo part is needed here too: a
-      // peaked student softmax leaves one slot with |G| near |w|, whose bf16
-      // rounding alone moved dq_I by 1e-2.)
+      // read MN-major (16 slot lines per K step).  (G's lo part is needed here
+      // too: a peaked student softmax leaves one slot with |G| near |w|, whose
+      // bf16 rounding alone moved dq_I by 1e-2.)
       constexpr uint32_t idesc_q = idesc_bf16_f32_major(kDI, kRows, 1, 1);
 #pragma unroll
       for (int k = 0; k < kSlots / 16; ++k) {
@@ -499,69 +526,61 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
                     (it > 0 || k > 0) ? 1u : 0u);
         mma_bf16_ss(tmem + kColDQ, a, sw128_desc_mn(la + k * 2048, kBlk), idesc_q, 1u);
       }
-      mma_commit(bar_dq);
-      // dK^T [d, slots] = Q^T [d, rows] G [rows, slots]: A = Q read MN-major, B =
-      // G read K-major (its slot lines hold the rows contiguously); the TMEM
-      // lane is then d, so a warp adds 32 consecutive floats of a block row
+      // dK^T [d, slots] = Q^T [d, rows] G [rows, slots] into buffer it & 1: A = Q
+      // read MN-major, B = G read K-major (its slot lines hold the rows
+      // contiguously); the TMEM lane is then d
       constexpr uint32_t idesc_k = idesc_bf16_f32_major(kDI, kSlots, 1, 0);
+      const uint32_t col_k = (uint32_t)(it & 1) * 128;
 #pragma unroll
       for (int k = 0; k < kRows / 16; ++k) {
         const uint32_t boff = (k >> 2) * kBlk + (k & 3) * 32;
         const uint64_t aq = sw128_desc_mn(qa + k * 2048, kBlk);
-        mma_bf16_ss(tmem + kColDK, aq, sw128_desc(ga + boff), idesc_k, k > 0 ? 1u : 0u);
-        mma_bf16_ss(tmem + kColDK, aq, sw128_desc(la + boff), idesc_k, 1u);
+        mma_bf16_ss(tmem + col_k, aq, sw128_desc(ga + boff), idesc_k, k > 0 ? 1u : 0u);
+        mma_bf16_ss(tmem + col_k, aq, sw128_desc(la + boff), idesc_k, 1u);
       }
       mma_commit(bar_dk);
-      // the next tile's X^T runs behind these products (its commit also
-      // covers them: G is free once it has completed)
-      if (it + 1 < ntiles) issue_x((it + 1) & 1, ((it + 1) & 1) * 128, &bar_s[(it + 1) & 1]);
     }
-    // Every warp goes on as soon as the product it needs is complete (warp 0
-    // once its thread 0 has issued them); a wait that gives up is carried to
-    // the next CTA-wide wait.  dQ^T done: KV buffer (it & 1) takes tile it+2.
-    const bool dq_ok = mbar_wait(bar_dq, it & 1);
-    fail |= !dq_ok;
-    if (dq_ok && it + 2 < ntiles) stage(it + 2, it & 1);
-    // dK done: thread (d = its TMEM lane) reads its 32 slot columns from
-    // TMEM; quad transposes give lane 4a+b four consecutive d of slot 4k+b,
-    // so each vector reduction of a warp covers 128 contiguous bytes of four
-    // block rows (a quarter of the reduction instructions of one scalar per
-    // column), while the tensor core forms X^T
-    const bool dk_ok = __all_sync(0xffffffffu, mbar_wait(bar_dk, it & 1));
-    fail |= !dk_ok;
-    if (dk_ok) {
-      fence_after();
-      uint32_t v[32];
-      tmem_ld32_wait(tmem + lane_base + kColDK + cg * 32, v);
-      const int u0 = it * kSlots + cg * 32;
-      float* dk_q = dk_b + qd * 32 + 4 * (lane >> 2);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float x[4] = {__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                      __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])};
-        quad_transpose4(x);
-        const int u = u0 + 4 * k + (lane & 3);
-        if (u < n_u) red_add_v4(dk_q + (long long)ulist[u] * kDI, x[0], x[1], x[2], x[3]);
-      }
-    }
+    // the previous tile's dK^T is added into dk_I while the tensor core forms
+    // this tile's products
+    if (it > 0) drain_dk(it - 1);
     fence_before();
-    if (it + 1 == ntiles) {
-      // after the last tile: every product complete before the epilogue
-      ok = __syncthreads_and(mbar_wait(bar_dk, it & 1) && !fail);
-      if (!ok) site = kSiteLossG;
+  }
+  if (ok && ntiles > 0) {
+    // the last tile's products: then its dK^T, and dQ^T is complete
+    const bool k_ok = __all_sync(0xffffffffu, mbar_wait(bar_dk, (ntiles - 1) & 1));
+    if (k_ok) {
+      fence_after();
+      drain_dk(ntiles - 1);
     }
+    ok = __syncthreads_and(k_ok);
+    if (!ok) site = kSiteLossG;
   }
   cp_async_wait_all_();                               // no copy in flight past this point
   if (!ok && tid == 0) set_status(status, kDevTimeout, site);
 
-  // ---- epilogue: dw (a sum over the slot lanes), dq_I rows, loss ----------------------
-  {
+  // ---- epilogue: dq_I rows and dw = q_I . dq_I / w, from dQ^T; loss ---------------------
+  // thread (d = its TMEM lane, 32 rows): dQ^T[d][rows] and q_I[rows][d]
+  uint32_t v[32];
+  if (ok) {
+    fence_after();
+    if (ntiles > 0) {
+      tmem_ld32_wait(tmem + lane_base + kColDQ + cg * 32, v);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) v[c] = 0u;
+    }
+    const long long qrow0 = ((long long)bi * sq + t0) * H_I;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
-      float v16[16];
+      float p16[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) v16[c] = dwp[h2 * 16 + c];
-      const float s = lane_transpose_sum16(v16);
+      for (int c = 0; c < 16; ++c) {
+        const int row = cg * 32 + h2 * 16 + c;
+        const bool live = t0 + row / H_I < sq;
+        const float qv = live ? __bfloat162float(q_I[(qrow0 + row) * kDI + r]) : 0.f;
+        p16[c] = qv * __uint_as_float(v[h2 * 16 + c]);
+      }
+      const float s = lane_transpose_sum16(p16);
       if (lane < 16) red[qd * kRows + cg * 32 + h2 * 16 + lane] = s;
     }
   }
@@ -570,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
     const int q = tid / H_I, t = t0 + q;
     if (t < sq) {
       const float s = (red[tid] + red[kRows + tid]) + (red[2 * kRows + tid] + red[3 * kRows + tid]);
-      dw[((long long)bi * sq + t) * H_I + tid % H_I] = s;
+      dw[((long long)bi * sq + t) * H_I + tid % H_I] = s / wg[tid];
       if (tid % H_I == 0) loss[(long long)bi * sq + t] = qst[q * 8 + kStLoss];
     }
   }
@@ -578,17 +597,13 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
   // then one bulk copy of the block's contiguous rows instead of plain
   // stores queued behind the dk_I reductions
   if (ok) {
-    fence_after();
-    uint32_t v[32];
-    if (ntiles > 0) {
-      tmem_ld32_wait(tmem + lane_base + kColDQ + cg * 32, v);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 32; ++c) v[c] = 0u;
-    }
     float* stg = reinterpret_cast<float*>(GH);       // [128 rows][128 d] fp32 = 64 KB
 #pragma unroll
-    for (int c = 0; c < 32; ++c) stg[(cg * 32 + c) * kDI + r] = __uint_as_float(v[c]);
+    for (int c = 0; c < 32; ++c) {
+      const int row = cg * 32 + c;
+      const float g = __uint_as_float(v[c]);
+      stg[row * kDI + r] = wg[row] == wr[row] ? g : g * wr[row];
+    }
     fence_proxy_async_smem();
   }
   fence_before();
@@ -632,6 +647,7 @@ size_t indexer_loss_tc_smem(int QB, int n_c) {
 bool indexer_loss_tc_supported(int H_I, int d_I, int n_c) {
   if (d_I != ilt::kDI || !(H_I == 32 || H_I == 64)) return false;
   if (encode_fn_loss() == nullptr) return false;
+  if (n_c > 4096) return false;                 // 32 tiles of sign words in TMEM
   return indexer_loss_tc_smem(ilt::kRows / H_I, n_c) <= 227 * 1024;
 }
 
@@ -660,7 +676,8 @@ cudaError_t launch_indexer_loss_tc(const void* q_I, const void* k_I, const float
     auto k = ilt::indexer_loss_tc_kernel<QQ>;                                                 \
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);     \
     if (e != cudaSuccess) return e;                                                           \
-    k<<<grid, ilt::kThreads, smem, s>>>(tq, (const __nv_bfloat16*)k_I, w, idx, target, loss,  \
+    k<<<grid, ilt::kThreads, smem, s>>>(tq, (const __nv_bfloat16*)q_I,                        \
+                                        (const __nv_bfloat16*)k_I, w, idx, target, loss,      \
                                         dq_I, dk_I, dw, sq, n_c, ratio, K, status);           \
     count_launches(1);                                                                        \
   }

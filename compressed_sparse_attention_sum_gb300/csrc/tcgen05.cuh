@@ -210,6 +210,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// One 32-bit column per lane of the warp's lane quarter (32x32b.x1): store,
+// and load with the wait that makes the value usable (the register is an
+// operand of the wait, so no use of it is moved above).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t tmem_ld1_wait(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v)::"memory");
+  return v;
+}
 
 // 16 consecutive 32-bit TMEM columns of this thread's lane, with the wait.
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {

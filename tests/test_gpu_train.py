@@ -192,6 +192,28 @@ def test_loss_tensor_core_shapes(H_I, sq, ratio, K, b):
     assert torch.all(dq[:, 5] == 0) and torch.all(dw[:, 5] == 0) and torch.all(loss[:, 5] == 0)
 
 
+@pytest.mark.parametrize("H_I", [32, 64])
+def test_loss_tensor_core_zero_and_tiny_head_weights(H_I):
+    """Head weights that are exactly zero or below 2^-60: the tcgen05 kernel
+    forms dw from its dq_I products divided by w, so those rows take the
+    weight-1 products and a zeroed Q row instead (dw from the same products,
+    dq_I scaled by w, nothing added to dk_I)."""
+    b, sq, ratio, K, d_I = 2, 150, 2, 40, 128
+    g = torch.Generator().manual_seed(77 + H_I)
+    n_c = sq // ratio
+    q_I = torch.randn(b, sq, H_I, d_I, generator=g).to(torch.bfloat16)
+    k_I = torch.randn(b, n_c, d_I, generator=g).to(torch.bfloat16)
+    w = torch.randn(b, sq, H_I, generator=g) * 0.5
+    w[:, :, 3] = 0.0                          # one head without weight everywhere
+    w[:, 40:60, 5] = 1e-30                    # below 2^-60
+    w[0, 90, :] = 0.0                         # a query whose heads all weigh nothing
+    w[1, 100, 7] = -3e-19                     # just below 2^-60 in magnitude
+    idx = _messy_idx(g, b, sq, n_c, K)
+    target = torch.rand(b, sq, K, generator=g)
+    target = target / target.sum(-1, keepdim=True).clamp_min(1e-30)
+    _check_loss(q_I, k_I, w, idx, target, ratio, "bf16")
+
+
 @pytest.mark.parametrize("name", ["debug_bf16", "csa4_bf16"])
 def test_loss_layer_with_teacher(name):
     """The workload's indexer inputs and top-k, the oracle's teacher as the
