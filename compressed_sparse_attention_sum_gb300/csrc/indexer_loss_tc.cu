@@ -460,19 +460,28 @@ __global__ void __launch_bounds__(kThreads, 1) indexer_loss_tc_kernel(
   // dK^T of tile it drained from TMEM (buffer it & 1): quad transposes give
   // lane 4a+b four consecutive d of slot 4k+b, so each vector reduction of a
   // warp covers 128 contiguous bytes of four block rows
-  auto drain_dk = [&](int it) {
+  // Warp 0's thread 0 issues the products and is held until the tensor core
+  // has taken them, so warp 0 drains nothing: the other three warps of its
+  // lane quarter (column groups 1-3) share its eight 4-column blocks.
+  auto drain_cols = [&](int it, int cgs, uint32_t blocks) {
     uint32_t v[32];
-    tmem_ld32_wait(tmem + lane_base + (uint32_t)(it & 1) * 128 + cg * 32, v);
-    const int u0 = it * kSlots + cg * 32;
+    tmem_ld32_wait(tmem + lane_base + (uint32_t)(it & 1) * 128 + cgs * 32, v);
+    const int u0 = it * kSlots + cgs * 32;
     float* dk_q = dk_b + qd * 32 + 4 * (lane >> 2);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
+      if (!((blocks >> k) & 1u)) continue;
       float x[4] = {__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
                     __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])};
       quad_transpose4(x);
       const int u = u0 + 4 * k + (lane & 3);
       if (u < n_u) red_add_v4(dk_q + (long long)ulist[u] * kDI, x[0], x[1], x[2], x[3]);
     }
+  };
+  auto drain_dk = [&](int it) {
+    if (warp == 0) return;
+    drain_cols(it, cg, 0xFFu);
+    if (qd == 0) drain_cols(it, 0, cg == 1 ? 0x07u : cg == 2 ? 0x38u : 0xC0u);
   };
   bool fail = false;                                 // a per-warp wait of this thread gave up
   if (ok && ntiles > 0) {
