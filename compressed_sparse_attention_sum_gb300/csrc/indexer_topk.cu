@@ -314,9 +314,11 @@ __global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __res
   int32_t* oi = out_idx + ((size_t)bi * sq + t) * K;
   float* os = out_score ? out_score + ((size_t)bi * sq + t) * K : nullptr;
   // the score grid's output is read only where the selection depends on it
-  // or the scores are returned (every thread of the warp decides alike)
-  const bool scored = vis > K || os != nullptr;
-  if (scored) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // or the scores are returned (every thread of the warp decides alike); with
+  // document ids that is known only from the candidates' count, which needs
+  // the ids alone (an input, not the score grid's output)
+  bool scored = vis > K || os != nullptr;
+  if (!DOC && scored) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!DOC && vis <= K) {
     for (int s = lane; s < K; s += 32) {
       oi[s] = s < vis ? s : -1;
@@ -332,11 +334,20 @@ __global__ void __launch_bounds__(128) topk_select_reg_kernel(const float* __res
   for (int i = 0; i < PER; ++i) {
     const int j = lane + 32 * i;
     const bool ok = j < vis && (!DOC || __ldg(docb + (size_t)j * ratio) == dt);
-    // 0: not a candidate; unscored rows (ncand <= vis <= K) only mark them
-    key[i] = ok ? (scored ? order_key(row[j]) : 1u) : 0u;
+    key[i] = ok ? 1u : 0u;                             // 0: not a candidate
     ncand += ok;
   }
-  if (DOC) ncand = __reduce_add_sync(FULL, ncand);
+  if (DOC) {
+    ncand = __reduce_add_sync(FULL, ncand);
+    scored = ncand > K || os != nullptr;
+    if (scored) asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
+  if (scored) {
+    // unscored rows (ncand <= K) only mark their candidates
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (key[i] != 0u) key[i] = order_key(row[lane + 32 * i]);
+  }
   if (DOC && ncand <= K) {
     // blocks l, l+32, ...: fetch the key of block j from its owner lane
     int out_pos = 0;
